@@ -1,0 +1,349 @@
+"""Pins for the CPU oracle, checked against things other than the oracle itself.
+
+Each test ties an oracle function to an independent fact: numpy's IEEE
+binary16 conversion, exact rational arithmetic (``fractions.Fraction``), a
+closed form, an invariant proved from the definition, a library matmul, or a
+value derived by hand in ``tests/golden/``. None of them calls the CUDA path.
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _f16(vals) -> np.ndarray:
+    a = np.asarray(vals, dtype=np.float64).astype(np.float16)
+    assert (a.astype(np.float64) == np.asarray(vals, dtype=np.float64)).all(), "fixture value not exact fp16"
+    return a
+
+
+def _fr(h) -> Fraction:
+    return Fraction(float(np.float16(h)))
+
+
+def _val_bits(b: int) -> Fraction:
+    return Fraction(float(np.uint16(b).view(np.float16)))
+
+
+# --------------------------------------------------------------------------- fp16
+
+
+def test_half_decode_matches_numpy_for_every_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+    # signed zeros keep their sign
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0])
+
+
+def test_half_encode_matches_numpy_rne():
+    rng = np.random.default_rng(123)
+    vals = [0.0, -0.0, 65504.0, 65519.999, 65520.0, -65520.0, 1e6, 2.0**-24, 2.0**-25,
+            3 * 2.0**-26, 2.0**-14, 2.0**-14 - 2.0**-25, 1.0 + 2.0**-11, 1.0 + 3 * 2.0**-11]
+    mags = np.exp2(rng.uniform(-30, 17, 4000)) * rng.choice([-1.0, 1.0], 4000)
+    vals += list(mags)
+    # exact midpoints between neighbouring fp16 values (ties), and points next to them
+    h = rng.integers(0, 0x7BFF, 3000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2  # exact in fp64
+    vals += list(mid) + list(np.nextafter(mid, 0)) + list(np.nextafter(mid, np.inf)) + list(-mid)
+    vals = np.array(vals, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.double_to_half(v) for v in vals], dtype=np.uint16)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(vals[i], hex(got[i]), hex(ref[i])) for i in bad[:5]]
+
+
+# ----------------------------------------------------------------------- quantize
+
+
+def _smallest_f16_at_least(r: Fraction) -> int:
+    """Exact: the least positive fp16 (bits) whose value is >= r."""
+    b = int(np.float16(float(r)).view(np.uint16)) & 0x7FFF
+    while _val_bits(b) < r:
+        b += 1
+    while b > 0 and _val_bits(b - 1) >= r:
+        b -= 1
+    return b
+
+
+def _quantize_exact(w: list[Fraction], K: int, g: int):
+    """The quantization definition in exact rational arithmetic (an independent formulation:
+    s is 'r/15 rounded up to fp16', Python's round() is round-half-even on Fractions)."""
+    G = -(-K // g)
+    q, s, z = [0] * K, [0] * G, [0] * G
+    for j in range(G):
+        grp = w[j * g:min((j + 1) * g, K)]
+        lo, hi = min([Fraction(0)] + grp), max([Fraction(0)] + grp)
+        r = hi - lo
+        if r == 0:
+            s[j], z[j] = 0x3C00, 0
+            continue
+        sb = _smallest_f16_at_least(r / 15)
+        sv = _val_bits(sb)
+        zj = min(15, max(0, round(-lo / sv)))
+        s[j], z[j] = sb, zj
+        for i, wk in enumerate(grp):
+            q[j * g + i] = min(15, max(0, round(wk / sv) + zj))
+    return q, s, z
+
+
+@pytest.mark.parametrize("K,g,seed", [(8, 8, 0), (40, 16, 1), (24, 8, 2), (100, 32, 3), (288, 256, 4),
+                                     (129, 64, 5), (7, 8, 6)])
+def test_quantize_equals_exact_rational_definition(K, g, seed):
+    rng = np.random.default_rng(seed)
+    N = 6
+    W = (rng.standard_normal((N, K)) * rng.choice([0.02, 1.0, 300.0], (N, 1))).astype(np.float16)
+    W[0, : min(K, g)] = 0  # a degenerate all-zero group
+    W[1] = np.abs(W[1])  # all positive: zero is the low end
+    W[2] = -np.abs(W[2])  # all negative: zero is the high end
+    q, s, z = oracle.quantize(W, g)
+    for n in range(N):
+        qe, se, ze = _quantize_exact([_fr(v) for v in W[n]], K, g)
+        assert list(q[n]) == qe
+        assert list(s[n].view(np.uint16)) == se
+        assert list(z[n]) == ze
+
+
+def test_quantize_invariants_on_config_shapes():
+    # the tiny config and the torchchat-style partial group, plus a third shape with a 104-wide tail
+    for (N, K, g) in [(256, 512, 128), (288, 288, 256), (64, 1000, 128)]:
+        W = workloads.weights_f16(N, K, seed=7)
+        q, s, z = oracle.quantize(W, g)
+        G = oracle.ngroups(K, g)
+        assert q.max() <= 15 and z.max() <= 15
+        w = W.astype(np.float64)
+        sv = s.astype(np.float64)
+        idx = np.arange(K) // g
+        what = (q.astype(np.float64) - z[:, idx]) * sv[:, idx]
+        # round-trip error bound |w - (q - z) s| <= s/2 (plus fp64 division slack)
+        assert (np.abs(w - what) <= sv[:, idx] / 2 * (1 + 2.0**-40)).all()
+        # s is the least fp16 with 15 s >= r (range including zero)
+        for j in range(G):
+            blk = w[:, j * g:min((j + 1) * g, K)]
+            r = np.maximum(blk.max(1), 0) - np.minimum(blk.min(1), 0)
+            nz = r > 0
+            assert (15 * sv[nz, j] >= r[nz]).all()
+            prev = (s[nz, j].view(np.uint16) - 1).view(np.float16).astype(np.float64)
+            assert (15 * prev < r[nz]).all()
+            assert (s[~nz, j].view(np.uint16) == 0x3C00).all()
+
+
+def test_quantize_rejects_non_finite():
+    W = np.zeros((2, 16), np.float16)
+    W[1, 3] = np.inf
+    with pytest.raises(ValueError):
+        oracle.quantize(W, 8)
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([c.strip() for c in line.split("|")])
+    return rows
+
+
+def test_quantize_hand_derived_groups():
+    for name, ws, sbits, zz, codes in _read_golden("quantize_groups.txt"):
+        W = _f16([float(v) for v in ws.split()])[None, :]
+        q, s, z = oracle.quantize(W, 8)
+        assert int(s[0, 0].view(np.uint16)) == int(sbits, 16), name
+        assert int(z[0, 0]) == int(zz), name
+        assert list(q[0]) == [int(c) for c in codes.split()], name
+
+
+def test_partial_last_group_hand_derived():
+    (head, ws, sbits, zz, codes), = _read_golden("partial_group.txt")
+    K, g = (int(v) for v in head.split())
+    W = _f16([float(v) for v in ws.split()])[None, :]
+    q, s, z = oracle.quantize(W, g)
+    assert list(s[0].view(np.uint16)) == [int(b, 16) for b in sbits.split()]
+    assert list(z[0]) == [int(v) for v in zz.split()]
+    assert list(q[0]) == [int(c) for c in codes.split()]
+    # and the GEMM over it: x = ones gives the sum of the dequantized row, by hand:
+    # group 0: (-5-2+0+1+4+5+7+10) * 1639/16384, group 1: (7-7+4+0) * 1093/16384
+    qw, zw = oracle.pack_nibbles(q), oracle.pack_nibbles(z)
+    y = oracle.gemm(np.ones((1, K), np.float16), qw, s, zw, 1, K, g)
+    assert y[0, 0] == 20 * 1639 / 16384 + 4 * 1093 / 16384
+
+
+# ------------------------------------------------------------------------- pack
+
+
+def test_pack_golden_words():
+    for kind, codes, word in _read_golden("layout_words.txt"):
+        c = [int(v) for v in codes.split()]
+        if kind == "canonical":
+            got = oracle.pack_nibbles(np.array([c], np.uint8))
+            assert got.shape == (1, 1) and int(got[0, 0]) == int(word, 16)
+
+
+def test_pack_roundtrip_and_padding():
+    rng = np.random.default_rng(5)
+    for cols in (1, 7, 8, 9, 63, 500):
+        v = rng.integers(0, 16, (5, cols)).astype(np.uint8)
+        p = oracle.pack_nibbles(v)
+        assert p.shape == (5, -(-cols // 8))
+        assert (oracle.unpack_nibbles(p, cols) == v).all()
+        if cols % 8:
+            assert (p[:, -1] >> np.uint32(4 * (cols % 8)) == 0).all()  # padding nibbles are 0
+
+
+# ----------------------------------------------------------------------- repack
+
+
+def test_repack_golden_tile_words():
+    for kind, codes, word in _read_golden("layout_words.txt"):
+        if kind != "tiled":
+            continue
+        c = np.array([[int(v) for v in codes.split()]], np.uint8)
+        qw = oracle.pack_nibbles(c)
+        s = np.ones((1, 1), np.float16)
+        zw = np.zeros((1, 1), np.uint32)
+        buf = oracle.repack(qw, s, zw, 1, 8, 8)
+        assert buf.size == 4096 + 320
+        assert int(buf[:4].view(np.uint32)[0]) == int(word, 16)
+        assert (buf[4:4096] == 0).all()
+        assert int(buf[4096:4098].view(np.uint16)[0]) == 0x3C00
+
+
+@pytest.mark.parametrize("N,K,g", [(1, 8, 8), (130, 72, 8), (288, 288, 256), (256, 512, 128), (200, 4000 // 10, 128),
+                                   (129, 136, 24)])
+def test_repack_is_a_zero_padded_permutation(N, K, g):
+    rng = np.random.default_rng(N + K)
+    G = oracle.ngroups(K, g)
+    q = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    z = rng.integers(0, 16, (N, G)).astype(np.uint8)
+    s = rng.standard_normal((N, G)).astype(np.float16)
+    qw, zw = oracle.pack_nibbles(q), oracle.pack_nibbles(z)
+    buf = oracle.repack(qw, s, zw, N, K, g)
+    NT, KB = -(-N // 128), -(-K // 64)
+    assert buf.size == NT * KB * 4096 + NT * G * 320
+    # inverse map gives the canonical form back
+    qw2, s2, zw2 = oracle.unrepack(buf, N, K, g)
+    assert (qw2 == qw).all() and (s2.view(np.uint16) == s.view(np.uint16)).all() and (zw2 == zw).all()
+    # the code region holds exactly the codes plus zero padding (a permutation)
+    codes = buf[: NT * KB * 4096]
+    nibs = np.concatenate([codes & 0xF, codes >> 4])
+    hist = np.bincount(nibs, minlength=16)
+    ref = np.bincount(q.ravel(), minlength=16)
+    ref[0] += NT * 128 * KB * 64 - N * K
+    assert (hist == ref).all()
+    # each record's zero nibbles hold that n-tile's zeros of one group (multiset per (tile, group))
+    meta = buf[NT * KB * 4096:].reshape(NT, G, 320)
+    for t in range(NT):
+        rows = slice(128 * t, min(N, 128 * t + 128))
+        nrow = rows.stop - rows.start
+        for j in range(0, G, max(1, G // 3)):
+            zb = meta[t, j, 256:]
+            zn = np.stack([zb & 0xF, zb >> 4], 1).ravel()[:128]
+            assert sorted(zn[:nrow]) == sorted(z[rows, j]) and (zn[nrow:] == 0).all()
+            sc = meta[t, j, :256].view(np.uint16)
+            assert sorted(sc[:nrow]) == sorted(s[rows, j].view(np.uint16)) and (sc[nrow:] == 0).all()
+
+
+# ----------------------------------------------------------------- dequant/gemm
+
+
+def test_q_equal_z_decodes_to_exact_zero():
+    N, K, g = 9, 40, 16
+    G = oracle.ngroups(K, g)
+    rng = np.random.default_rng(11)
+    z = rng.integers(0, 16, (N, G)).astype(np.uint8)
+    q = z[:, np.arange(K) // g]
+    s = (rng.standard_normal((N, G)) * 100).astype(np.float16)
+    w = oracle.dequant(oracle.pack_nibbles(q), s, oracle.pack_nibbles(z), N, K, g)
+    assert (w == 0).all()
+
+
+def test_dequant_hand_derived_values():
+    rows = _read_golden("quantize_groups.txt")
+    name, ws, sbits, zz, codes = rows[0]
+    q = np.array([[int(c) for c in codes.split()]], np.uint8)
+    s = np.array([[int(sbits, 16)]], np.uint16).view(np.float16)
+    z = np.array([[int(zz)]], np.uint8)
+    w = oracle.dequant(oracle.pack_nibbles(q), s, oracle.pack_nibbles(z), 1, 8, 8)
+    assert list(w[0]) == [v * 1639 / 16384 for v in (-5, -2, 0, 1, 4, 5, 7, 10)]
+
+
+def _canonical(N, K, g, seed=0):
+    W = workloads.weights_f16(N, K, seed=seed)
+    return oracle.pack(W, g)
+
+
+def test_gemm_one_hot_rows_return_weight_columns():
+    N, K, g = 37, 136, 32  # partial last group of 8
+    qw, s, zw = _canonical(N, K, g)
+    w = oracle.dequant(qw, s, zw, N, K, g)
+    ks = [0, 1, 31, 32, 100, 128, 135]
+    x = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    y = oracle.gemm(x, qw, s, zw, N, K, g)
+    for i, k in enumerate(ks):
+        assert (y[i] == w[:, k]).all()
+
+
+def test_gemm_equals_library_matmul():
+    N, K, g, M = 96, 520, 128, 5
+    qw, s, zw = _canonical(N, K, g)
+    x = workloads.activations_f16(M, K)
+    y = oracle.gemm(x, qw, s, zw, N, K, g)
+    w = oracle.dequant(qw, s, zw, N, K, g)
+    ref = x.astype(np.float64) @ w.T
+    mag = np.abs(x.astype(np.float64)) @ np.abs(w).T
+    assert (np.abs(y - ref) <= 1e-13 * mag).all()
+    # sampled rows are the same numbers as the full product
+    rows = np.array([4, 0, 2])
+    assert (oracle.gemm(x, qw, s, zw, N, K, g, rows=rows) == y[rows]).all()
+    # one thread and many threads agree exactly (same summation order)
+    assert (oracle.gemm(x, qw, s, zw, N, K, g, nthreads=1) == y).all()
+
+
+@pytest.mark.parametrize("M,N,K,g", [(1, 2, 8, 8), (2, 3, 40, 16), (3, 5, 24, 8), (2, 4, 72, 64)])
+def test_gemm_exact_rational_brute_force(M, N, K, g):
+    rng = np.random.default_rng(M * 100 + K)
+    W = (rng.standard_normal((N, K)) * 0.5).astype(np.float16)
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    q, s, z = oracle.quantize(W, g)
+    y = oracle.gemm(x, oracle.pack_nibbles(q), s, oracle.pack_nibbles(z), N, K, g)
+    for m in range(M):
+        for n in range(N):
+            terms = [_fr(x[m, k]) * (int(q[n, k]) - int(z[n, k // g])) * _fr(s[n, k // g]) for k in range(K)]
+            exact = sum(terms, Fraction(0))
+            bound = sum(abs(t) for t in terms) * Fraction(K, 2**52)
+            assert abs(Fraction(y[m, n]) - exact) <= bound
+
+
+def test_gemm_is_linear_in_x():
+    N, K, g = 20, 264, 64
+    qw, s, zw = _canonical(N, K, g)
+    x1 = workloads.activations_f16(1, K, seed=3)
+    x2 = workloads.activations_f16(1, K, seed=4)
+    x12 = (x1.astype(np.float64) + x2.astype(np.float64))
+    assert (x12.astype(np.float16).astype(np.float64) == x12).mean() > 0.3
+    exact = x12.astype(np.float16).astype(np.float64) == x12
+    x1[~exact] = 0
+    x2[~exact] = 0
+    x12 = (x1.astype(np.float64) + x2.astype(np.float64)).astype(np.float16)
+    ya = oracle.gemm(x1, qw, s, zw, N, K, g) + oracle.gemm(x2, qw, s, zw, N, K, g)
+    yb = oracle.gemm(x12, qw, s, zw, N, K, g)
+    w = oracle.dequant(qw, s, zw, N, K, g)
+    mag = (np.abs(x1.astype(np.float64)) + np.abs(x2.astype(np.float64))) @ np.abs(w).T
+    assert (np.abs(ya - yb) <= 1e-13 * mag).all()
