@@ -1,0 +1,172 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 group-quantized linear layer.
+ *
+ *   y[M,N] = x[M,K] . dequant(Wq)[N,K]^T,   w[n,k] = (q[n,k] - z[n,j]) * s[n,j],  j = floor(k/g)
+ *
+ * x and y are fp16, row-major. Each weight is an unsigned 4-bit code q in
+ * [0,15]; every (output row n, group j of g consecutive k) has an fp16 scale
+ * s and a 4-bit zero z. When K is not a multiple of g the last group is
+ * narrower than g and is handled as such: nothing is padded or skipped.
+ *
+ * Where this comes from:
+ *  - fp16 activations times 4-bit weights, memory-bound at small batch and
+ *    compute-bound at large batch: Marlin post ("FP16xINT4" kernel; ideal
+ *    speed-up of 4x from weight bytes alone).
+ *  - group-wise 4-bit weights with a group size: lmdeploy PR #202 "Blazing
+ *    fast W4A16 inference" (AWQ weights, --group_size 128), torchchat issue
+ *    #1362 ('linear:int4' with 'groupsize').
+ *  - a last group narrower than g: torchchat issue #1362, option 2 ("groupwise
+ *    GEMM with a last group that's not a full group").
+ *  - converting canonical packed weights into the kernel's own layout once,
+ *    offline: the converter step of lmdeploy PR #202 (deploy.py with
+ *    --model_format awq).
+ *
+ * Conventions for every call:
+ *  - Pointers named *_dev are device pointers; the caller allocates and owns
+ *    all buffers. The library allocates no device memory and never
+ *    synchronises a stream, except w4_last_device_error (documented there).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All device work is enqueued on it and is asynchronous to the host.
+ *  - Arguments are checked on the host first; a failed check returns a
+ *    status and enqueues nothing. Launch failures return W4_ERR_CUDA.
+ *  - The device code is built for sm_103a only.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4_API __attribute__((visibility("default")))
+#else
+#define W4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4_OK = 0,
+    W4_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, g not a positive multiple of 8 */
+    W4_ERR_UNSUPPORTED_SHAPE = 2,  /* a size the kernel does not take (e.g. K % 8 != 0 in the GEMM) */
+    W4_ERR_MISALIGNED = 3,         /* a pointer not aligned as the call requires */
+    W4_ERR_WORKSPACE_TOO_SMALL = 4,
+    W4_ERR_CUDA = 5,               /* a CUDA runtime/driver call or kernel launch failed */
+    W4_ERR_TIMEOUT = 6             /* a device-side wait gave up (read with w4_last_device_error) */
+} w4_status;
+
+/* Static, human-readable name of a status code. Never NULL. */
+W4_API const char *w4_status_string(int status);
+
+/*
+ * w4_pack -- quantize fp16 weights into the canonical packed form.
+ *
+ * W_dev      fp16 [N, K] row-major (nn.Linear weight layout). Must be finite.
+ * N, K       >= 1, any value.
+ * g          group size along K, a positive multiple of 8. G = ceil(K/g).
+ * qw_dev     out: uint32 [N, ceil(K/8)]; code of k = 8c + i in bits 4i..4i+3
+ *            of word c of row n; padding nibbles (k >= K) are 0.
+ * scales_dev out: fp16 [N, G].
+ * zeros_dev  out: uint32 [N, ceil(G/8)]; zero of group j = 8c + i in bits
+ *            4i..4i+3 of word c of row n; padding nibbles are 0.
+ *
+ * Per (n, j), over k in [j*g, min((j+1)*g, K)), in fp64:
+ *   lo = min(0, min w), hi = max(0, max w), r = hi - lo;
+ *   r == 0: s = 1, z = 0, q = 0;
+ *   else s = fp16(r / 15) rounded to nearest-even, raised one fp16 step if
+ *   15*s < r; z = clamp(rint(-lo / s), 0, 15); q = clamp(rint(w / s) + z, 0, 15)
+ *   (rint = round half to even). Bit-exact and deterministic.
+ * Alignment: W 2-byte, outputs 4-byte (scales 2-byte).
+ */
+W4_API int w4_pack(const void *W_dev, int64_t N, int64_t K, int32_t g,
+            uint32_t *qw_dev, void *scales_dev, uint32_t *zeros_dev, void *stream);
+
+/*
+ * Size in bytes of the GEMM's tile layout for an [N, K] weight with group size g:
+ *   ceil(N/128) * ceil(K/64) * 4096 + ceil(N/128) * ceil(K/g) * 320.
+ * Returns 0 for invalid sizes.
+ */
+W4_API size_t w4_repacked_bytes(int64_t N, int64_t K, int32_t g);
+
+/*
+ * w4_repack -- canonical packed form -> the GEMM's tile layout (a permutation
+ * of codes, scales and zeros; bit-exact, deterministic).
+ *
+ * Inputs as produced by w4_pack. `packed_dev` (out) has w4_repacked_bytes(N,K,g)
+ * bytes, 16-byte aligned. Layout, with NT = ceil(N/128), KB = ceil(K/64):
+ *  - code tiles: tile (t, b) of 4096 bytes at offset (t*KB + b)*4096 holds
+ *    rows n = 128t + r (r < 128) and k = 64b .. 64b+63; the little-endian
+ *    uint32 at byte h*2048 + r*16 + 4*i (h < 2, i < 4) holds the 8 codes of
+ *    row n at k = 64b + 32h + 8i + e (e < 8), code e at nibble 4*(e%2) + e/2;
+ *  - group records after the tiles: record (t, j) of 320 bytes at offset
+ *    NT*KB*4096 + (t*G + j)*320 holds the fp16 scale of row 128t + r at byte
+ *    2r and its zero in byte 256 + r/2 (low nibble for even r);
+ *  - everything at n >= N or k >= K is 0.
+ */
+W4_API int w4_repack(const uint32_t *qw_dev, const void *scales_dev, const uint32_t *zeros_dev,
+              int64_t N, int64_t K, int32_t g, void *packed_dev, void *stream);
+
+/*
+ * Bytes of device workspace w4a16_gemm needs for this problem on the current
+ * device (error word, split-K tile counters and fp32 partial sums). Always
+ * >= 256. Returns 0 for invalid sizes.
+ */
+W4_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t g);
+
+/*
+ * w4a16_gemm -- y = x . dequant(packed)^T.
+ *
+ * x_dev      fp16 [M, K] row-major, 16-byte aligned.
+ * packed_dev w4_repack output for (N, K, g), 16-byte aligned.
+ * y_dev      out: fp16 [M, N] row-major, 2-byte aligned.
+ * workspace_dev / workspace_bytes: at least w4a16_workspace_bytes(M, N, K, g)
+ *            bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE; the
+ *            kernels leave it ready for the next call. Calls sharing one
+ *            workspace must not overlap on the device.
+ * M >= 1, N >= 1, K >= 8 with K % 8 == 0 (the activation rows' byte stride
+ * must be a multiple of 16), g a positive multiple of 8; K % g may be
+ * anything (the last group is partial).
+ *
+ * Numerics: each weight is dequantized once to fp16, rounded once:
+ * fp16((q - z) * s) with q - z formed exactly; products are accumulated in
+ * fp32 on the tensor cores (tcgen05, accumulator in tensor memory); split-K
+ * partial sums are added in fp32 in a fixed order; y is rounded to fp16
+ * (nearest-even). Results are deterministic run to run.
+ */
+W4_API int w4a16_gemm(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K,
+               int32_t g, void *y_dev, void *workspace_dev, size_t workspace_bytes, void *stream);
+
+/*
+ * As w4a16_gemm with the tiling forced: block_n is the number of activation
+ * rows per tile (16, 32, 64, 128 or 256; 0 = automatic) and splits the number
+ * of K partitions (1..64; 0 = automatic). The workspace must be at least
+ * w4a16_workspace_bytes_ex(M, N, K, g, block_n, splits). For tests and tuning.
+ */
+W4_API int w4a16_gemm_ex(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K,
+                  int32_t g, void *y_dev, void *workspace_dev, size_t workspace_bytes,
+                  int32_t block_n, int32_t splits, void *stream);
+W4_API size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t g,
+                                int32_t block_n, int32_t splits);
+
+/*
+ * The tiling w4a16_gemm would pick on the current device: writes block_n,
+ * splits and the number of CTAs launched. Returns W4_OK or an error status.
+ */
+W4_API int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g,
+                    int32_t *block_n, int32_t *splits, int32_t *ctas);
+
+/*
+ * Reads and clears the device error word that GEMM kernels write into the
+ * workspace. SYNCHRONISES `stream`. Returns W4_OK, W4_ERR_TIMEOUT (a
+ * pipeline wait inside a kernel gave up after about a second and the kernel
+ * returned early; y is then undefined) or W4_ERR_CUDA.
+ */
+W4_API int w4_last_device_error(void *workspace_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,111 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol that
+include/w4a16.h declares, sizes its buffers by the documented formulas and
+rejects bad arguments on the host before any CUDA call."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import w4a16_group_quantized_gb300 as w4
+from w4a16_group_quantized_gb300 import build as w4build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    w4build.build()
+    return w4.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"W4_API\s+[\w\s\*]*?\b(w4\w*)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for required in ("w4_pack", "w4_repack", "w4a16_gemm"):
+        assert required in names
+    assert len(names) >= 10
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in w4.STATUS.items():
+        assert w4.w4_status_string(code).startswith(name)
+    assert "unknown" in w4.w4_status_string(99)
+
+
+def test_repacked_bytes_formula(lib):
+    for (N, K, g) in [(256, 512, 128), (288, 288, 256), (4096, 4000, 128), (12288, 4096, 128), (1, 8, 8),
+                      (57344, 8192, 128), (130, 72, 8)]:
+        NT, KB, G = -(-N // 128), -(-K // 64), -(-K // g)
+        assert w4.w4_repacked_bytes(N, K, g) == NT * KB * 4096 + NT * G * 320
+    assert w4.w4_repacked_bytes(0, 8, 8) == 0
+    assert w4.w4_repacked_bytes(8, 8, 12) == 0  # g not a multiple of 8
+
+
+def test_workspace_sizes(lib):
+    # no split: error word + counters only
+    b = w4.w4a16_workspace_bytes_ex(512, 8192, 8192, 128, 256, 1)
+    assert b == 256 + 512  # error word block + 2 x 64 tile counters of 4 bytes
+    # forced split: partial sums S x M x Npad fp32
+    M, N, K, S = 16, 300, 1024, 4
+    b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 16, S)
+    assert b >= S * M * 384 * 4 + 256
+    assert w4.w4a16_workspace_bytes(0, 1, 8, 8) == 0
+    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 1) == 0  # block_n must be 16..256, a power of two
+
+
+def _vp(v):
+    return ctypes.c_void_p(v)
+
+
+def test_host_side_argument_checks(lib):
+    fake = _vp(0x10000)  # never dereferenced: every case below fails its host-side check first
+    ws = _vp(0x20000)
+    S = w4
+    # null pointers / bad sizes / bad group
+    assert lib.w4a16_gemm(None, fake, 1, 1, 8, 8, fake, ws, 4096, None) == 1
+    assert lib.w4a16_gemm(fake, fake, 0, 1, 8, 8, fake, ws, 4096, None) == 1
+    assert lib.w4a16_gemm(fake, fake, 1, 1, 8, 12, fake, ws, 4096, None) == 1
+    assert lib.w4a16_gemm(fake, fake, 1, 1, 8, 0, fake, ws, 4096, None) == 1
+    # K not a multiple of 8
+    assert lib.w4a16_gemm(fake, fake, 1, 1, 12, 8, fake, ws, 4096, None) == 2
+    # misaligned x / packed / workspace
+    assert lib.w4a16_gemm(_vp(0x10008), fake, 1, 1, 8, 8, fake, ws, 4096, None) == 3
+    assert lib.w4a16_gemm(fake, _vp(0x10004), 1, 1, 8, 8, fake, ws, 4096, None) == 3
+    assert lib.w4a16_gemm(fake, fake, 1, 1, 8, 8, fake, _vp(0x20010), 4096, None) == 3
+    # workspace too small
+    assert lib.w4a16_gemm(fake, fake, 1, 1, 8, 8, fake, ws, 16, None) == 4
+    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1024, 16, 4, None) == 4
+    # forced tiling out of range
+    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1 << 30, 48, 1, None) == 1
+    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1 << 30, 16, 65, None) == 1
+    # pack / repack
+    assert lib.w4_pack(None, 4, 8, 8, fake, fake, fake, None) == 1
+    assert lib.w4_pack(fake, 4, 8, 7, fake, fake, fake, None) == 1
+    assert lib.w4_pack(_vp(0x10001), 4, 8, 8, fake, fake, fake, None) == 3
+    assert lib.w4_repack(fake, fake, fake, 4, 8, 8, _vp(0x10008), None) == 3
+    assert lib.w4_repack(fake, fake, fake, -1, 8, 8, fake, None) == 1
+    assert lib.w4_last_device_error(None, None) == 1
+    del S
+
+
+def test_binding_has_no_cpu_path():
+    import torch
+
+    x = torch.zeros(4, 8, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        w4.w4a16_gemm(x, torch.zeros(16, dtype=torch.uint8), 8, 8, 8)
+    with pytest.raises(ValueError):
+        w4.w4_pack(torch.zeros(4, 8, dtype=torch.float16), 8)

@@ -1,0 +1,189 @@
+"""w4a16_gemm on the GPU against the fp64 CPU oracle.
+
+Tolerance per element: |y - y_ref| <= 1e-3 * ||x_m|| * ||w_n|| + 1e-3 (y_ref
+and w_n from the oracle). Small cases compare every element; the full-size
+layers compare every row the oracle can afford plus sampled rows, in the same
+launch configuration the bench times (automatic tiling)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a16_group_quantized_gb300 as w4
+import workloads
+from helpers import assert_within_tolerance, gemm_tolerance, row_norms_dequant
+
+pytestmark = pytest.mark.gpu
+
+_cache = {}
+
+
+def layer(N, K, g, seed=0):
+    """Oracle canonical form of a seeded layer and its GPU tile layout (via the oracle's canonical buffers)."""
+    key = (N, K, g, seed)
+    if key not in _cache:
+        W = workloads.weights_f16(N, K, seed=seed)
+        qw, s, zw = oracle.pack(W, g)
+        packed = w4.w4_repack(torch.from_numpy(qw.view(np.int32)).cuda(), torch.from_numpy(s).cuda(),
+                              torch.from_numpy(zw.view(np.int32)).cuda(), N, K, g)
+        wn = row_norms_dequant(qw, s, zw, N, K, g)
+        if len(_cache) > 6:
+            _cache.clear()
+        _cache[key] = (qw, s, zw, packed, wn)
+    return _cache[key]
+
+
+def run_gemm(x, packed, N, K, g, block_n=0, splits=0, ws=None):
+    xd = torch.from_numpy(x).cuda()
+    if block_n or splits:
+        y = w4.w4a16_gemm_ex(xd, packed, N, K, g, block_n, splits, workspace=ws)
+    else:
+        y = w4.w4a16_gemm(xd, packed, N, K, g, workspace=ws)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def check(M, N, K, g, block_n=0, splits=0, rows=None, outliers=False, seed_x=1):
+    qw, s, zw, packed, wn = layer(N, K, g)
+    x = workloads.activations_f16(M, K, seed=seed_x, outliers=outliers)
+    ws = w4.Workspace()
+    y = run_gemm(x, packed, N, K, g, block_n, splits, ws)
+    assert w4.w4_last_device_error(ws) == 0
+    if rows is None:
+        rows = np.arange(M)
+    yref = oracle.gemm(x, qw, s, zw, N, K, g, rows=rows)
+    tol = gemm_tolerance(x[rows], wn)
+    return assert_within_tolerance(y[rows], yref, tol, f"M={M} N={N} K={K} g={g} bn={block_n} S={splits}")
+
+
+# ------------------------------------------------------------ small, every element
+
+
+def test_tiny_config():
+    L = workloads.TINY
+    check(workloads.TINY_M, L.n, L.k, L.g)
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+@pytest.mark.parametrize("L", workloads.PARTIAL_LAYERS, ids=lambda L: L.name)
+def test_partial_last_group_configs(M, L):
+    check(M, L.n, L.k, L.g)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 7, 15, 16, 17, 31, 33, 63, 65, 127, 129, 255, 257, 300])
+def test_tile_edges(M):
+    # N = 300: a partial n-tile; K = 520: a 64-block tail of 8 and a last group 8 wide
+    check(M, 300, 520, 128)
+
+
+@pytest.mark.parametrize("block_n", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_forced_tilings(block_n, splits):
+    check(20, 260, 1024, 128, block_n=block_n, splits=splits)
+
+
+@pytest.mark.parametrize("g", [8, 16, 24, 32, 40, 96, 192, 256, 1024])
+def test_group_sizes(g):
+    # 64 % g != 0 or g % 64 != 0 takes the per-chunk group path; K = 1000 leaves a partial last group
+    check(9, 200, 1000, g)
+    check(9, 200, 1000, g, block_n=16, splits=3)
+
+
+def test_one_hot_rows_return_rounded_weights_exactly():
+    N, K, g = 384, 640, 128
+    qw, s, zw, packed, wn = layer(N, K, g)
+    ks = [0, 1, 63, 64, 127, 128, 300, 511, 600, 639]
+    x = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    wd = oracle.dequant(qw, s, zw, N, K, g)
+    expect = wd[:, ks].T.astype(np.float16)  # (q - z) * s is exact in fp64; one rounding to fp16
+    for bn, sp in [(0, 0), (16, 1), (16, 4), (256, 1), (64, 3)]:
+        y = run_gemm(x, packed, N, K, g, bn, sp)
+        assert (y.view(np.uint16) == expect.view(np.uint16)).all(), (bn, sp)
+
+
+def test_q_equal_z_gives_exact_zero():
+    N, K, g = 256, 512, 64
+    G = K // g
+    rng = np.random.default_rng(4)
+    z = rng.integers(0, 16, (N, G)).astype(np.uint8)
+    q = z[:, np.arange(K) // g]
+    s = (np.abs(rng.standard_normal((N, G))) + 0.01).astype(np.float16)
+    qw, zw = oracle.pack_nibbles(q), oracle.pack_nibbles(z)
+    packed = w4.w4_repack(torch.from_numpy(qw.view(np.int32)).cuda(), torch.from_numpy(s).cuda(),
+                          torch.from_numpy(zw.view(np.int32)).cuda(), N, K, g)
+    x = workloads.activations_f16(17, K)
+    y = run_gemm(x, packed, N, K, g)
+    assert (y == 0).all()
+
+
+def test_deterministic_and_workspace_reuse():
+    N, K, g, M = 1000, 2048, 128, 12
+    qw, s, zw, packed, wn = layer(N, K, g)
+    x = torch.from_numpy(workloads.activations_f16(M, K)).cuda()
+    ws = w4.Workspace()
+    outs = [w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 5, workspace=ws).clone() for _ in range(3)]
+    outs += [w4.w4a16_gemm(x, packed, N, K, g, workspace=ws).clone() for _ in range(2)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    assert torch.equal(outs[3], outs[4])
+    # counters were left at zero: a fresh workspace gives the same bits
+    y2 = w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 5, workspace=w4.Workspace())
+    assert torch.equal(outs[0], y2)
+    assert w4.w4_last_device_error(ws) == 0
+
+
+def test_end_to_end_from_fp16_weights():
+    # GPU pack -> GPU repack -> GEMM, against the oracle run from the same fp16 weights
+    N, K, g, M = 512, 768, 128, 6
+    W = workloads.weights_f16(N, K, seed=21)
+    qw, s, zw = w4.w4_pack(torch.from_numpy(W).cuda(), g)
+    packed = w4.w4_repack(qw, s, zw, N, K, g)
+    x = workloads.activations_f16(M, K, seed=22)
+    y = w4.w4a16_gemm(torch.from_numpy(x).cuda(), packed, N, K, g).cpu().numpy()
+    oq, os_, oz = oracle.pack(W, g)
+    yref = oracle.gemm(x, oq, os_, oz, N, K, g)
+    assert_within_tolerance(y, yref, gemm_tolerance(x, row_norms_dequant(oq, os_, oz, N, K, g)), "e2e")
+
+
+def test_host_errors_on_device_tensors():
+    N, K, g = 256, 512, 128
+    qw, s, zw, packed, wn = layer(N, K, g)
+    flat = torch.zeros(3 * K + 8, dtype=torch.float16, device="cuda")
+    x_mis = flat[1:1 + 3 * K].view(3, K)  # contiguous but 2 bytes off a 16-byte boundary
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4a16_gemm(x_mis, packed, N, K, g)
+    assert e.value.status == 3
+    x12 = torch.zeros(3, 12, dtype=torch.float16, device="cuda")
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4a16_gemm(x12, packed, N, 12, 8)
+    assert e.value.status == 2
+    x = torch.zeros(16, K, dtype=torch.float16, device="cuda")
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 4, workspace=torch.zeros(256, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 4
+
+
+# ------------------------------------------------------- full-size layers, sampled
+
+
+def _sample_rows(M, k=24, seed=5):
+    if M <= k:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, M - 1], rng.choice(M, k - 2, replace=False)]))
+
+
+@pytest.mark.parametrize("L", workloads.DECODE_LAYERS, ids=lambda L: L.name)
+def test_decode_sweep_layers(L):
+    for M in workloads.DECODE_MS:
+        check(M, L.n, L.k, L.g, rows=_sample_rows(M, 16))
+
+
+@pytest.mark.parametrize("L", workloads.PREFILL_LAYERS, ids=lambda L: L.name)
+def test_prefill_layers_sampled(L):
+    for M in (256, 4096):
+        check(M, L.n, L.k, L.g, rows=_sample_rows(M, 8), outliers=True)

@@ -1,0 +1,207 @@
+"""Thin Python binding of libw4a16.so (the C ABI in include/w4a16.h).
+
+Argument marshalling only: every step of the quantized linear layer runs in
+the library's CUDA kernels. PyTorch supplies device memory and the current
+stream. There is no CPU or PyTorch fallback: if the library is missing or a
+call fails, a ``W4Error`` is raised.
+
+Names follow the C ABI:
+
+    qw, scales, zeros = w4_pack(W, g)                 # fp16 [N,K] cuda -> canonical packed form
+    packed = w4_repack(qw, scales, zeros, N, K, g)    # -> the GEMM's tile layout (uint8 buffer)
+    y = w4a16_gemm(x, packed, N, K, g)                # fp16 [M,K] -> fp16 [M,N]
+
+uint32 words are carried in torch.int32 tensors (same bits).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "W4Error", "lib_path", "load", "w4_pack", "w4_repack", "w4_repacked_bytes", "w4a16_gemm",
+    "w4a16_gemm_ex", "w4a16_workspace_bytes", "w4a16_workspace_bytes_ex", "w4a16_gemm_plan",
+    "w4_last_device_error", "w4_status_string", "Workspace", "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libw4a16.so")
+
+STATUS = {
+    0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED_SHAPE", 3: "W4_ERR_MISALIGNED",
+    4: "W4_ERR_WORKSPACE_TOO_SMALL", 5: "W4_ERR_CUDA", 6: "W4_ERR_TIMEOUT",
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {w4_status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libw4a16.so (built by ``python -m w4a16_group_quantized_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(lib_path):
+            raise ImportError(f"{lib_path} is missing: build it with `python -m w4a16_group_quantized_gb300.build`")
+        lib = ctypes.CDLL(lib_path)
+        P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        sigs = {
+            "w4_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "w4_pack": ([P, I64, I64, I32, P, P, P, P], ctypes.c_int),
+            "w4_repacked_bytes": ([I64, I64, I32], SZ),
+            "w4_repack": ([P, P, P, I64, I64, I32, P, P], ctypes.c_int),
+            "w4a16_workspace_bytes": ([I64, I64, I64, I32], SZ),
+            "w4a16_workspace_bytes_ex": ([I64, I64, I64, I32, I32, I32], SZ),
+            "w4a16_gemm": ([P, P, I64, I64, I64, I32, P, P, SZ, P], ctypes.c_int),
+            "w4a16_gemm_ex": ([P, P, I64, I64, I64, I32, P, P, SZ, I32, I32, P], ctypes.c_int),
+            "w4a16_gemm_plan": ([I64, I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
+                                 ctypes.POINTER(I32)], ctypes.c_int),
+            "w4_last_device_error": ([P, P], ctypes.c_int),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def w4_status_string(status: int) -> str:
+    return load().w4_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise W4Error(rc, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> ctypes.c_void_p:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ngroups(K: int, g: int) -> int:
+    return -(-K // g)
+
+
+def w4_pack(W: torch.Tensor, g: int, stream=None):
+    """fp16 W [N,K] (cuda) -> (qw int32 [N,ceil(K/8)], scales fp16 [N,G], zeros int32 [N,ceil(G/8)])."""
+    if W.dtype != torch.float16 or W.dim() != 2:
+        raise ValueError("W must be a 2-D fp16 tensor")
+    N, K = W.shape
+    G = _ngroups(K, g) if g > 0 else 1
+    qw = torch.empty((N, -(-K // 8)), dtype=torch.int32, device=W.device)
+    scales = torch.empty((N, G), dtype=torch.float16, device=W.device)
+    zeros = torch.empty((N, -(-G // 8)), dtype=torch.int32, device=W.device)
+    _check(load().w4_pack(_dev(W, "W"), N, K, g, _dev(qw, "qw"), _dev(scales, "scales"), _dev(zeros, "zeros"),
+                          _stream(stream)), "w4_pack")
+    return qw, scales, zeros
+
+
+def w4_repacked_bytes(N: int, K: int, g: int) -> int:
+    return int(load().w4_repacked_bytes(N, K, g))
+
+
+def w4_repack(qw: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, N: int, K: int, g: int,
+              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Canonical packed form -> uint8 buffer in the GEMM's tile layout."""
+    nbytes = w4_repacked_bytes(N, K, g)
+    if nbytes == 0:
+        raise W4Error(1, "w4_repack")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=qw.device)
+    elif out.numel() * out.element_size() < nbytes:
+        raise ValueError("out is too small")
+    _check(load().w4_repack(_dev(qw, "qw"), _dev(scales, "scales"), _dev(zeros, "zeros"), N, K, g,
+                            _dev(out, "out"), _stream(stream)), "w4_repack")
+    return out
+
+
+def w4a16_workspace_bytes(M: int, N: int, K: int, g: int) -> int:
+    return int(load().w4a16_workspace_bytes(M, N, K, g))
+
+
+def w4a16_workspace_bytes_ex(M: int, N: int, K: int, g: int, block_n: int, splits: int) -> int:
+    return int(load().w4a16_workspace_bytes_ex(M, N, K, g, block_n, splits))
+
+
+def w4a16_gemm_plan(M: int, N: int, K: int, g: int):
+    """(block_n, splits, ctas) that w4a16_gemm picks on the current device."""
+    b, s, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().w4a16_gemm_plan(M, N, K, g, ctypes.byref(b), ctypes.byref(s), ctypes.byref(c)), "w4a16_gemm_plan")
+    return b.value, s.value, c.value
+
+
+class Workspace:
+    """A zero-filled device workspace that grows on demand (reuse it across calls on one stream)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = torch.zeros(256, dtype=torch.uint8, device=self.device)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 2 * self.buf.numel()), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def _gemm_common(x, packed, N, K, g, y, workspace, block_n, splits, stream):
+    if x.dtype != torch.float16 or x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be fp16 [M, K]")
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    elif y.dtype != torch.float16 or tuple(y.shape) != (M, N):
+        raise ValueError("y must be fp16 [M, N]")
+    need = w4a16_workspace_bytes_ex(M, N, K, g, block_n, splits)
+    if need == 0:
+        raise W4Error(1, "w4a16_workspace_bytes")
+    if workspace is None:
+        workspace = Workspace(x.device)
+    ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    nbytes = ws.numel() * ws.element_size()
+    lib = load()
+    if block_n == 0 and splits == 0:
+        rc = lib.w4a16_gemm(_dev(x, "x"), _dev(packed, "packed"), M, N, K, g, _dev(y, "y"), _dev(ws, "workspace"),
+                            nbytes, _stream(stream))
+    else:
+        rc = lib.w4a16_gemm_ex(_dev(x, "x"), _dev(packed, "packed"), M, N, K, g, _dev(y, "y"),
+                               _dev(ws, "workspace"), nbytes, block_n, splits, _stream(stream))
+    _check(rc, "w4a16_gemm")
+    return y
+
+
+def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: int, y: torch.Tensor | None = None,
+               workspace=None, stream=None) -> torch.Tensor:
+    """y fp16 [M,N] = x fp16 [M,K] . dequant(packed)^T. ``workspace``: a Workspace or a zeroed uint8 tensor."""
+    return _gemm_common(x, packed, N, K, g, y, workspace, 0, 0, stream)
+
+
+def w4a16_gemm_ex(x, packed, N, K, g, block_n: int, splits: int, y=None, workspace=None, stream=None):
+    """w4a16_gemm with the tiling forced (block_n in {16,32,64,128,256}, splits >= 1; 0 = automatic)."""
+    return _gemm_common(x, packed, N, K, g, y, workspace, block_n, splits, stream)
+
+
+def w4_last_device_error(workspace, stream=None) -> int:
+    """Reads and clears the workspace's device error word (synchronises the stream)."""
+    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
+    return int(load().w4_last_device_error(_dev(ws, "workspace"), _stream(stream)))

@@ -1,0 +1,152 @@
+// C ABI of the library (declared in include/w4a16.h): host-side argument
+// checks, workspace sizing, tiling choice and the launches. Every check runs
+// before anything is enqueued; a failed check returns a status and touches
+// no device state.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "w4a16.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_group(int32_t g) { return g > 0 && g % 8 == 0; }
+
+// 2^31 - 1 bounds every index the kernels form in 32-bit arithmetic.
+constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+int num_sms_current_device() {
+  static int cache[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+int check_gemm_args(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y,
+                    void *ws) {
+  if (!x || !packed || !y || !ws) return W4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || !valid_group(g)) return W4_ERR_INVALID_ARG;
+  if (K % 8 != 0) return W4_ERR_UNSUPPORTED_SHAPE;  // the x row stride must be a multiple of 16 bytes
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim || M * N > (int64_t{1} << 40)) return W4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(y, 2) || !aligned(ws, 256)) return W4_ERR_MISALIGNED;
+  return W4_OK;
+}
+
+int gemm_impl(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y, void *ws,
+              size_t ws_bytes, int32_t block_n, int32_t splits, void *stream) {
+  const int rc = check_gemm_args(x, packed, M, N, K, g, y, ws);
+  if (rc != W4_OK) return rc;
+  w4::GemmPlan plan;
+  if (!w4::make_gemm_plan(M, N, K, g, block_n, splits, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
+  if (ws_bytes < plan.workspace_bytes) return W4_ERR_WORKSPACE_TOO_SMALL;
+  bool encode_failed = false;
+  const cudaError_t e =
+      w4::launch_gemm(x, packed, M, N, K, g, y, ws, plan, static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return W4_ERR_CUDA;
+  return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *w4_status_string(int status) {
+  switch (status) {
+    case W4_OK: return "W4_OK";
+    case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG: null pointer, non-positive size or bad group size";
+    case W4_ERR_UNSUPPORTED_SHAPE: return "W4_ERR_UNSUPPORTED_SHAPE";
+    case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED";
+    case W4_ERR_WORKSPACE_TOO_SMALL: return "W4_ERR_WORKSPACE_TOO_SMALL";
+    case W4_ERR_CUDA: return "W4_ERR_CUDA: a CUDA call or kernel launch failed";
+    case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a device-side wait gave up";
+    default: return "unknown w4 status";
+  }
+}
+
+int w4_pack(const void *W_dev, int64_t N, int64_t K, int32_t g, uint32_t *qw_dev, void *scales_dev,
+            uint32_t *zeros_dev, void *stream) {
+  if (!W_dev || !qw_dev || !scales_dev || !zeros_dev) return W4_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || !valid_group(g)) return W4_ERR_INVALID_ARG;
+  if (N > kMaxDim || K > kMaxDim || N * K > (int64_t{1} << 40)) return W4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_dev, 2) || !aligned(qw_dev, 4) || !aligned(scales_dev, 2) || !aligned(zeros_dev, 4))
+    return W4_ERR_MISALIGNED;
+  const cudaError_t e =
+      w4::launch_pack(W_dev, N, K, g, qw_dev, scales_dev, zeros_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+size_t w4_repacked_bytes(int64_t N, int64_t K, int32_t g) {
+  if (N < 1 || K < 1 || !valid_group(g) || N > kMaxDim || K > kMaxDim) return 0;
+  const int64_t NT = w4::cdiv(N, w4::kTN), KB = w4::cdiv(K, w4::kTK), G = w4::cdiv(K, g);
+  return static_cast<size_t>(NT * KB * w4::kTileBytes + NT * G * w4::kRecBytes);
+}
+
+int w4_repack(const uint32_t *qw_dev, const void *scales_dev, const uint32_t *zeros_dev, int64_t N, int64_t K,
+              int32_t g, void *packed_dev, void *stream) {
+  if (!qw_dev || !scales_dev || !zeros_dev || !packed_dev) return W4_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || !valid_group(g)) return W4_ERR_INVALID_ARG;
+  if (N > kMaxDim || K > kMaxDim || N * K > (int64_t{1} << 40)) return W4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(qw_dev, 4) || !aligned(scales_dev, 2) || !aligned(zeros_dev, 4) || !aligned(packed_dev, 16))
+    return W4_ERR_MISALIGNED;
+  const cudaError_t e =
+      w4::launch_repack(qw_dev, scales_dev, zeros_dev, N, K, g, packed_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t g, int32_t block_n, int32_t splits) {
+  if (M < 1 || N < 1 || K < 1 || !valid_group(g) || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
+  w4::GemmPlan plan;
+  if (!w4::make_gemm_plan(M, N, K, g, block_n, splits, num_sms_current_device(), &plan)) return 0;
+  return plan.workspace_bytes;
+}
+
+size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t g) {
+  return w4a16_workspace_bytes_ex(M, N, K, g, 0, 0);
+}
+
+int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int32_t *block_n, int32_t *splits, int32_t *ctas) {
+  if (!block_n || !splits || !ctas) return W4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || !valid_group(g) || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return W4_ERR_INVALID_ARG;
+  w4::GemmPlan plan;
+  if (!w4::make_gemm_plan(M, N, K, g, 0, 0, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
+  *block_n = plan.block_n;
+  *splits = plan.splits;
+  *ctas = plan.ctas;
+  return W4_OK;
+}
+
+int w4a16_gemm(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g, void *y_dev,
+               void *workspace_dev, size_t workspace_bytes, void *stream) {
+  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, 0, 0, stream);
+}
+
+int w4a16_gemm_ex(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g, void *y_dev,
+                  void *workspace_dev, size_t workspace_bytes, int32_t block_n, int32_t splits, void *stream) {
+  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, block_n, splits, stream);
+}
+
+int w4_last_device_error(void *workspace_dev, void *stream) {
+  if (!workspace_dev) return W4_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace_dev, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return W4_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return W4_ERR_CUDA;
+  if (word == 0) return W4_OK;
+  if (cudaMemsetAsync(workspace_dev, 0, sizeof(word), st) != cudaSuccess) return W4_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return W4_ERR_CUDA;
+  return W4_ERR_TIMEOUT;
+}
+
+}  // extern "C"
