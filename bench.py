@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Throughput of the W4A16 group-quantized GEMM on one GB300 (or N replicas).
+
+One step = one pass of the Llama-2-7B-shaped decode sweep: every batch size
+M in {1, 4, 8, 16, 32, 64, 128} against each of the four layers
+12288x4096 (fused qkv), 4096x4096 (o_proj), 22016x4096 (fused gate/up) and
+4096x11008 (down_proj), group size 128: 28 GEMM launches. Inputs are seeded
+synthetic fp16 (weights ~ N(0, 0.02^2) quantized by w4_pack/w4_repack,
+activations ~ N(0, 1)), resident in HBM before the timed region.
+
+The step is captured once as a CUDA graph (host launch cost is larger than
+a decode GEMM) and replayed; each layer has three weight copies used in turn
+inside a step and L2 is flushed (a write of a buffer larger than L2) between
+timed replays, so weights stream from HBM. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (fp64, naive triple loop, all host
+cores) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "W4A16 GEMM TFLOP/s and weight GB/s vs M=1..4096; % of roofline, 1×GB300"
+UNIT = "TFLOP/s"
+WORKLOAD = ("llama2-7b decode sweep, g=128: M in {1,4,8,16,32,64,128} x "
+            "[12288x4096 qkv, 4096x4096 o_proj, 22016x4096 gate_up, 4096x11008 down] (28 GEMMs/step)")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def sweep():
+    return [(m, L) for m in workloads.DECODE_MS for L in workloads.DECODE_LAYERS]
+
+
+def weight_bytes(n, k, g):
+    G = -(-k // g)
+    return n * (-(-k // 8)) * 4 + n * G * 2 + n * (-(-G // 8)) * 4
+
+
+def alg_bytes(m, n, k, g):
+    """Bytes each moved once: packed codes + scales + zeros + x + y."""
+    return weight_bytes(n, k, g) + m * k * 2 + m * n * 2
+
+
+def gemm_flops(m, n, k):
+    return 2.0 * m * n * k
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+
+
+def oracle_sample(max_rows_per_m=None):
+    """Canonical weights (oracle pack) and activations for the sweep, for timing the oracle."""
+    import oracle
+
+    data = {}
+    for L in workloads.DECODE_LAYERS:
+        W = workloads.weights_f16(L.n, L.k)
+        data[L.name] = oracle.pack(W, L.g)
+    xs = {k: workloads.activations_f16(max(workloads.DECODE_MS), k) for k in {L.k for L in workloads.DECODE_LAYERS}}
+    return data, xs
+
+
+def time_oracle(data, xs, ms):
+    """Runs the oracle GEMM for every (M in ms, layer); returns (seconds, flops)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    fl = 0.0
+    for m in ms:
+        for L in workloads.DECODE_LAYERS:
+            qw, s, zw = data[L.name]
+            oracle.gemm(xs[L.k][:m], qw, s, zw, L.n, L.k, L.g)
+            fl += gemm_flops(m, L.n, L.k)
+    return time.perf_counter() - t0, fl
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cores = os.cpu_count() or 1
+    data, xs = oracle_sample()
+    ms = (1, 4)  # bounded sample per step: M = 1 and 4 against all four layers
+    for _ in range(args.warmup):
+        time_oracle(data, xs, ms)
+    times, fl = [], 0.0
+    for _ in range(args.steps):
+        t, fl = time_oracle(data, xs, ms)
+        times.append(t)
+    total = sum(times)
+    value = fl * args.steps / total / 1e12
+    sample = "oracle GEMM (fp64 triple loop) for M in {1,4} x the 4 decode layers per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args):
+    import torch
+
+    import w4a16_group_quantized_gb300 as w4
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 << 20) or (126 << 20))
+    stream = torch.cuda.Stream(dev)
+
+    # ---- weights: pack + repack on the GPU (timed separately: offline steps), then copies
+    layers = workloads.DECODE_LAYERS
+    copies, offline = {}, {}
+    for L in layers:
+        W = torch.from_numpy(workloads.weights_f16(L.n, L.k)).to(dev)
+        torch.cuda.synchronize()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            qw, sc, zw = w4.w4_pack(W, L.g)
+            e1.record(stream)
+            packed = w4.w4_repack(qw, sc, zw, L.n, L.k, L.g)
+            e2.record(stream)
+        stream.synchronize()
+        offline[L.name] = {"pack_ms": e0.elapsed_time(e1), "repack_ms": e1.elapsed_time(e2)}
+        nb = weight_bytes(L.n, L.k, L.g)
+        ncopy = max(3, math.ceil(2.2 * l2 / nb))  # enough distinct bytes that a copy leaves L2 before reuse
+        copies[L.name] = [packed] + [packed.clone() for _ in range(ncopy - 1)]
+        del W, qw, sc, zw
+    xs = {m: {k: torch.from_numpy(workloads.activations_f16(m, k)).to(dev) for k in {L.k for L in layers}}
+          for m in workloads.DECODE_MS}
+    ys = {(m, L.name): torch.empty((m, L.n), dtype=torch.float16, device=dev) for m, L in sweep()}
+    ws_need = max(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g) for m, L in sweep())
+    ws = torch.zeros(ws_need, dtype=torch.uint8, device=dev)
+    flush = torch.empty(max(L2_FLUSH_BYTES, 2 * l2), dtype=torch.uint8, device=dev)
+
+    def step_eager(rot=0):
+        use = {L.name: rot for L in layers}
+        for m, L in sweep():
+            c = copies[L.name]
+            w4.w4a16_gemm(xs[m][L.k], c[use[L.name] % 3], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
+            use[L.name] += 1
+
+    # warm-up launches outside capture (per-device kernel attributes), then capture the step
+    with torch.cuda.stream(stream):
+        step_eager()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_eager()
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_error(ws) == 0
+
+    flops_step = sum(gemm_flops(m, L.n, L.k) for m, L in sweep())
+    bytes_step = sum(alg_bytes(m, L.n, L.k, L.g) for m, L in sweep())
+    wbytes_step = sum(weight_bytes(L.n, L.k, L.g) for m, L in sweep())
+
+    # ---- timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    uuid = str(getattr(props, "uuid", "") or "")
+    gpu_id = ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(torch.cuda.current_device())
+    with ClockSampler(gpu_id) as clk:
+        torch.cuda.nvtx.range_push("w4a16_timed")
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.zero_()  # L2 flush between timed steps (outside the events)
+                starts[i].record(stream)
+                graph.replay()
+                ends[i].record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    clocks = clk.summary()
+
+    # ---- per-(M, layer): back-to-back launches over rotating copies, captured as one graph each
+    per = []
+    for m, L in sweep():
+        c = copies[L.name]
+        R = len(c)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            for i in range(R):
+                w4.w4a16_gemm(xs[m][L.k], c[i], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
+        with torch.cuda.stream(stream):
+            g2.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 4
+            e0.record(stream)
+            for _ in range(reps):
+                g2.replay()
+            e1.record(stream)
+        stream.synchronize()
+        t_launch = e0.elapsed_time(e1) * 1e-3 / (reps * R)
+        b = alg_bytes(m, L.n, L.k, L.g)
+        f = gemm_flops(m, L.n, L.k)
+        t_hbm = b / (peaks["hbm_gbs"] * 1e9)
+        t_tc = f / (peaks["bf16_tflops"] * 1e12)
+        bn, ctas, sched = w4.w4a16_gemm_plan(m, L.n, L.k, L.g)
+        per.append({"M": m, "layer": L.name, "us": round(t_launch * 1e6, 3),
+                    "tflops": round(f / t_launch / 1e12, 2),
+                    "weight_gbs": round(weight_bytes(L.n, L.k, L.g) / t_launch / 1e9, 1),
+                    "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                    "roofline_frac": round(max(t_hbm, t_tc) / t_launch, 3),
+                    "block_n": bn, "ctas": ctas, "schedule": "stream-K" if sched == 1 else "whole tiles"})
+        del g2
+    assert w4.w4_last_device_error(ws) == 0
+
+    # ---- end to end through the public API: pinned host x -> device, GEMM, y -> pinned host
+    hx = {m: {k: xs[m][k].cpu().pin_memory() for k in xs[m]} for m in xs}
+    hy = {key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in ys.items()}
+    dx = {m: {k: torch.empty_like(xs[m][k]) for k in xs[m]} for m in xs}
+    h2d = sum(hx[m][L.k].numel() * 2 for m, L in sweep())
+    d2h = sum(hy[(m, L.name)].numel() * 2 for m, L in sweep())
+
+    def step_e2e():
+        for m, L in sweep():
+            dx[m][L.k].copy_(hx[m][L.k], non_blocking=True)
+            w4.w4a16_gemm(dx[m][L.k], copies[L.name][0], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
+            hy[(m, L.name)].copy_(ys[(m, L.name)], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step_e2e()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step_e2e()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+
+    # ---- dense fp16 torch.matmul on the same shapes (cuBLAS), for comparison
+    dense = None
+    if not args.no_dense:
+        dw = {L.name: [torch.randn(L.n, L.k, device=dev, dtype=torch.float16) for _ in range(3)] for L in layers}
+
+        def step_dense():
+            use = {L.name: 0 for L in layers}
+            for m, L in sweep():
+                torch.matmul(xs[m][L.k], dw[L.name][use[L.name] % 3].t(), out=ys[(m, L.name)])
+                use[L.name] += 1
+
+        with torch.cuda.stream(stream):
+            step_dense()
+        stream.synchronize()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd, stream=stream):
+            step_dense()
+        dts = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                gd.replay()
+                b.record(stream)
+                if i >= args.warmup:
+                    dts.append((a, b))
+        stream.synchronize()
+        dms = sum(a.elapsed_time(b) for a, b in dts) / len(dts)
+        dense = {"value": round(flops_step / (dms * 1e-3) / 1e12, 2), "unit": UNIT, "ms_per_step": round(dms, 4),
+                 "kind": "torch.matmul fp16 dense weights (cuBLAS)"}
+        del dw, gd
+
+    # ---- CPU oracle on the host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        data, hxs = oracle_sample()
+        t, fl = time_oracle(data, hxs, workloads.DECODE_MS)
+        cpu = {"value": fl / t / 1e12, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
+               "sample": "the whole decode sweep (28 GEMMs) through the fp64 oracle, timed once",
+               "seconds": round(t, 2)}
+
+    t_roof = sum(max(alg_bytes(m, L.n, L.k, L.g) / (peaks["hbm_gbs"] * 1e9),
+                     gemm_flops(m, L.n, L.k) / (peaks["bf16_tflops"] * 1e12)) for m, L in sweep())
+    achieved = bytes_step / (ms_per_step * 1e-3) / 1e9
+    dec = [p for p in per if p["M"] <= 16]
+    dec_bytes = sum(alg_bytes(p["M"], L.n, L.k, L.g) for p in dec for L in layers if L.name == p["layer"])
+    dec_time = sum(p["us"] for p in dec) * 1e-6
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "gemms_per_step": len(sweep()),
+                   "l2": "flushed between timed steps (512 MB write); 3 weight copies per layer rotate within a step",
+                   "timing": "step captured as one CUDA graph, CUDA events per replay, max over ranks",
+                   "parallelism": f"replicas x{world}"},
+        "weight_gbs": round(wbytes_step / (ms_per_step * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                     "time_frac": round(t_roof / (ms_per_step * 1e-3), 4),
+                     "decode_m_le_16": {"achieved": round(dec_bytes / dec_time / 1e9, 1),
+                                        "frac": round(dec_bytes / dec_time / 1e9 / peaks["hbm_gbs"], 4)}},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": len(sweep()) * args.steps,
+        "clocks": clocks,
+        "dense_fp16": dense,
+        "offline": offline,
+        "per_launch": per,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_case(args):
+    """One GEMM configuration launched --steps times (for focused profiling); prints a short JSON line."""
+    import torch
+
+    import w4a16_group_quantized_gb300 as w4
+
+    m_s, name = args.case.split(":", 1)
+    m = int(m_s)
+    table = {L.name: L for L in workloads.DECODE_LAYERS + workloads.PREFILL_LAYERS + workloads.PARTIAL_LAYERS}
+    L = table[name]
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    W = torch.from_numpy(workloads.weights_f16(L.n, L.k)).to(dev)
+    qw, sc, zw = w4.w4_pack(W, L.g)
+    packed = w4.w4_repack(qw, sc, zw, L.n, L.k, L.g)
+    del W, qw, sc, zw
+    x = torch.from_numpy(workloads.activations_f16(m, L.k, outliers=L in workloads.PREFILL_LAYERS)).to(dev)
+    y = torch.empty((m, L.n), dtype=torch.float16, device=dev)
+    ws = torch.zeros(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        w4.w4a16_gemm(x, packed, L.n, L.k, L.g, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        w4.w4a16_gemm(x, packed, L.n, L.k, L.g, y=y, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_error(ws) == 0
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    bn, ctas, sched = w4.w4a16_gemm_plan(m, L.n, L.k, L.g)
+    print(json.dumps({"case": args.case, "us_per_launch_eager": round(us, 3), "block_n": bn, "schedule": sched,
+                      "ctas": ctas, "alg_bytes": alg_bytes(m, L.n, L.k, L.g), "flops": gemm_flops(m, L.n, L.k)}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense fp16 comparison")
+    ap.add_argument("--case", default=None, help="M:layer_name - run only that GEMM (for profiling)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.case:
+        return run_case(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

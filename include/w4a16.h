@@ -110,8 +110,8 @@ W4_API int w4_repack(const uint32_t *qw_dev, const void *scales_dev, const uint3
 
 /*
  * Bytes of device workspace w4a16_gemm needs for this problem on the current
- * device (error word, split-K tile counters and fp32 partial sums). Always
- * >= 256. Returns 0 for invalid sizes.
+ * device (error word, per-tile counters and fp32 partial tiles for the
+ * stream-K fixup). Always >= 256. Returns 0 for invalid sizes.
  */
 W4_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t g);
 
@@ -131,31 +131,35 @@ W4_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t g);
  *
  * Numerics: each weight is dequantized once to fp16, rounded once:
  * fp16((q - z) * s) with q - z formed exactly; products are accumulated in
- * fp32 on the tensor cores (tcgen05, accumulator in tensor memory); split-K
- * partial sums are added in fp32 in a fixed order; y is rounded to fp16
- * (nearest-even). Results are deterministic run to run.
+ * fp32 on the tensor cores (tcgen05, accumulator in tensor memory); pieces of
+ * a tile cut along K are added in fp32 in K order; y is rounded to fp16
+ * (nearest-even). Results are deterministic run to run on one device.
  */
 W4_API int w4a16_gemm(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K,
                int32_t g, void *y_dev, void *workspace_dev, size_t workspace_bytes, void *stream);
 
 /*
- * As w4a16_gemm with the tiling forced: block_n is the number of activation
- * rows per tile (16, 32, 64, 128 or 256; 0 = automatic) and splits the number
- * of K partitions (1..64; 0 = automatic). The workspace must be at least
- * w4a16_workspace_bytes_ex(M, N, K, g, block_n, splits). For tests and tuning.
+ * As w4a16_gemm with the schedule forced. block_n: activation rows per output
+ * tile (16, 32, 64, 128 or 256; 0 = automatic). ctas: number of persistent
+ * CTAs (1..65535; 0 = one per SM). schedule: 0 = automatic, 1 = stream-K
+ * (CTAs may cut a tile along K; the cut tiles are finished by a fixup through
+ * the workspace), 2 = whole tiles per CTA. The workspace must be at least
+ * w4a16_workspace_bytes_ex(M, N, K, g, block_n, ctas, schedule) bytes.
+ * Results are identical up to fp32 summation order. For tests and tuning.
  */
 W4_API int w4a16_gemm_ex(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K,
                   int32_t g, void *y_dev, void *workspace_dev, size_t workspace_bytes,
-                  int32_t block_n, int32_t splits, void *stream);
+                  int32_t block_n, int32_t ctas, int32_t schedule, void *stream);
 W4_API size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t g,
-                                int32_t block_n, int32_t splits);
+                                int32_t block_n, int32_t ctas, int32_t schedule);
 
 /*
- * The tiling w4a16_gemm would pick on the current device: writes block_n,
- * splits and the number of CTAs launched. Returns W4_OK or an error status.
+ * The schedule w4a16_gemm picks on the current device: writes block_n, the
+ * number of CTAs and the schedule (1 stream-K, 2 whole tiles).
+ * Returns W4_OK or an error status.
  */
 W4_API int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g,
-                    int32_t *block_n, int32_t *splits, int32_t *ctas);
+                    int32_t *block_n, int32_t *ctas, int32_t *schedule);
 
 /*
  * Reads and clears the device error word that GEMM kernels write into the

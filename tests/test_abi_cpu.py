@@ -55,15 +55,16 @@ def test_repacked_bytes_formula(lib):
 
 
 def test_workspace_sizes(lib):
-    # no split: error word + counters only
-    b = w4.w4a16_workspace_bytes_ex(512, 8192, 8192, 128, 256, 1)
-    assert b == 256 + 512  # error word block + 2 x 64 tile counters of 4 bytes
-    # forced split: partial sums S x M x Npad fp32
-    M, N, K, S = 16, 300, 1024, 4
-    b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 16, S)
-    assert b >= S * M * 384 * 4 + 256
+    # whole tiles: error word block + per-tile counters only
+    b = w4.w4a16_workspace_bytes_ex(512, 8192, 8192, 128, 256, 0, 2)
+    assert b == 256 + 512  # 2 x 64 tile counters of 4 bytes
+    # stream-K with P CTAs: plus two fp32 partial tiles (128 x block_n) per CTA
+    M, N, K, P = 16, 300, 1024, 4
+    b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 16, P, 1)
+    assert b == 256 + 256 + P * 2 * 128 * 16 * 4
     assert w4.w4a16_workspace_bytes(0, 1, 8, 8) == 0
-    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 1) == 0  # block_n must be 16..256, a power of two
+    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 0, 0) == 0  # block_n must be 16..256, a power of two
+    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 16, 0, 3) == 0  # no schedule 3
 
 
 def _vp(v):
@@ -87,10 +88,11 @@ def test_host_side_argument_checks(lib):
     assert lib.w4a16_gemm(fake, fake, 1, 1, 8, 8, fake, _vp(0x20010), 4096, None) == 3
     # workspace too small
     assert lib.w4a16_gemm(fake, fake, 1, 1, 8, 8, fake, ws, 16, None) == 4
-    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1024, 16, 4, None) == 4
-    # forced tiling out of range
-    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1 << 30, 48, 1, None) == 1
-    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1 << 30, 16, 65, None) == 1
+    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1024, 16, 4, 1, None) == 4
+    # forced schedule out of range
+    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1 << 30, 48, 1, 0, None) == 1
+    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1 << 30, 16, -1, 0, None) == 1
+    assert lib.w4a16_gemm_ex(fake, fake, 16, 300, 1024, 128, fake, ws, 1 << 30, 16, 1, 7, None) == 1
     # pack / repack
     assert lib.w4_pack(None, 4, 8, 8, fake, fake, fake, None) == 1
     assert lib.w4_pack(fake, 4, 8, 7, fake, fake, fake, None) == 1

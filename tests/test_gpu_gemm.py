@@ -35,27 +35,28 @@ def layer(N, K, g, seed=0):
     return _cache[key]
 
 
-def run_gemm(x, packed, N, K, g, block_n=0, splits=0, ws=None):
+def run_gemm(x, packed, N, K, g, block_n=0, ctas=0, schedule=0, ws=None):
     xd = torch.from_numpy(x).cuda()
-    if block_n or splits:
-        y = w4.w4a16_gemm_ex(xd, packed, N, K, g, block_n, splits, workspace=ws)
+    if block_n or ctas or schedule:
+        y = w4.w4a16_gemm_ex(xd, packed, N, K, g, block_n, ctas, schedule, workspace=ws)
     else:
         y = w4.w4a16_gemm(xd, packed, N, K, g, workspace=ws)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
 
-def check(M, N, K, g, block_n=0, splits=0, rows=None, outliers=False, seed_x=1):
+def check(M, N, K, g, block_n=0, ctas=0, schedule=0, rows=None, outliers=False, seed_x=1):
     qw, s, zw, packed, wn = layer(N, K, g)
     x = workloads.activations_f16(M, K, seed=seed_x, outliers=outliers)
     ws = w4.Workspace()
-    y = run_gemm(x, packed, N, K, g, block_n, splits, ws)
+    y = run_gemm(x, packed, N, K, g, block_n, ctas, schedule, ws)
     assert w4.w4_last_device_error(ws) == 0
     if rows is None:
         rows = np.arange(M)
     yref = oracle.gemm(x, qw, s, zw, N, K, g, rows=rows)
     tol = gemm_tolerance(x[rows], wn)
-    return assert_within_tolerance(y[rows], yref, tol, f"M={M} N={N} K={K} g={g} bn={block_n} S={splits}")
+    return assert_within_tolerance(y[rows], yref, tol,
+                                   f"M={M} N={N} K={K} g={g} bn={block_n} ctas={ctas} schedule={schedule}")
 
 
 # ------------------------------------------------------------ small, every element
@@ -79,16 +80,18 @@ def test_tile_edges(M):
 
 
 @pytest.mark.parametrize("block_n", [16, 32, 64, 128, 256])
-@pytest.mark.parametrize("splits", [1, 2, 3, 7])
-def test_forced_tilings(block_n, splits):
-    check(20, 260, 1024, 128, block_n=block_n, splits=splits)
+@pytest.mark.parametrize("ctas,schedule", [(1, 1), (2, 1), (3, 1), (7, 1), (13, 1), (64, 1), (1, 2), (5, 2)])
+def test_forced_schedules(block_n, ctas, schedule):
+    # 3 n-tiles x 16 K blocks (x m-tiles): stream-K cuts tiles at many places, incl. one CTA holding
+    # the tail of one tile and the head of the next, and CTAs whose whole range sits inside one tile
+    check(20, 260, 1024, 128, block_n=block_n, ctas=ctas, schedule=schedule)
 
 
 @pytest.mark.parametrize("g", [8, 16, 24, 32, 40, 96, 192, 256, 1024])
 def test_group_sizes(g):
     # 64 % g != 0 or g % 64 != 0 takes the per-chunk group path; K = 1000 leaves a partial last group
     check(9, 200, 1000, g)
-    check(9, 200, 1000, g, block_n=16, splits=3)
+    check(9, 200, 1000, g, block_n=16, ctas=3, schedule=1)
 
 
 def test_one_hot_rows_return_rounded_weights_exactly():
@@ -100,9 +103,9 @@ def test_one_hot_rows_return_rounded_weights_exactly():
         x[i, k] = 1.0
     wd = oracle.dequant(qw, s, zw, N, K, g)
     expect = wd[:, ks].T.astype(np.float16)  # (q - z) * s is exact in fp64; one rounding to fp16
-    for bn, sp in [(0, 0), (16, 1), (16, 4), (256, 1), (64, 3)]:
-        y = run_gemm(x, packed, N, K, g, bn, sp)
-        assert (y.view(np.uint16) == expect.view(np.uint16)).all(), (bn, sp)
+    for bn, ctas, sch in [(0, 0, 0), (16, 1, 2), (16, 4, 1), (256, 1, 1), (64, 5, 1), (16, 11, 1)]:
+        y = run_gemm(x, packed, N, K, g, bn, ctas, sch)
+        assert (y.view(np.uint16) == expect.view(np.uint16)).all(), (bn, ctas, sch)
 
 
 def test_q_equal_z_gives_exact_zero():
@@ -125,13 +128,13 @@ def test_deterministic_and_workspace_reuse():
     qw, s, zw, packed, wn = layer(N, K, g)
     x = torch.from_numpy(workloads.activations_f16(M, K)).cuda()
     ws = w4.Workspace()
-    outs = [w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 5, workspace=ws).clone() for _ in range(3)]
+    outs = [w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 5, 1, workspace=ws).clone() for _ in range(3)]
     outs += [w4.w4a16_gemm(x, packed, N, K, g, workspace=ws).clone() for _ in range(2)]
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     assert torch.equal(outs[3], outs[4])
     # counters were left at zero: a fresh workspace gives the same bits
-    y2 = w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 5, workspace=w4.Workspace())
+    y2 = w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 5, 1, workspace=w4.Workspace())
     assert torch.equal(outs[0], y2)
     assert w4.w4_last_device_error(ws) == 0
 
@@ -163,7 +166,8 @@ def test_host_errors_on_device_tensors():
     assert e.value.status == 2
     x = torch.zeros(16, K, dtype=torch.float16, device="cuda")
     with pytest.raises(w4.W4Error) as e:
-        w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 4, workspace=torch.zeros(256, dtype=torch.uint8, device="cuda"))
+        w4.w4a16_gemm_ex(x, packed, N, K, g, 16, 4, 1,
+                         workspace=torch.zeros(256, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 4
 
 
@@ -187,3 +191,23 @@ def test_decode_sweep_layers(L):
 def test_prefill_layers_sampled(L):
     for M in (256, 4096):
         check(M, L.n, L.k, L.g, rows=_sample_rows(M, 8), outliers=True)
+
+
+@pytest.mark.parametrize("block_n,ctas,schedule", [(256, 80, 2), (256, 0, 1), (128, 0, 1), (64, 0, 1), (16, 0, 1)])
+def test_repeated_launches_bit_identical(block_n, ctas, schedule):
+    # The schedule is deterministic, so back-to-back launches must agree bit for bit; a pipeline
+    # hazard (a stage or slot read before its data landed) shows up here as a differing launch.
+    N, K, M = 10240, 8192, 256
+    qw, s, zw, packed, wn = layer(N, K, 128)
+    x = torch.from_numpy(workloads.activations_f16(M, K, outliers=True)).cuda()
+    ws = w4.Workspace()
+    first = w4.w4a16_gemm_ex(x, packed, N, K, 128, block_n, ctas, schedule, workspace=ws)
+    ndiff = 0
+    for _ in range(30):
+        y = w4.w4a16_gemm_ex(x, packed, N, K, 128, block_n, ctas, schedule, workspace=ws)
+        ndiff += int(not torch.equal(y, first))
+    assert ndiff == 0
+    rows = np.array([0, 17, 130, 255])
+    yref = oracle.gemm(x.cpu().numpy()[rows], qw, s, zw, N, K, 128)
+    assert_within_tolerance(first.cpu().numpy()[rows], yref, gemm_tolerance(x.cpu().numpy()[rows], wn), "repeat")
+    assert w4.w4_last_device_error(ws) == 0

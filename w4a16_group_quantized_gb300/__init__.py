@@ -61,9 +61,9 @@ def load() -> ctypes.CDLL:
             "w4_repacked_bytes": ([I64, I64, I32], SZ),
             "w4_repack": ([P, P, P, I64, I64, I32, P, P], ctypes.c_int),
             "w4a16_workspace_bytes": ([I64, I64, I64, I32], SZ),
-            "w4a16_workspace_bytes_ex": ([I64, I64, I64, I32, I32, I32], SZ),
+            "w4a16_workspace_bytes_ex": ([I64, I64, I64, I32, I32, I32, I32], SZ),
             "w4a16_gemm": ([P, P, I64, I64, I64, I32, P, P, SZ, P], ctypes.c_int),
-            "w4a16_gemm_ex": ([P, P, I64, I64, I64, I32, P, P, SZ, I32, I32, P], ctypes.c_int),
+            "w4a16_gemm_ex": ([P, P, I64, I64, I64, I32, P, P, SZ, I32, I32, I32, P], ctypes.c_int),
             "w4a16_gemm_plan": ([I64, I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                                  ctypes.POINTER(I32)], ctypes.c_int),
             "w4_last_device_error": ([P, P], ctypes.c_int),
@@ -140,12 +140,12 @@ def w4a16_workspace_bytes(M: int, N: int, K: int, g: int) -> int:
     return int(load().w4a16_workspace_bytes(M, N, K, g))
 
 
-def w4a16_workspace_bytes_ex(M: int, N: int, K: int, g: int, block_n: int, splits: int) -> int:
-    return int(load().w4a16_workspace_bytes_ex(M, N, K, g, block_n, splits))
+def w4a16_workspace_bytes_ex(M: int, N: int, K: int, g: int, block_n: int, ctas: int, schedule: int) -> int:
+    return int(load().w4a16_workspace_bytes_ex(M, N, K, g, block_n, ctas, schedule))
 
 
 def w4a16_gemm_plan(M: int, N: int, K: int, g: int):
-    """(block_n, splits, ctas) that w4a16_gemm picks on the current device."""
+    """(block_n, ctas, schedule) that w4a16_gemm picks on the current device (schedule 1 stream-K, 2 whole tiles)."""
     b, s, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check(load().w4a16_gemm_plan(M, N, K, g, ctypes.byref(b), ctypes.byref(s), ctypes.byref(c)), "w4a16_gemm_plan")
     return b.value, s.value, c.value
@@ -164,7 +164,7 @@ class Workspace:
         return self.buf
 
 
-def _gemm_common(x, packed, N, K, g, y, workspace, block_n, splits, stream):
+def _gemm_common(x, packed, N, K, g, y, workspace, block_n, ctas, schedule, stream):
     if x.dtype != torch.float16 or x.dim() != 2 or x.shape[1] != K:
         raise ValueError("x must be fp16 [M, K]")
     M = x.shape[0]
@@ -172,7 +172,7 @@ def _gemm_common(x, packed, N, K, g, y, workspace, block_n, splits, stream):
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     elif y.dtype != torch.float16 or tuple(y.shape) != (M, N):
         raise ValueError("y must be fp16 [M, N]")
-    need = w4a16_workspace_bytes_ex(M, N, K, g, block_n, splits)
+    need = w4a16_workspace_bytes_ex(M, N, K, g, block_n, ctas, schedule)
     if need == 0:
         raise W4Error(1, "w4a16_workspace_bytes")
     if workspace is None:
@@ -180,12 +180,12 @@ def _gemm_common(x, packed, N, K, g, y, workspace, block_n, splits, stream):
     ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
     nbytes = ws.numel() * ws.element_size()
     lib = load()
-    if block_n == 0 and splits == 0:
+    if block_n == 0 and ctas == 0 and schedule == 0:
         rc = lib.w4a16_gemm(_dev(x, "x"), _dev(packed, "packed"), M, N, K, g, _dev(y, "y"), _dev(ws, "workspace"),
                             nbytes, _stream(stream))
     else:
         rc = lib.w4a16_gemm_ex(_dev(x, "x"), _dev(packed, "packed"), M, N, K, g, _dev(y, "y"),
-                               _dev(ws, "workspace"), nbytes, block_n, splits, _stream(stream))
+                               _dev(ws, "workspace"), nbytes, block_n, ctas, schedule, _stream(stream))
     _check(rc, "w4a16_gemm")
     return y
 
@@ -193,12 +193,14 @@ def _gemm_common(x, packed, N, K, g, y, workspace, block_n, splits, stream):
 def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: int, y: torch.Tensor | None = None,
                workspace=None, stream=None) -> torch.Tensor:
     """y fp16 [M,N] = x fp16 [M,K] . dequant(packed)^T. ``workspace``: a Workspace or a zeroed uint8 tensor."""
-    return _gemm_common(x, packed, N, K, g, y, workspace, 0, 0, stream)
+    return _gemm_common(x, packed, N, K, g, y, workspace, 0, 0, 0, stream)
 
 
-def w4a16_gemm_ex(x, packed, N, K, g, block_n: int, splits: int, y=None, workspace=None, stream=None):
-    """w4a16_gemm with the tiling forced (block_n in {16,32,64,128,256}, splits >= 1; 0 = automatic)."""
-    return _gemm_common(x, packed, N, K, g, y, workspace, block_n, splits, stream)
+def w4a16_gemm_ex(x, packed, N, K, g, block_n: int = 0, ctas: int = 0, schedule: int = 0, y=None, workspace=None,
+                  stream=None):
+    """w4a16_gemm with the schedule forced: block_n in {16,32,64,128,256}, ctas >= 1, schedule 1 stream-K or
+    2 whole tiles (0 = automatic for each)."""
+    return _gemm_common(x, packed, N, K, g, y, workspace, block_n, ctas, schedule, stream)
 
 
 def w4_last_device_error(workspace, stream=None) -> int:

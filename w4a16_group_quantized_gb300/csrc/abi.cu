@@ -43,11 +43,12 @@ int check_gemm_args(const void *x, const void *packed, int64_t M, int64_t N, int
 }
 
 int gemm_impl(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y, void *ws,
-              size_t ws_bytes, int32_t block_n, int32_t splits, void *stream) {
+              size_t ws_bytes, int32_t block_n, int32_t ctas, int32_t schedule, void *stream) {
   const int rc = check_gemm_args(x, packed, M, N, K, g, y, ws);
   if (rc != W4_OK) return rc;
   w4::GemmPlan plan;
-  if (!w4::make_gemm_plan(M, N, K, g, block_n, splits, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
+  if (!w4::make_gemm_plan(M, N, K, g, block_n, ctas, schedule, num_sms_current_device(), &plan))
+    return W4_ERR_INVALID_ARG;
   if (ws_bytes < plan.workspace_bytes) return W4_ERR_WORKSPACE_TOO_SMALL;
   bool encode_failed = false;
   const cudaError_t e =
@@ -103,37 +104,41 @@ int w4_repack(const uint32_t *qw_dev, const void *scales_dev, const uint32_t *ze
   return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t g, int32_t block_n, int32_t splits) {
+size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t g, int32_t block_n, int32_t ctas,
+                                int32_t schedule) {
   if (M < 1 || N < 1 || K < 1 || !valid_group(g) || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
   w4::GemmPlan plan;
-  if (!w4::make_gemm_plan(M, N, K, g, block_n, splits, num_sms_current_device(), &plan)) return 0;
+  if (!w4::make_gemm_plan(M, N, K, g, block_n, ctas, schedule, num_sms_current_device(), &plan)) return 0;
   return plan.workspace_bytes;
 }
 
 size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t g) {
-  return w4a16_workspace_bytes_ex(M, N, K, g, 0, 0);
+  return w4a16_workspace_bytes_ex(M, N, K, g, 0, 0, 0);
 }
 
-int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int32_t *block_n, int32_t *splits, int32_t *ctas) {
-  if (!block_n || !splits || !ctas) return W4_ERR_INVALID_ARG;
+int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int32_t *block_n, int32_t *ctas,
+                    int32_t *schedule) {
+  if (!block_n || !ctas || !schedule) return W4_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || !valid_group(g) || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return W4_ERR_INVALID_ARG;
   w4::GemmPlan plan;
-  if (!w4::make_gemm_plan(M, N, K, g, 0, 0, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
+  if (!w4::make_gemm_plan(M, N, K, g, 0, 0, 0, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
   *block_n = plan.block_n;
-  *splits = plan.splits;
   *ctas = plan.ctas;
+  *schedule = plan.gran == 1 ? 1 : 2;
   return W4_OK;
 }
 
 int w4a16_gemm(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g, void *y_dev,
                void *workspace_dev, size_t workspace_bytes, void *stream) {
-  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, 0, 0, stream);
+  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, 0, 0, 0, stream);
 }
 
 int w4a16_gemm_ex(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g, void *y_dev,
-                  void *workspace_dev, size_t workspace_bytes, int32_t block_n, int32_t splits, void *stream) {
-  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, block_n, splits, stream);
+                  void *workspace_dev, size_t workspace_bytes, int32_t block_n, int32_t ctas, int32_t schedule,
+                  void *stream) {
+  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, block_n, ctas, schedule,
+                   stream);
 }
 
 int w4_last_device_error(void *workspace_dev, void *stream) {

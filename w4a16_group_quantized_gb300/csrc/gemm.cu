@@ -1,21 +1,30 @@
 // w4a16_gemm: y[M,N] = x[M,K] . dequant(Wq)[N,K]^T on sm_103a tensor cores.
 //
-// One CTA computes a 128 (weight rows n) x BN (activation rows m) tile of y^T
-// over a range of K ("swap-AB": the weights sit on the MMA's M = 128 side, the
-// tokens on its N side, so a batch of 1..16 tokens still fills an MMA).
+// Output tiles are 128 (weight rows n) x BN (activation rows m) tiles of y^T
+// ("swap-AB": the weights sit on the MMA's M = 128 side, the tokens on its N
+// side, so a batch of 1..16 tokens still fills an MMA). The kernel is
+// persistent: one CTA per SM walks a contiguous range of (tile, 64-wide K
+// block) units, so the work is split evenly whatever the number of tiles
+// (stream-K); a tile cut between CTAs is finished by a fixup (below).
 //
-// Warp roles (one CTA, 64 + 128 * kDqGroups threads):
-//   warp 0, lane 0  producer: per 64-wide K block, one TMA tensor copy of the
-//                   x tile (128-byte swizzle, zero fill outside [M, K]) and
-//                   two bulk copies of the weight tile (4 KB of codes) and its
-//                   group records, all completing on one mbarrier.
-//   warp 1          allocates tensor memory; lane 0 issues tcgen05.mma.
-//   warps 2..       dequant warpgroup(s): thread r owns weight row r; it turns
-//                   the row's 64 codes into fp16 (q - z) * s and stores them
-//                   into tensor memory (tcgen05.st), where they are the MMA's
-//                   A operand; shared memory only ever holds 4-bit codes.
-//                   After the K loop the same warps read the fp32 accumulator
-//                   out of tensor memory and write y (or split-K partials).
+// Warp roles (one CTA per SM):
+//   4 producer warps (lane 0) take the 64-wide K blocks in turn: per block one
+//                   TMA tensor copy of the x tile (128-byte swizzle, zero fill
+//                   outside [M, K]) and two bulk copies (4 KB of codes, group
+//                   records), all completing on the stage's mbarrier.
+//   1-4 MMA warps   (lane 0) take whole K blocks in turn, each accumulating its
+//                   blocks into its own tensor-memory accumulator; the first
+//                   one also allocates tensor memory.
+//   2-4 dequant warpgroups take K blocks in turn: thread r owns weight row r;
+//                   it turns the row's 64 codes into fp16 (q - z) * s and stores
+//                   them into tensor memory (tcgen05.st), where they are the
+//                   MMA's A operand; shared memory only ever holds 4-bit codes.
+//   1 epilogue warpgroup: reads a finished tile's accumulators (double-buffered
+//                   for BN <= 64, so the next tile's MMAs overlap it), adds the
+//                   MMA warps' parts in a fixed order and writes y, or an fp32
+//                   partial tile when the tile was cut between CTAs.
+// Several producer and MMA warps are needed because a single thread issues a
+// bulk copy only every ~350 cycles and a tcgen05 instruction every ~100.
 //
 // This is the GB300 form of the techniques the Marlin post lists (prefetch,
 // activation reuse, asynchronous weight loads, dequant interleaved with the
@@ -24,10 +33,10 @@
 // dequant warps run ahead of the asynchronous MMAs through a ring of tensor-
 // memory slots.
 //
-// Split-K: with S > 1 the CTAs of one output tile each write fp32 partials to
-// the workspace; the last CTA to arrive on the tile's counter adds them in
-// split order 0..S-1 (deterministic) and writes y. Nothing ever waits on
-// another CTA. Every mbarrier wait is bounded (ptx.cuh).
+// Fixup of a cut tile: each CTA holding a piece writes it (fp32) to the
+// workspace and counts itself in on the tile's counter; the last to arrive
+// adds the pieces in K order (deterministic) and writes y. Nothing ever waits
+// on another CTA. Every mbarrier wait is bounded (ptx.cuh).
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -52,32 +61,69 @@ struct Cfg {
   static constexpr int kXBytes = BN * 128;  // BN rows x 64 fp16
   static constexpr int kMetaBytes = GENERAL ? kMaxRecs * kRecBytes : kRecBytes;
   static constexpr int kStageBytes = (kXBytes + kTileBytes + kMetaBytes + 1023) / 1024 * 1024;
-  // Two CTAs per SM for BN <= 128 (about 110 KB of stages each), one for BN = 256.
-  static constexpr int kSmemBudget = BN == 256 ? 200 * 1024 : 108 * 1024;
+  static constexpr int kSmemBudget = 200 * 1024;  // one CTA per SM
+  // One thread can issue a bulk copy only every ~350 cycles, whatever its size, so four producer
+  // warps take the K blocks in turn (three copies each).
+  static constexpr int kProducers = 4;
+  // Dequant warpgroups: narrow (HBM-bound) tiles need four to hide each one's latency; wide
+  // (tensor-bound) tiles need a K block only every 256-512 cycles and keep the registers instead.
+  static constexpr int kDqGroups = BN <= 64 ? 4 : 2;
+  // A producer / dequant warpgroup waits only on the stages (and tensor-memory slots) of its own K
+  // blocks. An mbarrier parity wait is only sound for a waiter that sees every phase of that
+  // barrier: if a ring's size were not a multiple of the number of such waiters, successive uses of
+  // one stage would go to different waiters, and one that ran ahead could take the previous, still
+  // landing phase for its own (bulk copies complete out of order). So the rings are multiples of 4.
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kASlots = 4;  // tensor-memory slots of dequantized weights (32 columns each)
-  static constexpr int kDCols = BN < 32 ? 32 : BN;
-  static constexpr int kACol0 = kDCols;
-  static constexpr int kTmemCols = pow2_at_least(kDCols + kASlots * 32);
-  static constexpr int kDqGroups = 1;
-  static constexpr int kThreads = 64 + 128 * kDqGroups;
+  static constexpr int kStages = (kStagesRaw > 16 ? 16 : kStagesRaw) / 4 * 4;
+  static constexpr int kASlots = 8;    // tensor-memory slots of dequantized weights (32 columns each)
+  // Each tcgen05 instruction (mma, commit, fence) costs the issuing thread ~100 cycles whatever its
+  // size, so narrow tiles give the K blocks in turn to several issuing warps, each accumulating into
+  // its own tensor-memory accumulator (summed in a fixed order by the epilogue).
+  // (25 warps leave 72 registers a thread: 7 warps share one sub-partition's 16K registers.)
+  static constexpr int kMmaWarps = BN <= 32 ? 4 : (BN <= 128 ? 2 : 1);
+  static constexpr int kDBufs = BN <= 64 ? 2 : 1;  // accumulator sets (epilogue overlaps the next tile)
+  static constexpr int kDStride = BN < 32 ? 32 : BN;
+  static constexpr int kACol0 = kDBufs * kMmaWarps * kDStride;
+  static constexpr int kTmemCols = pow2_at_least(kACol0 + kASlots * 32);
+  static constexpr int kMmaWarp0 = kProducers;
+  static constexpr int kDqWarp0 = kMmaWarp0 + kMmaWarps;
+  static constexpr int kEpiWarp0 = kDqWarp0 + 4 * kDqGroups;
+  static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
-  static_assert(kStages >= 2, "pipeline needs at least two stages");
+  static_assert(kStages >= 4 && kStages % kDqGroups == 0 && kStages % kProducers == 0,
+                "stage ring: a multiple of the producers and of the dequant groups");
+  static_assert(kASlots % kDqGroups == 0, "tensor-memory slot ring: a multiple of the dequant groups");
+  static_assert(kStages % kMmaWarps == 0 && kASlots % kMmaWarps == 0, "each ring slot keeps one issuing warp");
   static_assert(kTmemCols <= 512, "tensor memory budget");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
 };
 
+// Work decomposition. A unit is one 64-wide K block of one output tile (128 weight rows x BN
+// activation rows); units are numbered tile-major: u = tile * KB + kb, tile = t * MT + mt.
+// CTA c owns the contiguous units [begin(c), begin(c+1)), cut at multiples of `gran` units
+// (gran = 1: stream-K, any cut; gran = KB: whole tiles only).
 struct Params {
   const uint8_t *codes;  // tile region of the packed weights
   const uint8_t *meta;   // group-record region of the packed weights
   __half *y;
-  float *partials;  // [S][M][Npad]
-  uint32_t *counters;
+  float *pieces;         // [P][2][128][BN] fp32 partial tiles (first and last segment of each CTA)
+  uint32_t *counters;    // [tiles] arrivals per split tile
   uint32_t *err;
-  int M, N, K, g, G, NT, KB, MT, S;
-  int Npad;
+  int M, N, K, g, G, NT, KB, MT;
+  int P;                 // CTAs
+  int gran;              // units per scheduling grain
+  int64_t grains;        // total units / gran
 };
+
+__device__ __forceinline__ int64_t range_begin(const Params &p, int c) {
+  return static_cast<int64_t>(c) * p.grains / p.P * p.gran;
+}
+
+// The CTA whose range holds unit u: the largest c with range_begin(c) <= u.
+__device__ __forceinline__ int owner_of(const Params &p, int64_t u) {
+  const int64_t v = u / p.gran;
+  return static_cast<int>(((v + 1) * p.P - 1) / p.grains);
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -137,9 +183,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // Waits ignoring the abort flag (used only to drain in-flight copies/MMAs before exit).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 1000000u)) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) return;
   }
+}
+
+__device__ __forceinline__ void st_f32x4(float *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  *reinterpret_cast<float4 *>(p) = make_float4(__uint_as_float(a), __uint_as_float(b), __uint_as_float(c),
+                                               __uint_as_float(d));
 }
 
 template <int BN, bool GENERAL>
@@ -151,7 +202,9 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
   __shared__ __align__(8) uint64_t afull_bar[C::kASlots];
   __shared__ __align__(8) uint64_t aempty_bar[C::kASlots];
-  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ __align__(8) uint64_t dfull_bar[C::kDBufs];
+  __shared__ __align__(8) uint64_t dempty_bar[C::kDBufs];
+  __shared__ __align__(8) uint64_t drain_bar[C::kMmaWarps];
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t abort_sh;
   __shared__ uint32_t last_sh;
@@ -161,16 +214,9 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
   const int lane = threadIdx.x % 32;
   volatile uint32_t *abort_flag = &abort_sh;
 
-  // tile of this CTA: m fastest, then n, then the K split
-  int bid = blockIdx.x;
-  const int mt = bid % p.MT;
-  bid /= p.MT;
-  const int t = bid % p.NT;
-  const int sk = bid / p.NT;
-  const int kb0 = static_cast<int>(static_cast<int64_t>(sk) * p.KB / p.S);
-  const int kb1 = static_cast<int>(static_cast<int64_t>(sk + 1) * p.KB / p.S);
-  const int nkb = kb1 - kb0;
-  const int m0 = mt * BN;
+  const int cta = blockIdx.x;
+  const int64_t u0 = range_begin(p, cta);
+  const int nu = static_cast<int>(range_begin(p, cta + 1) - u0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -181,12 +227,16 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
       mbar_init(smem_u32(&afull_bar[a]), 128);
       mbar_init(smem_u32(&aempty_bar[a]), 1);
     }
-    mbar_init(smem_u32(&acc_bar), 1);
+    for (int d = 0; d < C::kDBufs; ++d) {
+      mbar_init(smem_u32(&dfull_bar[d]), C::kMmaWarps);
+      mbar_init(smem_u32(&dempty_bar[d]), 128);
+    }
+    for (int w = 0; w < C::kMmaWarps; ++w) mbar_init(smem_u32(&drain_bar[w]), 1);
     abort_sh = 0;
     last_sh = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == C::kMmaWarp0) {
     tmem_alloc(smem_u32(&tmem_base_sh), C::kTmemCols);
     tmem_relinquish();
   }
@@ -196,18 +246,22 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp < C::kProducers) {
+    // ------------------------------------------------------------ producers
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
-      const uint8_t *codes = p.codes + static_cast<int64_t>(t) * p.KB * kTileBytes;
-      const uint8_t *meta = p.meta + static_cast<int64_t>(t) * p.G * kRecBytes;
-      int it = 0;
-      for (; it < nkb; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
+      // producer warp pw loads units pw, pw + P, ...; coordinates advance without divisions:
+      // u = (t * MT + mt) * KB + kb
+      const int pw = warp;
+      int kb = static_cast<int>((u0 + pw) % p.KB);
+      const int tile0 = static_cast<int>((u0 + pw) / p.KB);
+      int t = tile0 / p.MT;
+      int mt = tile0 % p.MT;
+      int i = pw;
+      for (; i < nu; i += C::kProducers) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (i / C::kStages) & 1;
         if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag, p.err)) break;
-        const int kb = kb0 + it;
         const int kfirst = kb * kTK;
         const int jlo = min(kfirst / p.g, p.G - 1);
         int nrec = 1;
@@ -215,69 +269,99 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
         const uint32_t stage = smem_base + s * C::kStageBytes;
         const uint32_t bar = smem_u32(&full_bar[s]);
         mbar_arrive_expect_tx(bar, C::kXBytes + kTileBytes + nrec * kRecBytes);
-        tma_load_2d(stage, &x_map, kfirst, m0, bar);
-        bulk_g2s(stage + C::kXBytes, codes + static_cast<int64_t>(kb) * kTileBytes, kTileBytes, bar, pol_stream);
-        bulk_g2s(stage + C::kXBytes + kTileBytes, meta + static_cast<int64_t>(jlo) * kRecBytes, nrec * kRecBytes,
-                 bar, pol_stream);
+        tma_load_2d(stage, &x_map, kfirst, mt * BN, bar);
+        bulk_g2s(stage + C::kXBytes, p.codes + (static_cast<int64_t>(t) * p.KB + kb) * kTileBytes, kTileBytes, bar,
+                 pol_stream);
+        bulk_g2s(stage + C::kXBytes + kTileBytes, p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes,
+                 nrec * kRecBytes, bar, pol_stream);
+        kb += C::kProducers;
+        while (kb >= p.KB) {
+          kb -= p.KB;
+          if (++mt == p.MT) {
+            mt = 0;
+            ++t;
+          }
+        }
       }
       if (*abort_flag) {
-        // let every copy already issued land before the CTA's shared memory goes away
-        for (int i = max(0, it - C::kStages); i < it; ++i)
-          drain_wait(smem_u32(&full_bar[i % C::kStages]), (i / C::kStages) & 1);
+        // let every copy this warp issued land before the CTA's shared memory goes away
+        for (int j = i - C::kProducers; j >= 0 && j >= i - C::kStages; j -= C::kProducers)
+          drain_wait(smem_u32(&full_bar[j % C::kStages]), (j / C::kStages) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp < C::kDqWarp0) {
+    // ---------------------------------------------------------- MMA issuers
+    // issuing warp w takes the K blocks i = w, w + kMmaWarps, ... into its own accumulator; every
+    // issuer follows the segments (tiles) to wait for a free accumulator set and to close it
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(128, BN);
-      for (int it = 0; it < nkb; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        const int a = it % C::kASlots;
-        const uint32_t aph = (it / C::kASlots) & 1;
-        if (!mbar_wait(smem_u32(&full_bar[s]), ph, abort_flag, p.err)) break;
-        if (!mbar_wait(smem_u32(&afull_bar[a]), aph, abort_flag, p.err)) break;
-        tc_fence_after();
-        const uint64_t bdesc = sw128_kmajor_desc(smem_base + s * C::kStageBytes);
-#pragma unroll
-        for (int kk = 0; kk < kTK / 16; ++kk) {
-          // A: 128 x 16 fp16 in tensor memory (8 columns per 16 K); B: 16 K-columns of the x tile (32 bytes)
-          mma_f16_ts(tmem, tmem + C::kACol0 + a * 32 + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                     (it | kk) != 0);
+      const int w = warp - C::kMmaWarp0;
+      int kb = static_cast<int>(u0 % p.KB);
+      int seg = 0;
+      bool own_first = true;  // the next own block is this issuer's first in the segment
+      int i = 0;
+      for (; i < nu; ++i) {
+        const bool first = i == 0 || kb == 0;
+        const bool last = i == nu - 1 || kb == p.KB - 1;
+        const int db = seg % C::kDBufs;
+        if (first) {
+          if (!mbar_wait(smem_u32(&dempty_bar[db]), ((seg / C::kDBufs) & 1) ^ 1, abort_flag, p.err)) break;
+          own_first = true;
         }
-        mma_commit(smem_u32(&empty_bar[s]));
-        mma_commit(smem_u32(&aempty_bar[a]));
+        if (i % C::kMmaWarps == w) {
+          const int s = i % C::kStages;
+          const int a = i % C::kASlots;
+          // the dequant group arrives on afull only after it saw this stage's copies land (full), so
+          // the x tile the MMA reads is in shared memory too
+          if (!mbar_wait(smem_u32(&afull_bar[a]), (i / C::kASlots) & 1, abort_flag, p.err)) break;
+          tc_fence_after();
+          const uint64_t bdesc = sw128_kmajor_desc(smem_base + s * C::kStageBytes);
+          const uint32_t dcol = tmem + (db * C::kMmaWarps + w) * C::kDStride;
+#pragma unroll
+          for (int kk = 0; kk < kTK / 16; ++kk) {
+            // A: 128 x 16 fp16 in tensor memory (8 columns per 16 K); B: 16 K-columns of the x tile
+            mma_f16_ts(dcol, tmem + C::kACol0 + a * 32 + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), idesc,
+                       (own_first && kk == 0) ? 0u : 1u);
+          }
+          own_first = false;
+          mma_commit(smem_u32(&empty_bar[s]));
+          mma_commit(smem_u32(&aempty_bar[a]));
+        }
+        if (last) {
+          mma_commit(smem_u32(&dfull_bar[db]));
+          ++seg;
+        }
+        if (++kb == p.KB) kb = 0;
       }
-      mma_commit(smem_u32(&acc_bar));
-      if (*abort_flag) drain_wait(smem_u32(&acc_bar), 0);
+      if (*abort_flag) {
+        mma_commit(smem_u32(&drain_bar[w]));
+        drain_wait(smem_u32(&drain_bar[w]), 0);
+      }
     }
-  } else {
-    // ------------------------------------------------- dequant + epilogue
-    const int dq = (warp - 2) / 4;
+  } else if (warp < C::kEpiWarp0) {
+    // ------------------------------------------------------------- dequant
+    const int dq = (warp - C::kDqWarp0) / 4;
     const int lq = warp % 4;  // tensor-memory lane quarter this warp may access
     const int r = lq * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
-    for (int it = dq; it < nkb; it += C::kDqGroups) {
-      const int s = it % C::kStages;
-      const uint32_t ph = (it / C::kStages) & 1;
-      const int a = it % C::kASlots;
-      const uint32_t aph = (it / C::kASlots) & 1;
-      if (!warp_wait(smem_u32(&full_bar[s]), ph, abort_flag, p.err)) break;
+    int kb = static_cast<int>((u0 + dq) % p.KB);  // K block of unit i, advanced without divisions
+    for (int i = dq; i < nu; i += C::kDqGroups) {
+      const int s = i % C::kStages;
+      const int a = i % C::kASlots;
+      if (!warp_wait(smem_u32(&full_bar[s]), (i / C::kStages) & 1, abort_flag, p.err)) break;
       const uint32_t codes = smem_base + s * C::kStageBytes + C::kXBytes;
       const uint32_t meta = codes + kTileBytes;
       const uint4 w0 = lds128(codes + r * 16);
       const uint4 w1 = lds128(codes + 2048 + r * 16);
       const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       uint32_t out[32];
-      if (!warp_wait(smem_u32(&aempty_bar[a]), aph ^ 1, abort_flag, p.err)) break;
-      tc_fence_after();
       if (!GENERAL) {
         const uint32_t z = (lds8(meta + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
         const GroupConsts c = group_consts(lds16(meta + 2 * r), z);
 #pragma unroll
         for (int ci = 0; ci < 8; ++ci) dequant_word(words[ci], c, &out[4 * ci]);
       } else {
-        const int kfirst = (kb0 + it) * kTK;
+        const int kfirst = kb * kTK;
         const int jlo = min(kfirst / p.g, p.G - 1);
         int j = jlo;
 #pragma unroll
@@ -289,66 +373,118 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
           dequant_word(words[ci], group_consts(lds16(rec + 2 * r), z), &out[4 * ci]);
         }
       }
+      if (!warp_wait(smem_u32(&aempty_bar[a]), ((i / C::kASlots) & 1) ^ 1, abort_flag, p.err)) break;
+      tc_fence_after();
       tmem_st_32x32b_x32(tmem + lane_addr + C::kACol0 + a * 32, out);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&afull_bar[a]));
+      kb += C::kDqGroups;
+      while (kb >= p.KB) kb -= p.KB;
     }
-
+  } else {
     // ------------------------------------------------------------ epilogue
-    const bool acc_ok = warp_wait(smem_u32(&acc_bar), 0, abort_flag, p.err);
-    tc_fence_after();
-    const int n = t * kTN + r;
-    const int m_end = min(p.M, m0 + BN);
-    if (__all_sync(0xffffffffu, acc_ok && !*abort_flag)) {
+    const int lq = warp % 4;
+    const int r = lq * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
+    const int64_t u_end = u0 + nu;
+    int seg = 0;
+    for (int64_t u = u0; u < u_end; ++seg) {
+      const int tile = static_cast<int>(u / p.KB);
+      const int64_t tile_end = static_cast<int64_t>(tile + 1) * p.KB;
+      const int64_t seg_end = min(u_end, tile_end);
+      const bool whole = (u % p.KB == 0) && seg_end == tile_end;
+      const int db = seg % C::kDBufs;
+      if (!warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int t = tile / p.MT;
+      const int m0 = (tile % p.MT) * BN;
+      const int m_end = min(p.M, m0 + BN);
+      const int n = t * kTN + r;
+      float *piece = p.pieces + ((static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * kTN + r) * BN;
+      // issuers that took a block of this segment: all of them unless the segment is shorter
+      const int i_first = static_cast<int>(u - u0);
+      const int seg_len = static_cast<int>(seg_end - u);
+      uint32_t contrib = 0;
+      for (int j = 0; j < seg_len && j < C::kMmaWarps; ++j) contrib |= 1u << ((i_first + j) % C::kMmaWarps);
+      const int w_first = __ffs(contrib) - 1;
 #pragma unroll 1
-      for (int c0 = dq * 16; c0 < BN; c0 += 16 * C::kDqGroups) {
-        if (m0 + c0 >= m_end) break;
+      for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
         uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem + lane_addr + c0, v);
+        const uint32_t dbase = tmem + lane_addr + db * C::kMmaWarps * C::kDStride + c0;
+        tmem_ld_32x32b_x16(dbase + w_first * C::kDStride, v);
         tmem_wait_ld();
-        if (n < p.N) {
+#pragma unroll 1
+        for (int w = w_first + 1; w < C::kMmaWarps; ++w) {  // the issuers' partial sums, in a fixed order
+          if (!(contrib >> w & 1u)) continue;
+          uint32_t v2[16];
+          tmem_ld_32x32b_x16(dbase + w * C::kDStride, v2);
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int m = m0 + c0 + i;
-            if (m < m_end) {
-              const float acc = __uint_as_float(v[i]);
-              if (p.S == 1)
-                p.y[static_cast<int64_t>(m) * p.N + n] = __float2half_rn(acc);
-              else
-                p.partials[(static_cast<int64_t>(sk) * p.M + m) * p.Npad + n] = acc;
+          for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(v2[e]));
+        }
+        if (whole) {
+          if (n < p.N) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (m0 + c0 + e < m_end)
+                p.y[static_cast<int64_t>(m0 + c0 + e) * p.N + n] = __float2half_rn(__uint_as_float(v[e]));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) st_f32x4(piece + c0 + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&dempty_bar[db]));
+      if (!whole) {
+        // the last CTA to finish a piece of this tile adds all pieces in K order and writes y
+        const int c_first = owner_of(p, static_cast<int64_t>(tile) * p.KB);
+        const int c_last = owner_of(p, tile_end - 1);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (r == 0) {
+          const uint32_t old = atomicAdd(&p.counters[tile], 1u);
+          last_sh = (old == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
+        }
+        named_bar_sync(1, 128);
+        if (last_sh) {
+          __threadfence();
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll 1
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const int slot = (range_begin(p, cc) / p.KB == tile) ? 0 : 1;
+              const float4 *src = reinterpret_cast<const float4 *>(
+                  p.pieces + ((static_cast<int64_t>(cc) * 2 + slot) * kTN + r) * BN + c0);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 v4 = __ldcg(src + q4);
+                acc[4 * q4 + 0] += v4.x;
+                acc[4 * q4 + 1] += v4.y;
+                acc[4 * q4 + 2] += v4.z;
+                acc[4 * q4 + 3] += v4.w;
+              }
+            }
+            if (n < p.N) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                if (m0 + c0 + e < m_end) p.y[static_cast<int64_t>(m0 + c0 + e) * p.N + n] = __float2half_rn(acc[e]);
             }
           }
+          if (r == 0) p.counters[tile] = 0u;  // ready for the next call
         }
       }
-    }
-    if (p.S > 1) {
-      // last-arriving CTA of this output tile adds the partials in split order
-      __threadfence();
-      named_bar_sync(1, 128 * C::kDqGroups);
-      if (threadIdx.x == 64) {
-        const uint32_t old = atomicAdd(&p.counters[t * p.MT + mt], 1u);
-        last_sh = (old == static_cast<uint32_t>(p.S - 1)) ? 1u : 0u;
-      }
-      named_bar_sync(1, 128 * C::kDqGroups);
-      if (last_sh) {
-        __threadfence();
-        if (n < p.N && !*abort_flag) {
-          for (int m = m0 + dq; m < m_end; m += C::kDqGroups) {
-            float acc = 0.f;
-            for (int s = 0; s < p.S; ++s)
-              acc += __ldcg(&p.partials[(static_cast<int64_t>(s) * p.M + m) * p.Npad + n]);
-            p.y[static_cast<int64_t>(m) * p.N + n] = __float2half_rn(acc);
-          }
-        }
-        if (threadIdx.x == 64) p.counters[t * p.MT + mt] = 0u;  // ready for the next call
-      }
+      u = seg_end;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == C::kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -423,36 +559,36 @@ cudaError_t launch_bn(int bn, const CUtensorMap &map, const Params &p, int ctas,
 
 }  // namespace
 
-bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int splits, int num_sms,
-                    GemmPlan *plan) {
+bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int ctas, int schedule,
+                    int num_sms, GemmPlan *plan) {
   (void)g;
   int bn = block_n;
   if (bn == 0) bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   if (bn != 16 && bn != 32 && bn != 64 && bn != 128 && bn != 256) return false;
-  if (splits < 0 || splits > 64) return false;
+  if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
   const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK);
   const int64_t tiles = mt * nt;
-  int64_t S = splits;
-  if (S == 0) {
-    const int64_t per_sm = bn == 256 ? 1 : 2;
-    const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * per_sm;
-    S = tiles >= slots ? 1 : slots / tiles;
-    S = std::min<int64_t>(S, std::max<int64_t>(1, kb / 4));  // at least 4 K blocks per split
-    S = std::min<int64_t>(S, 32);
-  }
-  S = std::max<int64_t>(1, std::min<int64_t>(S, kb));
-  if (tiles * S > 0x7FFFFFFF) return false;
+  const int64_t units = tiles * kb;
+  if (tiles > 0x7FFFFFFF || units > (int64_t{1} << 40)) return false;
+  int64_t P = ctas > 0 ? ctas : (num_sms > 0 ? num_sms : 148);
+  // whole-tile scheduling when every CTA gets many tiles (imbalance <= 1/8) or the tiles divide
+  // evenly; otherwise stream-K over 64-wide K blocks, which needs the partial-tile fixup
+  bool whole = schedule == 2 || (schedule == 0 && (tiles >= 8 * P || (tiles >= P && tiles % P == 0)));
+  const int64_t gran = whole ? kb : 1;
+  const int64_t grains = units / gran;
+  P = std::min(P, grains);
   plan->block_n = bn;
-  plan->splits = static_cast<int>(S);
   plan->m_tiles = static_cast<int>(mt);
   plan->n_tiles = static_cast<int>(nt);
   plan->k_blocks = static_cast<int>(kb);
-  plan->ctas = static_cast<int>(tiles * S);
+  plan->ctas = static_cast<int>(P);
+  plan->gran = static_cast<int>(gran);
+  plan->grains = grains;
   plan->counters_offset = 256;
   const size_t counters_bytes = static_cast<size_t>(cdiv(tiles * 4, 256) * 256);
-  plan->partials_offset = plan->counters_offset + counters_bytes;
-  const size_t partial_bytes = S > 1 ? static_cast<size_t>(S * M * nt * kTN * 4) : 0;
-  plan->workspace_bytes = plan->partials_offset + partial_bytes;
+  plan->pieces_offset = plan->counters_offset + counters_bytes;
+  const size_t piece_bytes = whole ? 0 : static_cast<size_t>(P * 2 * kTN * bn * 4);
+  plan->workspace_bytes = plan->pieces_offset + piece_bytes;
   return true;
 }
 
@@ -469,7 +605,7 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.codes = static_cast<const uint8_t *>(packed);
   p.meta = p.codes + static_cast<int64_t>(plan.n_tiles) * plan.k_blocks * kTileBytes;
   p.y = static_cast<__half *>(y);
-  p.partials = reinterpret_cast<float *>(ws + plan.partials_offset);
+  p.pieces = reinterpret_cast<float *>(ws + plan.pieces_offset);
   p.counters = reinterpret_cast<uint32_t *>(ws + plan.counters_offset);
   p.err = reinterpret_cast<uint32_t *>(ws);
   p.M = static_cast<int>(M);
@@ -480,8 +616,9 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.NT = plan.n_tiles;
   p.KB = plan.k_blocks;
   p.MT = plan.m_tiles;
-  p.S = plan.splits;
-  p.Npad = plan.n_tiles * kTN;
+  p.P = plan.ctas;
+  p.gran = plan.gran;
+  p.grains = plan.grains;
   const bool general = (g % kTK) != 0;
   return general ? launch_bn<true>(plan.block_n, map, p, plan.ctas, stream)
                  : launch_bn<false>(plan.block_n, map, p, plan.ctas, stream);

@@ -23,18 +23,20 @@ cudaError_t launch_repack(const uint32_t *qw, const void *scales, const uint32_t
 
 struct GemmPlan {
   int block_n;   // activation rows per tile: 16, 32, 64, 128 or 256
-  int splits;    // K partitions
   int m_tiles;
   int n_tiles;
   int k_blocks;
-  int ctas;
+  int ctas;      // persistent CTAs (one per SM)
+  int gran;      // K blocks per scheduling grain: 1 (stream-K) or k_blocks (whole tiles)
+  int64_t grains;
   size_t counters_offset;
-  size_t partials_offset;
+  size_t pieces_offset;
   size_t workspace_bytes;
 };
 
-// Returns false if block_n / splits are not valid values.
-bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int splits, int num_sms,
+// schedule: 0 automatic, 1 stream-K, 2 whole tiles. ctas: 0 = one per SM.
+// Returns false if block_n / ctas / schedule are not valid values.
+bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int ctas, int schedule, int num_sms,
                     GemmPlan *plan);
 
 // Launches the GEMM for a validated plan. Returns the CUDA error (cudaSuccess on success);
