@@ -56,14 +56,15 @@ def test_repacked_bytes_formula(lib):
 
 def test_workspace_sizes(lib):
     # whole tiles: error word block + per-tile counters only
-    b = w4.w4a16_workspace_bytes_ex(512, 8192, 8192, 128, 256, 0, 2)
-    assert b == 256 + 512  # 2 x 64 tile counters of 4 bytes
+    b = w4.w4a16_workspace_bytes_ex(512, 8192, 8192, 128, 128, 0, 2)
+    assert b == 256 + 1024  # 4 x 64 tile counters of 4 bytes
     # stream-K with P CTAs: plus two fp32 partial tiles (128 x block_n) per CTA
     M, N, K, P = 16, 300, 1024, 4
     b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 16, P, 1)
     assert b == 256 + 256 + P * 2 * 128 * 16 * 4
     assert w4.w4a16_workspace_bytes(0, 1, 8, 8) == 0
-    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 0, 0) == 0  # block_n must be 16..256, a power of two
+    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 0, 0) == 0  # block_n must be 16..128, a power of two
+    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 256, 0, 0) == 0
     assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 16, 0, 3) == 0  # no schedule 3
 
 

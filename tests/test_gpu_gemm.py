@@ -79,7 +79,7 @@ def test_tile_edges(M):
     check(M, 300, 520, 128)
 
 
-@pytest.mark.parametrize("block_n", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("block_n", [16, 32, 64, 128])
 @pytest.mark.parametrize("ctas,schedule", [(1, 1), (2, 1), (3, 1), (7, 1), (13, 1), (64, 1), (1, 2), (5, 2)])
 def test_forced_schedules(block_n, ctas, schedule):
     # 3 n-tiles x 16 K blocks (x m-tiles): stream-K cuts tiles at many places, incl. one CTA holding
@@ -103,7 +103,7 @@ def test_one_hot_rows_return_rounded_weights_exactly():
         x[i, k] = 1.0
     wd = oracle.dequant(qw, s, zw, N, K, g)
     expect = wd[:, ks].T.astype(np.float16)  # (q - z) * s is exact in fp64; one rounding to fp16
-    for bn, ctas, sch in [(0, 0, 0), (16, 1, 2), (16, 4, 1), (256, 1, 1), (64, 5, 1), (16, 11, 1)]:
+    for bn, ctas, sch in [(0, 0, 0), (16, 1, 2), (16, 4, 1), (128, 1, 1), (64, 5, 1), (16, 11, 1), (32, 3, 1)]:
         y = run_gemm(x, packed, N, K, g, bn, ctas, sch)
         assert (y.view(np.uint16) == expect.view(np.uint16)).all(), (bn, ctas, sch)
 
@@ -193,11 +193,14 @@ def test_prefill_layers_sampled(L):
         check(M, L.n, L.k, L.g, rows=_sample_rows(M, 8), outliers=True)
 
 
-@pytest.mark.parametrize("block_n,ctas,schedule", [(256, 80, 2), (256, 0, 1), (128, 0, 1), (64, 0, 1), (16, 0, 1)])
-def test_repeated_launches_bit_identical(block_n, ctas, schedule):
+@pytest.mark.parametrize("N,K,M,block_n,ctas,schedule", [
+    (10240, 8192, 256, 128, 80, 2), (10240, 8192, 256, 128, 0, 1), (10240, 8192, 256, 64, 0, 1),
+    (10240, 8192, 256, 32, 0, 1), (10240, 8192, 256, 16, 0, 1),
+    # 172 tiles over 152 CTAs: many CTAs hold a short head or tail segment that some dequant groups skip
+    (22016, 4096, 64, 64, 0, 1), (22016, 4096, 128, 128, 0, 1), (22016, 4096, 16, 16, 0, 1)])
+def test_repeated_launches_bit_identical(N, K, M, block_n, ctas, schedule):
     # The schedule is deterministic, so back-to-back launches must agree bit for bit; a pipeline
-    # hazard (a stage or slot read before its data landed) shows up here as a differing launch.
-    N, K, M = 10240, 8192, 256
+    # hazard (a stage, slot or accumulator used before it was ready) shows up as a differing launch.
     qw, s, zw, packed, wn = layer(N, K, 128)
     x = torch.from_numpy(workloads.activations_f16(M, K, outliers=True)).cuda()
     ws = w4.Workspace()
@@ -207,7 +210,7 @@ def test_repeated_launches_bit_identical(block_n, ctas, schedule):
         y = w4.w4a16_gemm_ex(x, packed, N, K, 128, block_n, ctas, schedule, workspace=ws)
         ndiff += int(not torch.equal(y, first))
     assert ndiff == 0
-    rows = np.array([0, 17, 130, 255])
+    rows = np.unique(np.array([0, min(17, M - 1), M // 2, M - 1]))
     yref = oracle.gemm(x.cpu().numpy()[rows], qw, s, zw, N, K, 128)
     assert_within_tolerance(first.cpu().numpy()[rows], yref, gemm_tolerance(x.cpu().numpy()[rows], wn), "repeat")
     assert w4.w4_last_device_error(ws) == 0

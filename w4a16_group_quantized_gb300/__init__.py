@@ -198,7 +198,7 @@ def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: int, y:
 
 def w4a16_gemm_ex(x, packed, N, K, g, block_n: int = 0, ctas: int = 0, schedule: int = 0, y=None, workspace=None,
                   stream=None):
-    """w4a16_gemm with the schedule forced: block_n in {16,32,64,128,256}, ctas >= 1, schedule 1 stream-K or
+    """w4a16_gemm with the schedule forced: block_n in {16,32,64,128}, ctas >= 1, schedule 1 stream-K or
     2 whole tiles (0 = automatic for each)."""
     return _gemm_common(x, packed, N, K, g, y, workspace, block_n, ctas, schedule, stream)
 

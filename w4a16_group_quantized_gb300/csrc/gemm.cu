@@ -12,19 +12,19 @@
 //                   TMA tensor copy of the x tile (128-byte swizzle, zero fill
 //                   outside [M, K]) and two bulk copies (4 KB of codes, group
 //                   records), all completing on the stage's mbarrier.
-//   1-4 MMA warps   (lane 0) take whole K blocks in turn, each accumulating its
-//                   blocks into its own tensor-memory accumulator; the first
-//                   one also allocates tensor memory.
 //   2-4 dequant warpgroups take K blocks in turn: thread r owns weight row r;
 //                   it turns the row's 64 codes into fp16 (q - z) * s and stores
 //                   them into tensor memory (tcgen05.st), where they are the
-//                   MMA's A operand; shared memory only ever holds 4-bit codes.
+//                   MMA's A operand (shared memory only ever holds 4-bit codes);
+//                   then the group's first thread issues the block's MMAs into
+//                   the group's own accumulator. The first group also
+//                   allocates tensor memory.
 //   1 epilogue warpgroup: reads a finished tile's accumulators (double-buffered
-//                   for BN <= 64, so the next tile's MMAs overlap it), adds the
-//                   MMA warps' parts in a fixed order and writes y, or an fp32
+//                   for BN <= 32, so the next tile's MMAs overlap it), adds the
+//                   groups' parts in a fixed order and writes y, or an fp32
 //                   partial tile when the tile was cut between CTAs.
-// Several producer and MMA warps are needed because a single thread issues a
-// bulk copy only every ~350 cycles and a tcgen05 instruction every ~100.
+// The copies and MMAs are spread over several threads because one thread
+// issues a bulk copy only every ~350 cycles and a tcgen05 op every ~100.
 //
 // This is the GB300 form of the techniques the Marlin post lists (prefetch,
 // activation reuse, asynchronous weight loads, dequant interleaved with the
@@ -49,6 +49,7 @@ namespace w4 {
 namespace {
 
 constexpr int kMaxRecs = 9;  // group records one 64-wide K block can touch (g = 8: 8 groups)
+constexpr int kMaxPieces = 8;  // CTAs that may share one output tile (the planner guarantees it)
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
   int p = 32;
@@ -76,26 +77,22 @@ struct Cfg {
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = (kStagesRaw > 16 ? 16 : kStagesRaw) / 4 * 4;
   static constexpr int kASlots = 8;    // tensor-memory slots of dequantized weights (32 columns each)
-  // Each tcgen05 instruction (mma, commit, fence) costs the issuing thread ~100 cycles whatever its
-  // size, so narrow tiles give the K blocks in turn to several issuing warps, each accumulating into
-  // its own tensor-memory accumulator (summed in a fixed order by the epilogue).
-  // (25 warps leave 72 registers a thread: 7 warps share one sub-partition's 16K registers.)
-  static constexpr int kMmaWarps = BN <= 32 ? 4 : (BN <= 128 ? 2 : 1);
-  static constexpr int kDBufs = BN <= 64 ? 2 : 1;  // accumulator sets (epilogue overlaps the next tile)
+  // Each dequant warpgroup issues the MMAs of its own K blocks into its own tensor-memory
+  // accumulator (the epilogue adds the groups' accumulators in a fixed order): no separate issuing
+  // warp, no extra barrier hop between a block's dequant and its MMAs.
+  static constexpr int kDBufs = BN <= 32 ? 2 : 1;  // accumulator sets (epilogue overlaps the next tile)
   static constexpr int kDStride = BN < 32 ? 32 : BN;
-  static constexpr int kACol0 = kDBufs * kMmaWarps * kDStride;
+  static constexpr int kACol0 = kDBufs * kDqGroups * kDStride;
   static constexpr int kTmemCols = pow2_at_least(kACol0 + kASlots * 32);
-  static constexpr int kMmaWarp0 = kProducers;
-  static constexpr int kDqWarp0 = kMmaWarp0 + kMmaWarps;
+  static constexpr int kDqWarp0 = kProducers;
   static constexpr int kEpiWarp0 = kDqWarp0 + 4 * kDqGroups;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   static_assert(kStages >= 4 && kStages % kDqGroups == 0 && kStages % kProducers == 0,
                 "stage ring: a multiple of the producers and of the dequant groups");
   static_assert(kASlots % kDqGroups == 0, "tensor-memory slot ring: a multiple of the dequant groups");
-  static_assert(kStages % kMmaWarps == 0 && kASlots % kMmaWarps == 0, "each ring slot keeps one issuing warp");
   static_assert(kTmemCols <= 512, "tensor memory budget");
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
 };
 
 // Work decomposition. A unit is one 64-wide K block of one output tile (128 weight rows x BN
@@ -175,8 +172,8 @@ __device__ __forceinline__ void dequant_word(uint32_t w, const GroupConsts &c, u
 // A wait whose outcome is the same for all 32 lanes: the warp then either executes the
 // following .sync.aligned tcgen05 instructions together or leaves the loop together.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          uint32_t *err) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err);
+                                          uint32_t *err, uint32_t max_sleep_ns = 128) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, err, max_sleep_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -200,11 +197,10 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
-  __shared__ __align__(8) uint64_t afull_bar[C::kASlots];
   __shared__ __align__(8) uint64_t aempty_bar[C::kASlots];
   __shared__ __align__(8) uint64_t dfull_bar[C::kDBufs];
   __shared__ __align__(8) uint64_t dempty_bar[C::kDBufs];
-  __shared__ __align__(8) uint64_t drain_bar[C::kMmaWarps];
+  __shared__ __align__(8) uint64_t drain_bar[C::kDqGroups];
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t abort_sh;
   __shared__ uint32_t last_sh;
@@ -223,26 +219,24 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    for (int a = 0; a < C::kASlots; ++a) {
-      mbar_init(smem_u32(&afull_bar[a]), 128);
-      mbar_init(smem_u32(&aempty_bar[a]), 1);
-    }
+    for (int a = 0; a < C::kASlots; ++a) mbar_init(smem_u32(&aempty_bar[a]), 1);
     for (int d = 0; d < C::kDBufs; ++d) {
-      mbar_init(smem_u32(&dfull_bar[d]), C::kMmaWarps);
+      mbar_init(smem_u32(&dfull_bar[d]), C::kDqGroups);
       mbar_init(smem_u32(&dempty_bar[d]), 128);
     }
-    for (int w = 0; w < C::kMmaWarps; ++w) mbar_init(smem_u32(&drain_bar[w]), 1);
+    for (int w = 0; w < C::kDqGroups; ++w) mbar_init(smem_u32(&drain_bar[w]), 1);
     abort_sh = 0;
     last_sh = 0;
     fence_mbar_init();
   }
-  if (warp == C::kMmaWarp0) {
+  if (warp == C::kDqWarp0) {
     tmem_alloc(smem_u32(&tmem_base_sh), C::kTmemCols);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&x_map);
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cta_sync_all();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
@@ -289,98 +283,107 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
           drain_wait(smem_u32(&full_bar[j % C::kStages]), (j / C::kStages) & 1);
       }
     }
-  } else if (warp < C::kDqWarp0) {
-    // ---------------------------------------------------------- MMA issuers
-    // issuing warp w takes the K blocks i = w, w + kMmaWarps, ... into its own accumulator; every
-    // issuer follows the segments (tiles) to wait for a free accumulator set and to close it
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(128, BN);
-      const int w = warp - C::kMmaWarp0;
-      int kb = static_cast<int>(u0 % p.KB);
-      int seg = 0;
-      bool own_first = true;  // the next own block is this issuer's first in the segment
-      int i = 0;
-      for (; i < nu; ++i) {
-        const bool first = i == 0 || kb == 0;
-        const bool last = i == nu - 1 || kb == p.KB - 1;
-        const int db = seg % C::kDBufs;
-        if (first) {
-          if (!mbar_wait(smem_u32(&dempty_bar[db]), ((seg / C::kDBufs) & 1) ^ 1, abort_flag, p.err)) break;
-          own_first = true;
+  } else if (warp < C::kEpiWarp0) {
+    // ------------------------------------------------- dequant + MMA issue
+    // Group dq takes K blocks i = dq, dq + kDqGroups, ...: thread r dequantizes weight row r into
+    // a tensor-memory slot; after a group barrier the group's first thread issues the block's four
+    // MMAs into the group's own accumulator and commits the stage and the slot. That thread also
+    // keeps the group's part of the accumulator protocol: before the group's first block of a
+    // segment (tile) it waits for the segment's accumulator set to be free, and it commits dfull
+    // once for every segment of the CTA's range when the group is past it (a commit covers the
+    // committing thread's own MMAs, so the same thread issues and commits).
+    const int dq = (warp - C::kDqWarp0) / 4;
+    const bool issuer = warp == C::kDqWarp0 + 4 * dq && lane == 0;
+    const int lq = warp % 4;  // tensor-memory lane quarter this warp may access
+    const int r = lq * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
+    constexpr uint32_t idesc = idesc_f16_f32(128, BN);
+    const int64_t tile0 = u0 / p.KB;
+    const int seg_count = static_cast<int>((u0 + nu - 1) / p.KB - tile0) + 1;
+    int kb = static_cast<int>((u0 + dq) % p.KB);                  // K block of unit i
+    int seg_i = static_cast<int>((u0 + dq) / p.KB - tile0);        // segment of unit i
+    int prev_seg = -1;       // segment of this group's previous block
+    int seg_closed = 0;      // segments below this one have had this group's dfull commit
+    int seg_freed = 0;       // segments below this one are known to be read out by the epilogue
+    bool issue_ok = true;    // the issuer's own waits (shared with the group at the next barrier)
+    for (int i = dq; i < nu; i += C::kDqGroups) {
+      const int s = i % C::kStages;
+      const int a = i % C::kASlots;
+      const int db = seg_i % C::kDBufs;
+      bool okw = warp_wait(smem_u32(&full_bar[s]), (i / C::kStages) & 1, abort_flag, p.err);
+      uint32_t out[32];
+      if (okw) {
+        const uint32_t codes = smem_base + s * C::kStageBytes + C::kXBytes;
+        const uint32_t meta = codes + kTileBytes;
+        const uint4 w0 = lds128(codes + r * 16);
+        const uint4 w1 = lds128(codes + 2048 + r * 16);
+        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        if (!GENERAL) {
+          const uint32_t z = (lds8(meta + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
+          const GroupConsts c = group_consts(lds16(meta + 2 * r), z);
+#pragma unroll
+          for (int ci = 0; ci < 8; ++ci) dequant_word(words[ci], c, &out[4 * ci]);
+        } else {
+          const int kfirst = kb * kTK;
+          const int jlo = min(kfirst / p.g, p.G - 1);
+          int j = jlo;
+#pragma unroll
+          for (int ci = 0; ci < 8; ++ci) {
+            const int kc = kfirst + 8 * ci;
+            if (kc >= (j + 1) * p.g && j < p.G - 1) ++j;  // g >= 8: at most one group boundary per 8 codes
+            const uint32_t rec = meta + (j - jlo) * kRecBytes;
+            const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
+            dequant_word(words[ci], group_consts(lds16(rec + 2 * r), z), &out[4 * ci]);
+          }
         }
-        if (i % C::kMmaWarps == w) {
-          const int s = i % C::kStages;
-          const int a = i % C::kASlots;
-          // the dequant group arrives on afull only after it saw this stage's copies land (full), so
-          // the x tile the MMA reads is in shared memory too
-          if (!mbar_wait(smem_u32(&afull_bar[a]), (i / C::kASlots) & 1, abort_flag, p.err)) break;
+        // the slot's previous block (i - kASlots) is this group's too: its MMAs must be done
+        okw = warp_wait(smem_u32(&aempty_bar[a]), ((i / C::kASlots) & 1) ^ 1, abort_flag, p.err);
+      }
+      if (okw) {
+        tc_fence_after();
+        tmem_st_32x32b_x32(tmem + lane_addr + C::kACol0 + a * 32, out);
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      // one decision for the whole group: go on together or stop together
+      if (!named_bar_and(2 + dq, 128, okw && issue_ok)) break;
+      if (issuer) {
+        for (; seg_closed < seg_i; ++seg_closed) mma_commit(smem_u32(&dfull_bar[seg_closed % C::kDBufs]));
+        const bool first = prev_seg != seg_i;
+        // before the first block of segment seg_i, the accumulator set it reuses must be read out,
+        // i.e. segment seg_i - kDBufs finished. The group may have had no block in some segments:
+        // wait for every segment's phase in order, so no parity wait can skip a phase.
+        for (; first && issue_ok && seg_freed <= seg_i - C::kDBufs; ++seg_freed)
+          issue_ok = mbar_wait(smem_u32(&dempty_bar[seg_freed % C::kDBufs]), (seg_freed / C::kDBufs) & 1,
+                               abort_flag, p.err);
+        if (issue_ok) {
           tc_fence_after();
           const uint64_t bdesc = sw128_kmajor_desc(smem_base + s * C::kStageBytes);
-          const uint32_t dcol = tmem + (db * C::kMmaWarps + w) * C::kDStride;
+          const uint32_t dcol = tmem + (db * C::kDqGroups + dq) * C::kDStride;
 #pragma unroll
           for (int kk = 0; kk < kTK / 16; ++kk) {
             // A: 128 x 16 fp16 in tensor memory (8 columns per 16 K); B: 16 K-columns of the x tile
             mma_f16_ts(dcol, tmem + C::kACol0 + a * 32 + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                       (own_first && kk == 0) ? 0u : 1u);
+                       (first && kk == 0) ? 0u : 1u);
           }
-          own_first = false;
           mma_commit(smem_u32(&empty_bar[s]));
           mma_commit(smem_u32(&aempty_bar[a]));
         }
-        if (last) {
-          mma_commit(smem_u32(&dfull_bar[db]));
-          ++seg;
-        }
-        if (++kb == p.KB) kb = 0;
       }
-      if (*abort_flag) {
-        mma_commit(smem_u32(&drain_bar[w]));
-        drain_wait(smem_u32(&drain_bar[w]), 0);
+      prev_seg = seg_i;
+      kb += C::kDqGroups;
+      while (kb >= p.KB) {
+        kb -= p.KB;
+        ++seg_i;
       }
     }
-  } else if (warp < C::kEpiWarp0) {
-    // ------------------------------------------------------------- dequant
-    const int dq = (warp - C::kDqWarp0) / 4;
-    const int lq = warp % 4;  // tensor-memory lane quarter this warp may access
-    const int r = lq * 32 + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
-    int kb = static_cast<int>((u0 + dq) % p.KB);  // K block of unit i, advanced without divisions
-    for (int i = dq; i < nu; i += C::kDqGroups) {
-      const int s = i % C::kStages;
-      const int a = i % C::kASlots;
-      if (!warp_wait(smem_u32(&full_bar[s]), (i / C::kStages) & 1, abort_flag, p.err)) break;
-      const uint32_t codes = smem_base + s * C::kStageBytes + C::kXBytes;
-      const uint32_t meta = codes + kTileBytes;
-      const uint4 w0 = lds128(codes + r * 16);
-      const uint4 w1 = lds128(codes + 2048 + r * 16);
-      const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      uint32_t out[32];
-      if (!GENERAL) {
-        const uint32_t z = (lds8(meta + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
-        const GroupConsts c = group_consts(lds16(meta + 2 * r), z);
-#pragma unroll
-        for (int ci = 0; ci < 8; ++ci) dequant_word(words[ci], c, &out[4 * ci]);
-      } else {
-        const int kfirst = kb * kTK;
-        const int jlo = min(kfirst / p.g, p.G - 1);
-        int j = jlo;
-#pragma unroll
-        for (int ci = 0; ci < 8; ++ci) {
-          const int kc = kfirst + 8 * ci;
-          if (kc >= (j + 1) * p.g && j < p.G - 1) ++j;  // g >= 8: at most one group boundary per 8 codes
-          const uint32_t rec = meta + (j - jlo) * kRecBytes;
-          const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
-          dequant_word(words[ci], group_consts(lds16(rec + 2 * r), z), &out[4 * ci]);
-        }
+    if (issuer) {
+      // segments after the group's last block (or all of them if it had none) still need its commit
+      for (; seg_closed < seg_count; ++seg_closed) mma_commit(smem_u32(&dfull_bar[seg_closed % C::kDBufs]));
+      if (*abort_flag) {
+        mma_commit(smem_u32(&drain_bar[dq]));
+        drain_wait(smem_u32(&drain_bar[dq]), 0);
       }
-      if (!warp_wait(smem_u32(&aempty_bar[a]), ((i / C::kASlots) & 1) ^ 1, abort_flag, p.err)) break;
-      tc_fence_after();
-      tmem_st_32x32b_x32(tmem + lane_addr + C::kACol0 + a * 32, out);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&afull_bar[a]));
-      kb += C::kDqGroups;
-      while (kb >= p.KB) kb -= p.KB;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -395,27 +398,28 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
       const int64_t seg_end = min(u_end, tile_end);
       const bool whole = (u % p.KB == 0) && seg_end == tile_end;
       const int db = seg % C::kDBufs;
-      if (!warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err)) break;
+      // the epilogue waits a whole tile for its accumulator: sleep longer between looks
+      if (!warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err, 1024)) break;
       tc_fence_after();
       const int t = tile / p.MT;
       const int m0 = (tile % p.MT) * BN;
       const int m_end = min(p.M, m0 + BN);
       const int n = t * kTN + r;
       float *piece = p.pieces + ((static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * kTN + r) * BN;
-      // issuers that took a block of this segment: all of them unless the segment is shorter
+      // dequant groups that took a block of this segment: all of them unless the segment is shorter
       const int i_first = static_cast<int>(u - u0);
       const int seg_len = static_cast<int>(seg_end - u);
       uint32_t contrib = 0;
-      for (int j = 0; j < seg_len && j < C::kMmaWarps; ++j) contrib |= 1u << ((i_first + j) % C::kMmaWarps);
+      for (int j = 0; j < seg_len && j < C::kDqGroups; ++j) contrib |= 1u << ((i_first + j) % C::kDqGroups);
       const int w_first = __ffs(contrib) - 1;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
         uint32_t v[16];
-        const uint32_t dbase = tmem + lane_addr + db * C::kMmaWarps * C::kDStride + c0;
+        const uint32_t dbase = tmem + lane_addr + db * C::kDqGroups * C::kDStride + c0;
         tmem_ld_32x32b_x16(dbase + w_first * C::kDStride, v);
         tmem_wait_ld();
 #pragma unroll 1
-        for (int w = w_first + 1; w < C::kMmaWarps; ++w) {  // the issuers' partial sums, in a fixed order
+        for (int w = w_first + 1; w < C::kDqGroups; ++w) {  // the groups' partial sums, in a fixed order
           if (!(contrib >> w & 1u)) continue;
           uint32_t v2[16];
           tmem_ld_32x32b_x16(dbase + w * C::kDStride, v2);
@@ -442,37 +446,39 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
         const int c_first = owner_of(p, static_cast<int64_t>(tile) * p.KB);
         const int c_last = owner_of(p, tile_end - 1);
         __threadfence();
+        __syncwarp();
         named_bar_sync(1, 128);
         if (r == 0) {
           const uint32_t old = atomicAdd(&p.counters[tile], 1u);
           last_sh = (old == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
         }
+        __syncwarp();
         named_bar_sync(1, 128);
         if (last_sh) {
           __threadfence();
+          // all pieces' loads of a 2-column slice are in flight together, then added in K order
+          const int npieces = c_last - c_first + 1;
+          uint32_t slot_mask = 0;  // bit q: piece q is CTA (c_first + q)'s second slot
+          for (int q = 0; q < npieces; ++q)
+            if (range_begin(p, c_first + q) / p.KB != tile) slot_mask |= 1u << q;
+          const float *base = p.pieces + (static_cast<int64_t>(c_first) * 2 * kTN + r) * BN;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
-            float acc[16];
+          for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 2) {
+            float2 v[kMaxPieces];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-#pragma unroll 1
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int slot = (range_begin(p, cc) / p.KB == tile) ? 0 : 1;
-              const float4 *src = reinterpret_cast<const float4 *>(
-                  p.pieces + ((static_cast<int64_t>(cc) * 2 + slot) * kTN + r) * BN + c0);
+            for (int q = 0; q < kMaxPieces; ++q)
+              if (q < npieces)
+                v[q] = __ldcg(reinterpret_cast<const float2 *>(base + (2 * q + (slot_mask >> q & 1u)) * kTN * BN + c0));
+            float2 acc = v[0];
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const float4 v4 = __ldcg(src + q4);
-                acc[4 * q4 + 0] += v4.x;
-                acc[4 * q4 + 1] += v4.y;
-                acc[4 * q4 + 2] += v4.z;
-                acc[4 * q4 + 3] += v4.w;
+            for (int q = 1; q < kMaxPieces; ++q)
+              if (q < npieces) {
+                acc.x += v[q].x;
+                acc.y += v[q].y;
               }
-            }
             if (n < p.N) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                if (m0 + c0 + e < m_end) p.y[static_cast<int64_t>(m0 + c0 + e) * p.N + n] = __float2half_rn(acc[e]);
+              if (m0 + c0 < m_end) p.y[static_cast<int64_t>(m0 + c0) * p.N + n] = __float2half_rn(acc.x);
+              if (m0 + c0 + 1 < m_end) p.y[static_cast<int64_t>(m0 + c0 + 1) * p.N + n] = __float2half_rn(acc.y);
             }
           }
           if (r == 0) p.counters[tile] = 0u;  // ready for the next call
@@ -482,9 +488,12 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
     }
   }
 
+  // every role ends here; lanes of a warp arrive at different times (lane 0 ran the producer or
+  // MMA loop), so reconverge each warp and use the non-aligned barrier before freeing tensor memory
   tc_fence_before();
-  __syncthreads();
-  if (warp == C::kMmaWarp0) {
+  __syncwarp();
+  cta_sync_all();
+  if (warp == C::kDqWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -552,7 +561,6 @@ cudaError_t launch_bn(int bn, const CUtensorMap &map, const Params &p, int ctas,
     case 32: return launch_t<32, GENERAL>(map, p, ctas, stream);
     case 64: return launch_t<64, GENERAL>(map, p, ctas, stream);
     case 128: return launch_t<128, GENERAL>(map, p, ctas, stream);
-    case 256: return launch_t<256, GENERAL>(map, p, ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -563,8 +571,8 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
                     int num_sms, GemmPlan *plan) {
   (void)g;
   int bn = block_n;
-  if (bn == 0) bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-  if (bn != 16 && bn != 32 && bn != 64 && bn != 128 && bn != 256) return false;
+  if (bn == 0) bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  if (bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
   const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK);
   const int64_t tiles = mt * nt;
@@ -577,6 +585,20 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
   const int64_t gran = whole ? kb : 1;
   const int64_t grains = units / gran;
   P = std::min(P, grains);
+  if (!whole) {
+    // the fixup adds at most kMaxPieces pieces per tile: shrink the grid until no tile is cut into more
+    // (CTA c owns units [c*U/P, (c+1)*U/P); the owner of unit u is ((u + 1) * P - 1) / U)
+    auto max_pieces = [&](int64_t PP) {
+      int64_t worst = 1;
+      for (int64_t tt = 0; tt < tiles; ++tt) {
+        const int64_t first = ((tt * kb + 1) * PP - 1) / units;
+        const int64_t last = (((tt + 1) * kb) * PP - 1) / units;
+        worst = std::max(worst, last - first + 1);
+      }
+      return worst;
+    };
+    while (P > 1 && max_pieces(P) > kMaxPieces) --P;
+  }
   plan->block_n = bn;
   plan->m_tiles = static_cast<int>(mt);
   plan->n_tiles = static_cast<int>(nt);

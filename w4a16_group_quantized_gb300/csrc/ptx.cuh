@@ -73,13 +73,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // Waits for the phase of `bar` with the given parity to complete. Returns
 // false (and raises the CTA's abort flag and the device error word) when the
 // wait runs past kWaitLimitNs, or once another thread of the CTA aborted.
-// The clock and the abort flag are looked at every 16th attempt only.
+// A waiter that does not succeed at once backs off with __nanosleep (doubling
+// up to `max_sleep_ns`): a polling warp would take issue slots from the few
+// threads that issue the copies and MMAs. The clock and the abort flag are
+// looked at every 16th attempt only.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          uint32_t *err_word) {
+                                          uint32_t *err_word, uint32_t max_sleep_ns = 128) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
+  uint32_t sleep_ns = 16;
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    sleep_ns = sleep_ns * 2 > max_sleep_ns ? max_sleep_ns : sleep_ns * 2;
     if ((n & 15) == 0) {
       if (*abort_flag) return false;
       const uint64_t now = globaltimer_ns();
@@ -251,9 +257,29 @@ __device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c)
   return d;
 }
 
-// Named barrier among `nthreads` threads (whole warps), id 1..15.
+// Named barrier among `nthreads` threads (whole warps), id 1..15. The non-aligned form: a warp's
+// threads may arrive at different times (the aligned bar.sync is undefined for divergent warps).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// CTA-wide barrier in the non-aligned form, for the end of warp-specialized code where only some
+// lanes of a warp had work.
+__device__ __forceinline__ void cta_sync_all() { asm volatile("barrier.cta.sync 0;" ::: "memory"); }
+
+// Named barrier that also returns the AND of `pred` over all participating threads, so a group
+// of warps takes one decision together (nobody is left waiting at the next barrier).
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
 }
 
 }  // namespace w4
