@@ -169,6 +169,43 @@ W4_API int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g,
  */
 W4_API int w4_last_device_error(void *workspace_dev, void *stream);
 
+/*
+ * w4a16_gemm_noalloc -- w4a16_gemm for callers that cannot allocate device
+ * memory. The pages have no counterpart to this call; it exists for users of
+ * this library.
+ *
+ * Some callers have no way to hand the GEMM a workspace: code that runs while
+ * a stream is being captured into a CUDA graph (cudaMalloc is refused there
+ * and cudaFree would synchronise the device), engines that plan every device
+ * buffer up front and give kernels no scratch, and plug-ins that only see
+ * their input and output tensors. This call takes the same inputs and output
+ * as w4a16_gemm (same checks, same automatic schedule, same results) but keeps
+ * its scratch -- the error word, the per-tile counters and the fp32 partial
+ * tiles of tiles split between CTAs -- in a device array inside the library,
+ * W4A16_NOALLOC_SCRATCH_BYTES long. It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ *  - Every GPU on which the library is loaded holds that array until the
+ *    process exits.
+ *  - A problem whose workspace would not fit
+ *    (w4a16_workspace_bytes(M, N, K, g) > W4A16_NOALLOC_SCRATCH_BYTES; on
+ *    GB300 that is M > 32, unless the layer has at least 8 output tiles of
+ *    128 rows x 128 tokens per SM) is refused with W4_ERR_WORKSPACE_TOO_SMALL
+ *    before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture begins.
+ *  - All calls share the one array: calls that may overlap on the GPU (other
+ *    streams, other host threads) race and give wrong results; calls on one
+ *    stream are fine. Each call first clears the error word and the counters
+ *    on `stream`, so the previous call's leftovers do not matter.
+ *  - Device-side timeouts are not reported: there is no workspace to hand to
+ *    w4_last_device_error.
+ */
+#define W4A16_NOALLOC_SCRATCH_BYTES (8u << 20)
+W4_API int w4a16_gemm_noalloc(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K,
+                       int32_t g, void *y_dev, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -155,3 +155,64 @@ int w4_last_device_error(void *workspace_dev, void *stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// w4a16_gemm_noalloc: w4a16_gemm with its scratch in a fixed, library-owned
+// device array instead of a caller workspace (see include/w4a16.h).
+// ---------------------------------------------------------------------------
+namespace {
+
+// The scratch every call shares: error word, per-tile counters and the fp32
+// partial tiles of the stream-K fixup. Each GPU that loads the library keeps
+// these bytes until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[W4A16_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch for the current device. In host code the
+// array's name is only a host-side stand-in; the real address comes from
+// cudaGetSymbolAddress with that device current, looked up once per device.
+void *noalloc_scratch_address(int *status) {
+  static void *addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *status = W4_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      *status = W4_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *status = W4_OK;
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4a16_gemm_noalloc(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g,
+                       void *y_dev, void *stream) {
+  static_assert(W4A16_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
+  // the usual argument checks, with an aligned non-null stand-in for the workspace argument
+  int rc = check_gemm_args(x_dev, packed_dev, M, N, K, g, y_dev, reinterpret_cast<void *>(uintptr_t{256}));
+  if (rc != W4_OK) return rc;
+  w4::GemmPlan plan;
+  if (!w4::make_gemm_plan(M, N, K, g, 0, 0, 0, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
+  if (plan.workspace_bytes > W4A16_NOALLOC_SCRATCH_BYTES) return W4_ERR_WORKSPACE_TOO_SMALL;
+  void *scratch = noalloc_scratch_address(&rc);
+  if (rc != W4_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the error word and the tile counters must start at zero
+  if (cudaMemsetAsync(scratch, 0, plan.pieces_offset, st) != cudaSuccess) return W4_ERR_CUDA;
+  bool encode_failed = false;
+  const cudaError_t e = w4::launch_gemm(x_dev, packed_dev, M, N, K, g, y_dev, scratch, plan, st, &encode_failed);
+  if (encode_failed) return W4_ERR_CUDA;
+  return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+}  // extern "C"
