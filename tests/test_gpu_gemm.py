@@ -82,16 +82,32 @@ def test_tile_edges(M):
 @pytest.mark.parametrize("block_n", [16, 32, 64, 128])
 @pytest.mark.parametrize("ctas,schedule", [(1, 1), (2, 1), (3, 1), (7, 1), (13, 1), (64, 1), (1, 2), (5, 2)])
 def test_forced_schedules(block_n, ctas, schedule):
-    # 3 n-tiles x 16 K blocks (x m-tiles): stream-K cuts tiles at many places, incl. one CTA holding
+    # 3 n-tiles x 8 K stages (x m-tiles): stream-K cuts tiles at many places, incl. one CTA holding
     # the tail of one tile and the head of the next, and CTAs whose whole range sits inside one tile
-    check(20, 260, 1024, 128, block_n=block_n, ctas=ctas, schedule=schedule)
+    check(20, 260, 2048, 128, block_n=block_n, ctas=ctas, schedule=schedule)
 
 
-@pytest.mark.parametrize("g", [8, 16, 24, 32, 40, 96, 192, 256, 1024])
+@pytest.mark.parametrize("g", [8, 16, 24, 32, 40, 64, 96, 128, 192, 256, 384, 512, 1024])
 def test_group_sizes(g):
-    # 64 % g != 0 or g % 64 != 0 takes the per-chunk group path; K = 1000 leaves a partial last group
+    # g % 128 == 0 applies the scale outside the MMA (block_n <= 32); g % 64 == 0 inside with one
+    # group per 64-wide block (block_n >= 64); any other g looks the group up per 8 codes.
+    # K = 1000 leaves a partial last group and a last stage of 4 blocks whose last block is ragged.
     check(9, 200, 1000, g)
     check(9, 200, 1000, g, block_n=16, ctas=3, schedule=1)
+    check(30, 200, 1000, g, block_n=32, ctas=5, schedule=1)
+    check(70, 200, 1000, g, block_n=64, ctas=4, schedule=1)
+    check(100, 200, 1000, g, block_n=128, ctas=3, schedule=1)
+
+
+@pytest.mark.parametrize("K,g", [(288, 256), (320, 64), (320, 128), (448, 128), (576, 192), (4000, 128), (200, 8)])
+@pytest.mark.parametrize("block_n", [16, 32, 64, 128])
+def test_short_last_stage(K, g, block_n):
+    # A stage is four 64-wide K blocks; these K leave a last stage of 1..3 blocks (K % 64 != 0 also
+    # switches x to one tensor copy per block). Forced small grids start CTA ranges on that stage.
+    M = {16: 13, 32: 29, 64: 50, 128: 90}[block_n]
+    check(M, 264, K, g, block_n=block_n)
+    for ctas in (2, 3, 5):
+        check(M, 264, K, g, block_n=block_n, ctas=ctas, schedule=1)
 
 
 def test_one_hot_rows_return_rounded_weights_exactly():

@@ -125,7 +125,7 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int32_t *block_n
   if (!w4::make_gemm_plan(M, N, K, g, 0, 0, 0, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
   *block_n = plan.block_n;
   *ctas = plan.ctas;
-  *schedule = plan.gran == 1 ? 1 : 2;
+  *schedule = plan.whole ? 2 : 1;
   return W4_OK;
 }
 

@@ -3,35 +3,36 @@
 // Output tiles are 128 (weight rows n) x BN (activation rows m) tiles of y^T
 // ("swap-AB": the weights sit on the MMA's M = 128 side, the tokens on its N
 // side, so a batch of 1..16 tokens still fills an MMA). The kernel is
-// persistent: one CTA per SM walks a contiguous range of (tile, 64-wide K
-// block) units, so the work is split evenly whatever the number of tiles
+// persistent: one CTA per SM walks a contiguous range of (tile, 256-wide K
+// stage) units, so the work is split evenly whatever the number of tiles
 // (stream-K); a tile cut between CTAs is finished by a fixup (below).
 //
-// Warp roles (one CTA per SM):
-//   4 producer warps (lane 0) take the 64-wide K blocks in turn: per block one
-//                   TMA tensor copy of the x tile (128-byte swizzle, zero fill
-//                   outside [M, K]) and two bulk copies (4 KB of codes, group
-//                   records), all completing on the stage's mbarrier.
-//   2-4 dequant warpgroups take K blocks in turn: thread r owns weight row r;
-//                   it turns the row's 64 codes into fp16 (q - z) * s and stores
-//                   them into tensor memory (tcgen05.st), where they are the
-//                   MMA's A operand (shared memory only ever holds 4-bit codes);
-//                   then the group's first thread issues the block's MMAs into
-//                   the group's own accumulator. The first group also
-//                   allocates tensor memory.
-//   1 epilogue warpgroup: reads a finished tile's accumulators (double-buffered
-//                   for BN <= 32, so the next tile's MMAs overlap it), adds the
-//                   groups' parts in a fixed order and writes y, or an fp32
-//                   partial tile when the tile was cut between CTAs.
-// The copies and MMAs are spread over several threads because one thread
-// issues a bulk copy only every ~350 cycles and a tcgen05 op every ~100.
+// A stage is four 64-wide K blocks of one tile: 16 KB of 4-bit codes, the
+// group records they need and the four x sub-tiles, moved by three copies
+// (one thread can issue a bulk copy only every ~350 cycles, so copies are
+// made large). Warp roles (one CTA per SM):
+//   2 producer warps (lane 0) take the stages in turn: a TMA tensor copy of
+//                   x (128-byte swizzle, zero fill outside [M, K]) and two
+//                   bulk copies (codes, group records) on the stage's mbarrier.
+//   4 dequant warpgroups: group d turns K block d of every stage into fp16
+//                   w = (q - z) * s in tensor memory (thread r owns weight row
+//                   r; tcgen05.st), the MMA's A operand; shared memory only
+//                   holds 4-bit codes. A group never waits for the MMAs of its
+//                   own block, only for its two tensor-memory slots to come free.
+//   4 MMA warps (2 for BN = 128; lane 0): warp e issues the MMAs of its K
+//                   block(s) of every stage into its own accumulator and commits
+//                   once per stage (a thread issues a tcgen05.mma only every
+//                   ~50-130 cycles, so the issue is spread over several warps).
+//   1 epilogue warpgroup: adds the MMA warps' accumulators of a finished tile
+//                   segment in a fixed order and writes y, or an fp32 partial
+//                   tile when the tile was cut between CTAs.
+// When g is not a multiple of 64 the dequant looks the group up per 8 codes.
 //
 // This is the GB300 form of the techniques the Marlin post lists (prefetch,
 // activation reuse, asynchronous weight loads, dequant interleaved with the
 // tensor-core work, tuned warp roles): the weight stream is a multi-stage
 // TMA/mbarrier ring, each x tile is reused by all 128 weight rows, and the
-// dequant warps run ahead of the asynchronous MMAs through a ring of tensor-
-// memory slots.
+// dequant warps run ahead of the asynchronous MMAs through tensor-memory slots.
 //
 // Fixup of a cut tile: each CTA holding a piece writes it (fp32) to the
 // workspace and counts itself in on the tile's counter; the last to arrive
@@ -48,67 +49,82 @@
 namespace w4 {
 namespace {
 
-constexpr int kMaxRecs = 9;  // group records one 64-wide K block can touch (g = 8: 8 groups)
-constexpr int kMaxPieces = 8;  // CTAs that may share one output tile (the planner guarantees it)
+enum Mode { kScaleIn = 1, kGeneral = 2 };  // g % 64 == 0 (one group per K block) or any g
 
-__host__ __device__ constexpr int pow2_at_least(int v) {
-  int p = 32;
-  while (p < v) p *= 2;
-  return p;
-}
+constexpr int kSB = 4;           // 64-wide K blocks per stage
+constexpr int kStageK = kSB * kTK;
+constexpr int kMaxPieces = 8;    // CTAs that may share one output tile (the planner guarantees it)
 
-template <int BN, bool GENERAL>
+template <int BN, int MODE>
 struct Cfg {
-  static constexpr int kXBytes = BN * 128;  // BN rows x 64 fp16
-  static constexpr int kMetaBytes = GENERAL ? kMaxRecs * kRecBytes : kRecBytes;
-  static constexpr int kStageBytes = (kXBytes + kTileBytes + kMetaBytes + 1023) / 1024 * 1024;
-  static constexpr int kSmemBudget = 200 * 1024;  // one CTA per SM
-  // One thread can issue a bulk copy only every ~350 cycles, whatever its size, so four producer
-  // warps take the K blocks in turn (three copies each).
-  static constexpr int kProducers = 4;
-  // Dequant warpgroups: narrow (HBM-bound) tiles need four to hide each one's latency; wide
-  // (tensor-bound) tiles need a K block only every 256-512 cycles and keep the registers instead.
-  static constexpr int kDqGroups = BN <= 64 ? 4 : 2;
-  // A producer / dequant warpgroup waits only on the stages (and tensor-memory slots) of its own K
-  // blocks. An mbarrier parity wait is only sound for a waiter that sees every phase of that
-  // barrier: if a ring's size were not a multiple of the number of such waiters, successive uses of
-  // one stage would go to different waiters, and one that ran ahead could take the previous, still
-  // landing phase for its own (bulk copies complete out of order). So the rings are multiples of 4.
-  static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
-  static constexpr int kStages = (kStagesRaw > 16 ? 16 : kStagesRaw) / 4 * 4;
-  static constexpr int kASlots = 8;    // tensor-memory slots of dequantized weights (32 columns each)
-  // Each dequant warpgroup issues the MMAs of its own K blocks into its own tensor-memory
-  // accumulator (the epilogue adds the groups' accumulators in a fixed order): no separate issuing
-  // warp, no extra barrier hop between a block's dequant and its MMAs.
-  static constexpr int kDBufs = BN <= 32 ? 2 : 1;  // accumulator sets (epilogue overlaps the next tile)
+  static constexpr int kXSub = BN * 128;  // x for one K block: BN rows x 64 fp16 (1024-byte multiple)
+  static constexpr int kXBytes = kSB * kXSub;
+  static constexpr int kCodeBytes = kSB * kTileBytes;
+  // group records one stage can touch: g >= 64 -> at most 256 / 64 + 1; g >= 8 -> 256 / 8 + 1
+  static constexpr int kMaxRecs = MODE == kGeneral ? kStageK / 8 + 1 : kStageK / 64 + 1;
+  static constexpr int kStageBytes = (kXBytes + kCodeBytes + kMaxRecs * kRecBytes + 1023) / 1024 * 1024;
+  static constexpr int kSmemBudget = 224 * 1024;  // one CTA per SM
+  static constexpr int kStagesRaw = kSmemBudget / kStageBytes > 8 ? 8 : kSmemBudget / kStageBytes;
+  // producer warp w fills the stages i = w (mod 2): an even ring keeps each slot with one producer
+  static constexpr int kStages = kStagesRaw / 2 * 2;
+  // MMA warps: one per K block of a stage (a thread issues a tcgen05.mma only every ~50-130 cycles),
+  // two for BN = 128, whose accumulators would not fit four times into tensor memory
+  static constexpr int kIssuers = BN == 128 ? 2 : 4;
+  static constexpr int kBPI = kSB / kIssuers;  // K blocks per MMA warp and stage
+  static constexpr int kASlots = 2;     // tensor-memory A slots per dequant group (32 columns each)
   static constexpr int kDStride = BN < 32 ? 32 : BN;
-  static constexpr int kACol0 = kDBufs * kDqGroups * kDStride;
-  static constexpr int kTmemCols = pow2_at_least(kACol0 + kASlots * 32);
-  static constexpr int kDqWarp0 = kProducers;
-  static constexpr int kEpiWarp0 = kDqWarp0 + 4 * kDqGroups;
+  static constexpr int kDBufs = BN <= 32 ? 2 : 1;  // accumulator sets (the epilogue overlaps the next tile)
+  static constexpr int kACol0 = 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kIssuerWarp0 = 2;
+  static constexpr int kDqWarp0 = kIssuerWarp0 + kIssuers;
+  static constexpr int kEpiWarp0 = kDqWarp0 + 4 * kSB;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
-  static_assert(kStages >= 4 && kStages % kDqGroups == 0 && kStages % kProducers == 0,
-                "stage ring: a multiple of the producers and of the dequant groups");
-  static_assert(kASlots % kDqGroups == 0, "tensor-memory slot ring: a multiple of the dequant groups");
-  static_assert(kTmemCols <= 512, "tensor memory budget");
+  static_assert(kStages >= 2, "stage ring");
+  static_assert(kIssuers * kDBufs * kDStride <= kACol0, "accumulators below the A slots");
+  static_assert(kACol0 + kSB * kASlots * 32 <= kTmemCols, "tensor memory budget");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
 };
 
-// Work decomposition. A unit is one 64-wide K block of one output tile (128 weight rows x BN
-// activation rows); units are numbered tile-major: u = tile * KB + kb, tile = t * MT + mt.
+// Division by the group size g without a divide instruction: Granlund and Montgomery, "Division by
+// invariant integers using multiplication" (PLDI 1994), the round-up method with a 33-bit multiplier
+// split as 2^32 + m: q = (t + ((n - t) >> s1)) >> s2 with t = umulhi(m, n), exact for all n < 2^32.
+struct FastDiv {
+  uint32_t m, s1, s2;
+  __device__ __forceinline__ int div(int n) const {
+    const uint32_t un = static_cast<uint32_t>(n);
+    const uint32_t t = __umulhi(m, un);
+    return static_cast<int>((t + ((un - t) >> s1)) >> s2);
+  }
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t{1} << l) < d) ++l;  // l = ceil(log2 d)
+  FastDiv f;
+  f.m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l < 1 ? 0 : l - 1;
+  return f;
+}
+
+// Work decomposition. A unit is one 256-wide K stage of one output tile (128 weight rows x BN
+// activation rows); units are numbered tile-major: u = tile * KS + ks, tile = t * MT + mt.
 // CTA c owns the contiguous units [begin(c), begin(c+1)), cut at multiples of `gran` units
-// (gran = 1: stream-K, any cut; gran = KB: whole tiles only).
+// (gran = 1: stream-K, any cut; gran = KS: whole tiles only).
 struct Params {
   const uint8_t *codes;  // tile region of the packed weights
   const uint8_t *meta;   // group-record region of the packed weights
   __half *y;
-  float *pieces;         // [P][2][128][BN] fp32 partial tiles (first and last segment of each CTA)
+  float *pieces;         // [P][2][BN][128] fp32 partial tiles (first and last segment of each CTA)
   uint32_t *counters;    // [tiles] arrivals per split tile
   uint32_t *err;
-  int M, N, K, g, G, NT, KB, MT;
+  int M, N, K, g, G, NT, KB, KS, MT;
   int P;                 // CTAs
   int gran;              // units per scheduling grain
+  int x3d;               // x tensor map is [KB][M][64] (one copy per stage); else [M][K] (one per block)
+  FastDiv gdiv;          // division by g
   int64_t grains;        // total units / gran
 };
 
@@ -121,6 +137,33 @@ __device__ __forceinline__ int owner_of(const Params &p, int64_t u) {
   const int64_t v = u / p.gran;
   return static_cast<int>(((v + 1) * p.P - 1) / p.grains);
 }
+
+// K blocks in stage ks of a tile: 4, except a shorter last stage when KB is not a multiple of 4.
+__device__ __forceinline__ int stage_blocks(const Params &p, int ks) {
+  return ks == p.KS - 1 ? p.KB - kSB * (p.KS - 1) : kSB;
+}
+
+// Walks (tile, ks, t, mt) over a CTA's units without divisions.
+struct StageIter {
+  int tile, ks, t, mt;
+  __device__ __forceinline__ void init(const Params &p, int64_t u) {
+    tile = static_cast<int>(u / p.KS);
+    ks = static_cast<int>(u % p.KS);
+    t = tile / p.MT;
+    mt = tile % p.MT;
+  }
+  __device__ __forceinline__ void advance(const Params &p, int step) {
+    ks += step;
+    while (ks >= p.KS) {
+      ks -= p.KS;
+      ++tile;
+      if (++mt == p.MT) {
+        mt = 0;
+        ++t;
+      }
+    }
+  }
+};
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -153,57 +196,118 @@ __device__ __forceinline__ GroupConsts group_consts(uint32_t sbits, uint32_t z) 
   return c;
 }
 
-// 8 codes (tile nibble order) -> 4 registers of fp16 pairs (k, k+1), each (q - z) * s rounded once.
+// 8 codes (tile nibble order) -> 4 registers of fp16 pairs (k, k+1) holding q - z exactly.
 // 0x6400 | q is the fp16 1024 + q and 0x6400 | (q << 4) is 1024 + 16 q, both exact; subtracting
-// 1024 + z (or scaling by 1/16 and adding -(64 + z)) gives q - z exactly; one multiply by s rounds.
-__device__ __forceinline__ void dequant_word(uint32_t w, const GroupConsts &c, uint32_t *o) {
+// 1024 + z (or scaling by 1/16 and adding -(64 + z)) leaves the small integer q - z, exact.
+__device__ __forceinline__ void dequant_word_int(uint32_t w, const GroupConsts &c, uint32_t *o) {
   constexpr uint32_t kInv16x2 = 0x2C002C00u;  // (1/16, 1/16)
   const uint32_t w8 = w >> 8;
-  const uint32_t p0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
-  const uint32_t p1 = lop3_and_or(w, 0x00F000F0u, 0x64006400u);
-  const uint32_t p2 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);
-  const uint32_t p3 = lop3_and_or(w8, 0x00F000F0u, 0x64006400u);
-  o[0] = hmul2_rn(hsub2_rn(p0, c.zb2), c.s2);
-  o[1] = hmul2_rn(hfma2_rn(p1, kInv16x2, c.nz2), c.s2);
-  o[2] = hmul2_rn(hsub2_rn(p2, c.zb2), c.s2);
-  o[3] = hmul2_rn(hfma2_rn(p3, kInv16x2, c.nz2), c.s2);
+  o[0] = hsub2_rn(lop3_and_or(w, 0x000F000Fu, 0x64006400u), c.zb2);
+  o[1] = hfma2_rn(lop3_and_or(w, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
+  o[2] = hsub2_rn(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), c.zb2);
+  o[3] = hfma2_rn(lop3_and_or(w8, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
+}
+
+// As dequant_word_int, then one multiply by s: each weight (q - z) * s rounded once to fp16.
+__device__ __forceinline__ void dequant_word(uint32_t w, const GroupConsts &c, uint32_t *o) {
+  dequant_word_int(w, c, o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = hmul2_rn(o[i], c.s2);
 }
 
 // A wait whose outcome is the same for all 32 lanes: the warp then either executes the
 // following .sync.aligned tcgen05 instructions together or leaves the loop together.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          uint32_t *err, uint32_t max_sleep_ns = 128) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err, max_sleep_ns);
+                                          uint32_t *err) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, err);
   return __all_sync(0xffffffffu, ok);
 }
 
 // Waits ignoring the abort flag (used only to drain in-flight copies/MMAs before exit).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait_sleep(bar, parity, 1000000u)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  const uint64_t t0 = clock_cycles();
+  while (!mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
+    if (clock_cycles() - t0 > kWaitLimitCycles) return;
   }
 }
 
-__device__ __forceinline__ void st_f32x4(float *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  *reinterpret_cast<float4 *>(p) = make_float4(__uint_as_float(a), __uint_as_float(b), __uint_as_float(c),
-                                               __uint_as_float(d));
+// Writes 16 consecutive columns (activation rows m0 + c0 ..) of weight row n of a finished tile
+// segment: to y (fp16, rounded once) for a whole tile, else to the CTA's fp32 piece, which is laid
+// out column by column ([BN][128]) so that a warp's 32 rows make one 128-byte line per column.
+template <int BN>
+__device__ __forceinline__ void emit16(const Params &p, bool whole, int n, int m0, int m_end, int c0,
+                                       const float (&v)[16], float *piece) {
+  if (whole) {
+    if (n < p.N) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (m0 + c0 + e < m_end) p.y[static_cast<int64_t>(m0 + c0 + e) * p.N + n] = __float2half_rn(v[e]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) __stcg(piece + (c0 + e) * kTN, v[e]);
+  }
 }
 
-template <int BN, bool GENERAL>
-__global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
+// The fixup of a cut tile, done by the last CTA to finish a piece of it.
+struct Fixup {
+  int tile;     // -1: nothing to do
+  int c_first;  // CTA holding the tile's first K stages (piece 0)
+  int npieces;
+  int slot0;    // piece 0 is that CTA's second slot (its range began in an earlier tile)
+};
+
+// y = the pieces added in K order (piece q >= 1 is CTA c_first + q's first slot). nthreads threads
+// from tid = 0 share the work, element by element in the pieces' column-major order, so stores and
+// loads are coalesced and every thread has several independent loads in flight.
+template <int BN>
+__device__ __forceinline__ void reduce_pieces(const Params &p, const Fixup &f, int tid, int nthreads) {
+  const float *src[kMaxPieces];
+#pragma unroll
+  for (int q = 0; q < kMaxPieces; ++q)
+    src[q] = p.pieces + (static_cast<int64_t>(f.c_first + (q < f.npieces ? q : 0)) * 2 + (q == 0 ? f.slot0 : 0)) *
+                            BN * kTN;
+  const int n0 = (f.tile / p.MT) * kTN;
+  const int m0 = (f.tile % p.MT) * BN;
+  const int ncols = min(p.M, m0 + BN) - m0;
+#pragma unroll 4
+  for (int e = tid; e < ncols * kTN; e += nthreads) {
+    float acc = __ldcg(src[0] + e);
+#pragma unroll
+    for (int q = 1; q < kMaxPieces; ++q)
+      if (q < f.npieces) acc += __ldcg(src[q] + e);
+    const int n = n0 + e % kTN;
+    if (n < p.N) p.y[static_cast<int64_t>(m0 + e / kTN) * p.N + n] = __float2half_rn(acc);
+  }
+  if (tid == 0) p.counters[f.tile] = 0u;  // ready for the next call
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const Params p) {
-  using C = Cfg<BN, GENERAL>;
+  using C = Cfg<BN, MODE>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[C::kStages];
-  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
-  __shared__ __align__(8) uint64_t aempty_bar[C::kASlots];
+  // Per-stage barriers (ring index = local stage index i mod the ring size; every waiter waits on
+  // every phase of the barriers it uses, in order, so no parity wait can skip a phase):
+  //   full[i % S]       the stage's copies landed (producer's expect_tx + the copies' bytes)
+  //   mdone[e][i % S]   the MMAs MMA warp e issued for stage i are complete (one commit per stage):
+  //                     frees the stage for the producer and the A slots of MMA warp e's dequant
+  //                     groups (reused two stages later)
+  //   afull[e][i % 2]   the dequant groups of MMA warp e's blocks (4 warps each) stored their A operands
+  //   dfull / dempty    a tile segment's accumulators are complete / read out by the epilogue
+  __shared__ __align__(8) uint64_t full_bar[S];
+  constexpr int I = C::kIssuers;
+  constexpr int BPI = C::kBPI;
+  __shared__ __align__(8) uint64_t mdone_bar[I][S];
+  __shared__ __align__(8) uint64_t afull_bar[I][C::kASlots];
   __shared__ __align__(8) uint64_t dfull_bar[C::kDBufs];
   __shared__ __align__(8) uint64_t dempty_bar[C::kDBufs];
-  __shared__ __align__(8) uint64_t drain_bar[C::kDqGroups];
+  __shared__ __align__(8) uint64_t drain_bar[I];
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t abort_sh;
-  __shared__ uint32_t last_sh;
+  __shared__ Fixup fix_sh;        // the fixup of the segment the epilogue just finished
+  __shared__ Fixup final_fix_sh;  // the fixup all dequant and epilogue warps do at the end
 
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x / 32;
@@ -212,21 +316,23 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
 
   const int cta = blockIdx.x;
   const int64_t u0 = range_begin(p, cta);
-  const int nu = static_cast<int>(range_begin(p, cta + 1) - u0);
+  const int nst = static_cast<int>(range_begin(p, cta + 1) - u0);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), 1);
+      for (int e = 0; e < I; ++e) mbar_init(smem_u32(&mdone_bar[e][s]), 1);
     }
-    for (int a = 0; a < C::kASlots; ++a) mbar_init(smem_u32(&aempty_bar[a]), 1);
+    for (int e = 0; e < I; ++e) {
+      for (int a = 0; a < C::kASlots; ++a) mbar_init(smem_u32(&afull_bar[e][a]), 4 * BPI);  // groups' warps
+      mbar_init(smem_u32(&drain_bar[e]), 1);
+    }
     for (int d = 0; d < C::kDBufs; ++d) {
-      mbar_init(smem_u32(&dfull_bar[d]), C::kDqGroups);
-      mbar_init(smem_u32(&dempty_bar[d]), 128);
+      mbar_init(smem_u32(&dfull_bar[d]), I);
+      mbar_init(smem_u32(&dempty_bar[d]), 4);
     }
-    for (int w = 0; w < C::kDqGroups; ++w) mbar_init(smem_u32(&drain_bar[w]), 1);
     abort_sh = 0;
-    last_sh = 0;
+    final_fix_sh.tile = -1;
     fence_mbar_init();
   }
   if (warp == C::kDqWarp0) {
@@ -239,252 +345,272 @@ __global__ void __launch_bounds__(Cfg<BN, GENERAL>::kThreads, 1)
   cta_sync_all();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // Programmatic dependent launch: the next grid in the stream may start launching now (its CTAs
+  // take SMs as this grid's CTAs exit). Each role waits for the previous grid before its first
+  // access to global memory that grid could have written: the producer (x, weights) after it has
+  // asked L2 for its first stages' weights (a prefetch only: L2 is the point of coherence), the
+  // epilogue (y, workspace) before its first store. Dequant and MMA warps touch only shared and
+  // tensor memory.
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
-  if (warp < C::kProducers) {
+  if (warp < C::kIssuerWarp0) {
     // ------------------------------------------------------------ producers
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
-      // producer warp pw loads units pw, pw + P, ...; coordinates advance without divisions:
-      // u = (t * MT + mt) * KB + kb
-      const int pw = warp;
-      int kb = static_cast<int>((u0 + pw) % p.KB);
-      const int tile0 = static_cast<int>((u0 + pw) / p.KB);
-      int t = tile0 / p.MT;
-      int mt = tile0 % p.MT;
-      int i = pw;
-      for (; i < nu; i += C::kProducers) {
-        const int s = i % C::kStages;
-        const uint32_t ph = (i / C::kStages) & 1;
-        if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag, p.err)) break;
-        const int kfirst = kb * kTK;
-        const int jlo = min(kfirst / p.g, p.G - 1);
-        int nrec = 1;
-        if (GENERAL) nrec = min((kfirst + kTK - 8) / p.g, p.G - 1) - jlo + 1;
+      if (warp == 0 && nst > 0) {
+        // the codes of the first stages (contiguous within a tile) and their group records
+        StageIter f;
+        f.init(p, u0);
+        const int n0 = min(nst, min(S, p.KS - f.ks));
+        const int kend = min((f.ks + n0) * kStageK, p.K);
+        const int blocks = min((f.ks + n0) * kSB, p.KB) - f.ks * kSB;
+        bulk_prefetch_l2(p.codes + (static_cast<int64_t>(f.t) * p.KB + f.ks * kSB) * kTileBytes, blocks * kTileBytes);
+        const int jlo = p.gdiv.div(f.ks * kStageK);
+        const int jhi = p.gdiv.div(kend - 1);
+        bulk_prefetch_l2(p.meta + (static_cast<int64_t>(f.t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
+      }
+      griddep_wait();
+      StageIter it;
+      it.init(p, u0 + warp);
+      int i = warp;
+      for (; i < nst; i += 2, it.advance(p, 2)) {
+        const int s = i % S;
+        if (i >= S) {  // every MMA warp is done with the stage this slot held
+          const uint32_t ph = ((i / S) - 1) & 1;
+          bool ok = true;
+          for (int e = 0; e < I && ok; ++e) ok = mbar_wait(smem_u32(&mdone_bar[e][s]), ph, abort_flag, p.err);
+          if (!ok) break;
+        }
+        const int nb = stage_blocks(p, it.ks);
+        const int k0 = it.ks * kStageK;
+        const int jlo = p.gdiv.div(k0);
+        const int jhi = p.gdiv.div(min(k0 + nb * kTK, p.K) - 1);
+        const int nrec = jhi - jlo + 1;
         const uint32_t stage = smem_base + s * C::kStageBytes;
         const uint32_t bar = smem_u32(&full_bar[s]);
-        mbar_arrive_expect_tx(bar, C::kXBytes + kTileBytes + nrec * kRecBytes);
-        tma_load_2d(stage, &x_map, kfirst, mt * BN, bar);
-        bulk_g2s(stage + C::kXBytes, p.codes + (static_cast<int64_t>(t) * p.KB + kb) * kTileBytes, kTileBytes, bar,
-                 pol_stream);
-        bulk_g2s(stage + C::kXBytes + kTileBytes, p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes,
-                 nrec * kRecBytes, bar, pol_stream);
-        kb += C::kProducers;
-        while (kb >= p.KB) {
-          kb -= p.KB;
-          if (++mt == p.MT) {
-            mt = 0;
-            ++t;
-          }
+        // the 3-D box always lands whole (zero fill past the last K block); the 2-D boxes per block
+        const uint32_t xbytes = p.x3d ? C::kXBytes : nb * C::kXSub;
+        mbar_arrive_expect_tx(bar, xbytes + nb * kTileBytes + nrec * kRecBytes);
+        if (p.x3d) {
+          tma_load_3d(stage, &x_map, 0, it.mt * BN, it.ks * kSB, bar);
+        } else {
+          for (int b = 0; b < nb; ++b) tma_load_2d(stage + b * C::kXSub, &x_map, k0 + b * kTK, it.mt * BN, bar);
         }
+        bulk_g2s(stage + C::kXBytes, p.codes + (static_cast<int64_t>(it.t) * p.KB + it.ks * kSB) * kTileBytes,
+                 nb * kTileBytes, bar, pol_stream);
+        bulk_g2s(stage + C::kXBytes + C::kCodeBytes, p.meta + (static_cast<int64_t>(it.t) * p.G + jlo) * kRecBytes,
+                 nrec * kRecBytes, bar, pol_stream);
       }
       if (*abort_flag) {
         // let every copy this warp issued land before the CTA's shared memory goes away
-        for (int j = i - C::kProducers; j >= 0 && j >= i - C::kStages; j -= C::kProducers)
-          drain_wait(smem_u32(&full_bar[j % C::kStages]), (j / C::kStages) & 1);
+        for (int j = i - 2; j >= 0 && j >= i - S; j -= 2) drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1);
+      }
+    }
+  } else if (warp < C::kDqWarp0) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const int e = warp - C::kIssuerWarp0;  // blocks e * BPI .. e * BPI + BPI - 1 of every stage
+      constexpr uint32_t idesc = idesc_f16_f32(128, BN);
+      StageIter it;
+      it.init(p, u0);
+      int seg = 0;          // segment (tile) index within the CTA's range
+      int seg_tile = it.tile;
+      int seg_freed = 0;    // segments below this one are known to be read out by the epilogue
+      bool started = false; // this warp issued an MMA into the current segment's accumulator
+      bool ok = true;
+      for (int i = 0; i < nst; ++i, it.advance(p, 1)) {
+        if (it.tile != seg_tile) {
+          mma_commit(smem_u32(&dfull_bar[seg % C::kDBufs]));
+          ++seg;
+          seg_tile = it.tile;
+          started = false;
+        }
+        const int nb = stage_blocks(p, it.ks);
+        if (BPI * e < nb && !started) {
+          // before the first MMA into a reused accumulator set, the epilogue must have read it out:
+          // wait for every earlier segment's release in order, so no parity wait skips a phase
+          for (; ok && seg_freed <= seg - C::kDBufs; ++seg_freed)
+            ok = mbar_wait(smem_u32(&dempty_bar[seg_freed % C::kDBufs]), (seg_freed / C::kDBufs) & 1, abort_flag,
+                           p.err);
+        }
+        const uint32_t dcol = tmem + ((seg % C::kDBufs) * I + e) * C::kDStride;
+        // the dequant groups stored their A operands; they saw the stage land before that, which
+        // orders the x tile's arrival before these MMAs
+        if (ok) ok = mbar_wait(smem_u32(&afull_bar[e][i % C::kASlots]), (i / C::kASlots) & 1, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t xs = smem_base + (i % S) * C::kStageBytes;
+#pragma unroll
+        for (int bb = 0; bb < BPI; ++bb) {
+          const int b = BPI * e + bb;
+          if (b >= nb) break;
+          const uint64_t bdesc = sw128_kmajor_desc(xs + b * C::kXSub);
+          const uint32_t acol = tmem + C::kACol0 + (b * C::kASlots + i % C::kASlots) * 32;
+#pragma unroll
+          for (int kk = 0; kk < kTK / 16; ++kk) {
+            // A: 128 x 16 fp16 in tensor memory (8 columns per 16 K); B: 16 K-columns of the x block
+            const bool fresh = kk == 0 && !started;
+            mma_f16_ts(dcol, acol + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), idesc, fresh ? 0u : 1u);
+          }
+          started = true;
+        }
+        mma_commit(smem_u32(&mdone_bar[e][i % S]));
+      }
+      if (ok && nst > 0) mma_commit(smem_u32(&dfull_bar[seg % C::kDBufs]));
+      if (*abort_flag) {
+        mma_commit(smem_u32(&drain_bar[e]));
+        drain_wait(smem_u32(&drain_bar[e]), 0);
       }
     }
   } else if (warp < C::kEpiWarp0) {
-    // ------------------------------------------------- dequant + MMA issue
-    // Group dq takes K blocks i = dq, dq + kDqGroups, ...: thread r dequantizes weight row r into
-    // a tensor-memory slot; after a group barrier the group's first thread issues the block's four
-    // MMAs into the group's own accumulator and commits the stage and the slot. That thread also
-    // keeps the group's part of the accumulator protocol: before the group's first block of a
-    // segment (tile) it waits for the segment's accumulator set to be free, and it commits dfull
-    // once for every segment of the CTA's range when the group is past it (a commit covers the
-    // committing thread's own MMAs, so the same thread issues and commits).
-    const int dq = (warp - C::kDqWarp0) / 4;
-    const bool issuer = warp == C::kDqWarp0 + 4 * dq && lane == 0;
+    // ------------------------------------------------------------ dequant
+    // Group d takes K block d of every stage: thread r turns weight row r's 64 codes into the
+    // A slot (d, i % 2), then its warp counts itself in on MMA warp d / BPI's afull barrier. A group
+    // with no block in a (short) stage still takes part in every wait and arrival.
+    const int d = (warp - C::kDqWarp0) / 4;
+    const int e = d / BPI;
     const int lq = warp % 4;  // tensor-memory lane quarter this warp may access
     const int r = lq * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
-    constexpr uint32_t idesc = idesc_f16_f32(128, BN);
-    const int64_t tile0 = u0 / p.KB;
-    const int seg_count = static_cast<int>((u0 + nu - 1) / p.KB - tile0) + 1;
-    int kb = static_cast<int>((u0 + dq) % p.KB);                  // K block of unit i
-    int seg_i = static_cast<int>((u0 + dq) / p.KB - tile0);        // segment of unit i
-    int prev_seg = -1;       // segment of this group's previous block
-    int seg_closed = 0;      // segments below this one have had this group's dfull commit
-    int seg_freed = 0;       // segments below this one are known to be read out by the epilogue
-    bool issue_ok = true;    // the issuer's own waits (shared with the group at the next barrier)
-    for (int i = dq; i < nu; i += C::kDqGroups) {
-      const int s = i % C::kStages;
-      const int a = i % C::kASlots;
-      const int db = seg_i % C::kDBufs;
-      bool okw = warp_wait(smem_u32(&full_bar[s]), (i / C::kStages) & 1, abort_flag, p.err);
-      uint32_t out[32];
-      if (okw) {
-        const uint32_t codes = smem_base + s * C::kStageBytes + C::kXBytes;
-        const uint32_t meta = codes + kTileBytes;
+    StageIter it;
+    it.init(p, u0);
+    for (int i = 0; i < nst; ++i, it.advance(p, 1)) {
+      const int s = i % S;
+      if (!warp_wait(smem_u32(&full_bar[s]), (i / S) & 1, abort_flag, p.err)) break;
+      const bool have = d < stage_blocks(p, it.ks);
+      // the A slot's previous stage (i - 2) must have gone through its MMAs
+      if (i >= C::kASlots &&
+          !warp_wait(smem_u32(&mdone_bar[e][(i - C::kASlots) % S]), ((i - C::kASlots) / S) & 1, abort_flag, p.err))
+        break;
+      if (have) {
+        const uint32_t stage = smem_base + s * C::kStageBytes;
+        const uint32_t codes = stage + C::kXBytes + d * kTileBytes;
+        const uint32_t recs = stage + C::kXBytes + C::kCodeBytes;
         const uint4 w0 = lds128(codes + r * 16);
         const uint4 w1 = lds128(codes + 2048 + r * 16);
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        if (!GENERAL) {
-          const uint32_t z = (lds8(meta + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
-          const GroupConsts c = group_consts(lds16(meta + 2 * r), z);
-#pragma unroll
-          for (int ci = 0; ci < 8; ++ci) dequant_word(words[ci], c, &out[4 * ci]);
-        } else {
-          const int kfirst = kb * kTK;
-          const int jlo = min(kfirst / p.g, p.G - 1);
-          int j = jlo;
-#pragma unroll
-          for (int ci = 0; ci < 8; ++ci) {
-            const int kc = kfirst + 8 * ci;
-            if (kc >= (j + 1) * p.g && j < p.G - 1) ++j;  // g >= 8: at most one group boundary per 8 codes
-            const uint32_t rec = meta + (j - jlo) * kRecBytes;
-            const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
-            dequant_word(words[ci], group_consts(lds16(rec + 2 * r), z), &out[4 * ci]);
-          }
-        }
-        // the slot's previous block (i - kASlots) is this group's too: its MMAs must be done
-        okw = warp_wait(smem_u32(&aempty_bar[a]), ((i / C::kASlots) & 1) ^ 1, abort_flag, p.err);
-      }
-      if (okw) {
+        const int kfirst = (it.ks * kSB + d) * kTK;
+        const int jlo = p.gdiv.div(it.ks * kStageK);
+        const uint32_t acol = tmem + lane_addr + C::kACol0 + (d * C::kASlots + i % C::kASlots) * 32;
         tc_fence_after();
-        tmem_st_32x32b_x32(tmem + lane_addr + C::kACol0 + a * 32, out);
-        tmem_wait_st();
-        tc_fence_before();
-      }
-      // one decision for the whole group: go on together or stop together
-      if (!named_bar_and(2 + dq, 128, okw && issue_ok)) break;
-      if (issuer) {
-        for (; seg_closed < seg_i; ++seg_closed) mma_commit(smem_u32(&dfull_bar[seg_closed % C::kDBufs]));
-        const bool first = prev_seg != seg_i;
-        // before the first block of segment seg_i, the accumulator set it reuses must be read out,
-        // i.e. segment seg_i - kDBufs finished. The group may have had no block in some segments:
-        // wait for every segment's phase in order, so no parity wait can skip a phase.
-        for (; first && issue_ok && seg_freed <= seg_i - C::kDBufs; ++seg_freed)
-          issue_ok = mbar_wait(smem_u32(&dempty_bar[seg_freed % C::kDBufs]), (seg_freed / C::kDBufs) & 1,
-                               abort_flag, p.err);
-        if (issue_ok) {
-          tc_fence_after();
-          const uint64_t bdesc = sw128_kmajor_desc(smem_base + s * C::kStageBytes);
-          const uint32_t dcol = tmem + (db * C::kDqGroups + dq) * C::kDStride;
+        if (MODE != kGeneral) {
+          const uint32_t rec = recs + (p.gdiv.div(kfirst) - jlo) * kRecBytes;  // g % 64 == 0: one group per block
+          const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
+          const GroupConsts gc = group_consts(lds16(rec + 2 * r), z);
 #pragma unroll
-          for (int kk = 0; kk < kTK / 16; ++kk) {
-            // A: 128 x 16 fp16 in tensor memory (8 columns per 16 K); B: 16 K-columns of the x tile
-            mma_f16_ts(dcol, tmem + C::kACol0 + a * 32 + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                       (first && kk == 0) ? 0u : 1u);
+          for (int h = 0; h < 2; ++h) {  // two halves of 16 columns: fewer registers live at once
+            uint32_t out[16];
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) dequant_word(words[4 * h + ci], gc, &out[4 * ci]);
+            tmem_st_32x32b_x16(acol + 16 * h, out);
           }
-          mma_commit(smem_u32(&empty_bar[s]));
-          mma_commit(smem_u32(&aempty_bar[a]));
+        } else {
+          int j = p.gdiv.div(kfirst);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t out[16];
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+              const int kc = kfirst + 8 * (4 * h + ci);
+              if (kc >= (j + 1) * p.g && j < p.G - 1) ++j;  // g >= 8: at most one group boundary per 8 codes
+              const uint32_t rec = recs + (j - jlo) * kRecBytes;
+              const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
+              dequant_word(words[4 * h + ci], group_consts(lds16(rec + 2 * r), z), &out[4 * ci]);
+            }
+            tmem_st_32x32b_x16(acol + 16 * h, out);
+          }
         }
       }
-      prev_seg = seg_i;
-      kb += C::kDqGroups;
-      while (kb >= p.KB) {
-        kb -= p.KB;
-        ++seg_i;
-      }
-    }
-    if (issuer) {
-      // segments after the group's last block (or all of them if it had none) still need its commit
-      for (; seg_closed < seg_count; ++seg_closed) mma_commit(smem_u32(&dfull_bar[seg_closed % C::kDBufs]));
-      if (*abort_flag) {
-        mma_commit(smem_u32(&drain_bar[dq]));
-        drain_wait(smem_u32(&drain_bar[dq]), 0);
-      }
+      if (have) tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&afull_bar[e][i % C::kASlots]));
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int lq = warp % 4;
     const int r = lq * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
-    const int64_t u_end = u0 + nu;
+    const int64_t u_end = u0 + nst;
+    griddep_wait();  // y and the workspace may still be in use by the previous grid
     int seg = 0;
     for (int64_t u = u0; u < u_end; ++seg) {
-      const int tile = static_cast<int>(u / p.KB);
-      const int64_t tile_end = static_cast<int64_t>(tile + 1) * p.KB;
-      const int64_t seg_end = min(u_end, tile_end);
-      const bool whole = (u % p.KB == 0) && seg_end == tile_end;
-      const int db = seg % C::kDBufs;
-      // the epilogue waits a whole tile for its accumulator: sleep longer between looks
-      if (!warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err, 1024)) break;
-      tc_fence_after();
+      const int tile = static_cast<int>(u / p.KS);
+      const int64_t tile_u0 = static_cast<int64_t>(tile) * p.KS;
+      const int64_t seg_end = min(u_end, tile_u0 + p.KS);
+      const int ks_first = static_cast<int>(u - tile_u0);
+      const int ks_last = static_cast<int>(seg_end - 1 - tile_u0);
+      const bool whole = ks_first == 0 && ks_last == p.KS - 1;
       const int t = tile / p.MT;
       const int m0 = (tile % p.MT) * BN;
       const int m_end = min(p.M, m0 + BN);
       const int n = t * kTN + r;
-      float *piece = p.pieces + ((static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * kTN + r) * BN;
-      // dequant groups that took a block of this segment: all of them unless the segment is shorter
-      const int i_first = static_cast<int>(u - u0);
-      const int seg_len = static_cast<int>(seg_end - u);
-      uint32_t contrib = 0;
-      for (int j = 0; j < seg_len && j < C::kDqGroups; ++j) contrib |= 1u << ((i_first + j) % C::kDqGroups);
-      const int w_first = __ffs(contrib) - 1;
+      float *piece = p.pieces + (static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * BN * kTN + r;
+      const int db = seg % C::kDBufs;
+      // MMA warp e took part iff some stage of the segment has more than BPI * e K blocks (only a
+      // tile's last stage can be short)
+      const int nparts = ks_first < ks_last ? I : (stage_blocks(p, ks_last) + BPI - 1) / BPI;
+      const bool ok = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err);
+      if (!named_bar_and(1, 128, ok)) break;
+      tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
         uint32_t v[16];
-        const uint32_t dbase = tmem + lane_addr + db * C::kDqGroups * C::kDStride + c0;
-        tmem_ld_32x32b_x16(dbase + w_first * C::kDStride, v);
+        const uint32_t dbase = tmem + lane_addr + db * I * C::kDStride + c0;
+        tmem_ld_32x32b_x16(dbase, v);
         tmem_wait_ld();
+        float f[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) f[q] = __uint_as_float(v[q]);
 #pragma unroll 1
-        for (int w = w_first + 1; w < C::kDqGroups; ++w) {  // the groups' partial sums, in a fixed order
-          if (!(contrib >> w & 1u)) continue;
-          uint32_t v2[16];
-          tmem_ld_32x32b_x16(dbase + w * C::kDStride, v2);
+        for (int e = 1; e < nparts; ++e) {  // the MMA warps' partial sums, in a fixed order
+          tmem_ld_32x32b_x16(dbase + e * C::kDStride, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(v2[e]));
+          for (int q = 0; q < 16; ++q) f[q] += __uint_as_float(v[q]);
         }
-        if (whole) {
-          if (n < p.N) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (m0 + c0 + e < m_end)
-                p.y[static_cast<int64_t>(m0 + c0 + e) * p.N + n] = __float2half_rn(__uint_as_float(v[e]));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) st_f32x4(piece + c0 + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
-        }
+        emit16<BN>(p, whole, n, m0, m_end, c0, f, piece);
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&dempty_bar[db]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[db]));
       if (!whole) {
-        // the last CTA to finish a piece of this tile adds all pieces in K order and writes y
-        const int c_first = owner_of(p, static_cast<int64_t>(tile) * p.KB);
-        const int c_last = owner_of(p, tile_end - 1);
-        __threadfence();
+        // the last CTA to finish a piece of this tile adds all pieces in K order and writes y. The
+        // warpgroup's piece stores are ordered before one thread's release (fence, then the count);
+        // the thread that sees the last count acquires (fence) before the pieces are read.
         __syncwarp();
         named_bar_sync(1, 128);
         if (r == 0) {
+          __threadfence();
+          Fixup f;
+          f.c_first = owner_of(p, tile_u0);
+          f.npieces = owner_of(p, tile_u0 + p.KS - 1) - f.c_first + 1;
+          f.slot0 = range_begin(p, f.c_first) != tile_u0 ? 1 : 0;
           const uint32_t old = atomicAdd(&p.counters[tile], 1u);
-          last_sh = (old == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
+          f.tile = old == static_cast<uint32_t>(f.npieces - 1) ? tile : -1;
+          if (f.tile >= 0) __threadfence();
+          fix_sh = f;
+          // the CTA's last segment: every dequant and epilogue warp is free after it, so they all do
+          // this fixup together below
+          if (seg_end == u_end) final_fix_sh = f;
         }
         __syncwarp();
         named_bar_sync(1, 128);
-        if (last_sh) {
-          __threadfence();
-          // all pieces' loads of a 2-column slice are in flight together, then added in K order
-          const int npieces = c_last - c_first + 1;
-          uint32_t slot_mask = 0;  // bit q: piece q is CTA (c_first + q)'s second slot
-          for (int q = 0; q < npieces; ++q)
-            if (range_begin(p, c_first + q) / p.KB != tile) slot_mask |= 1u << q;
-          const float *base = p.pieces + (static_cast<int64_t>(c_first) * 2 * kTN + r) * BN;
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 2) {
-            float2 v[kMaxPieces];
-#pragma unroll
-            for (int q = 0; q < kMaxPieces; ++q)
-              if (q < npieces)
-                v[q] = __ldcg(reinterpret_cast<const float2 *>(base + (2 * q + (slot_mask >> q & 1u)) * kTN * BN + c0));
-            float2 acc = v[0];
-#pragma unroll
-            for (int q = 1; q < kMaxPieces; ++q)
-              if (q < npieces) {
-                acc.x += v[q].x;
-                acc.y += v[q].y;
-              }
-            if (n < p.N) {
-              if (m0 + c0 < m_end) p.y[static_cast<int64_t>(m0 + c0) * p.N + n] = __float2half_rn(acc.x);
-              if (m0 + c0 + 1 < m_end) p.y[static_cast<int64_t>(m0 + c0 + 1) * p.N + n] = __float2half_rn(acc.y);
-            }
-          }
-          if (r == 0) p.counters[tile] = 0u;  // ready for the next call
-        }
+        if (fix_sh.tile >= 0 && seg_end != u_end) reduce_pieces<BN>(p, fix_sh, r, 128);
       }
       u = seg_end;
+    }
+  }
+
+  if (warp >= C::kDqWarp0) {
+    // the dequant warps (past their last stage) and the epilogue warpgroup (past its last segment)
+    // do the fixup of the CTA's last segment together, if this CTA finished that tile last
+    constexpr int kFixThreads = 32 * (C::kEpiWarp0 + 4 - C::kDqWarp0);
+    __syncwarp();
+    named_bar_sync(3, kFixThreads);
+    if (final_fix_sh.tile >= 0) {
+      griddep_wait();  // (already resolved: the epilogue waited before its first store)
+      reduce_pieces<BN>(p, final_fix_sh, static_cast<int>(threadIdx.x) - 32 * C::kDqWarp0, kFixThreads);
     }
   }
 
@@ -519,10 +645,24 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// x [M, K] fp16 row-major, boxes of 64 (K) x BN (rows), 128-byte swizzle, zero fill outside.
-bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn) {
+// x [M, K] fp16 row-major, 128-byte swizzle, zero fill outside, in one of two views:
+//  3-D [K/64][M][64] (K a multiple of 64): one box {64, BN, 4} is a whole stage, four BN x 64
+//      sub-tiles one after another, each laid out as the MMA reads it;
+//  2-D [M][K]: one box {64, BN} per K block.
+bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, bool three_d) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
+  if (three_d) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kTK), static_cast<cuuint64_t>(M),
+                                static_cast<cuuint64_t>(K / kTK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(kTK) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kTK), static_cast<cuuint32_t>(bn),
+                               static_cast<cuuint32_t>(kSB)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTK), static_cast<cuuint32_t>(bn)};
@@ -532,10 +672,10 @@ bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool GENERAL>
+template <int BN, int MODE>
 cudaError_t launch_t(const CUtensorMap &map, const Params &p, int ctas, cudaStream_t stream) {
-  using C = Cfg<BN, GENERAL>;
-  auto kern = w4a16_gemm_kernel<BN, GENERAL>;
+  using C = Cfg<BN, MODE>;
+  auto kern = w4a16_gemm_kernel<BN, MODE>;
   // the dynamic shared-memory opt-in is a per-device function attribute
   static uint64_t done_mask = 0;
   static std::mutex mu;
@@ -550,19 +690,44 @@ cudaError_t launch_t(const CUtensorMap &map, const Params &p, int ctas, cudaStre
       if (dev < 64) done_mask |= 1ull << dev;
     }
   }
-  kern<<<ctas, C::kThreads, C::kSmemBytes, stream>>>(map, p);
+  // programmatic stream serialization: the launch may overlap the previous kernel's tail (the kernel
+  // waits for it with griddepcontrol.wait before touching global memory)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, map, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <bool GENERAL>
-cudaError_t launch_bn(int bn, const CUtensorMap &map, const Params &p, int ctas, cudaStream_t stream) {
-  switch (bn) {
-    case 16: return launch_t<16, GENERAL>(map, p, ctas, stream);
-    case 32: return launch_t<32, GENERAL>(map, p, ctas, stream);
-    case 64: return launch_t<64, GENERAL>(map, p, ctas, stream);
-    case 128: return launch_t<128, GENERAL>(map, p, ctas, stream);
-    default: return cudaErrorInvalidValue;
+// Scale outside needs each 128-wide half-stage inside one quantization group (g % 128 == 0) and
+// BN <= 32; scale inside needs each 64-wide block inside one group (g % 64 == 0).
+int gemm_mode(int bn, int32_t g) {
+  (void)bn;
+  return g % 64 == 0 ? kScaleIn : kGeneral;
+}
+
+cudaError_t launch_variant(int bn, int mode, const CUtensorMap &map, const Params &p, int ctas,
+                           cudaStream_t stream) {
+  if (mode == kScaleIn) {
+    if (bn == 16) return launch_t<16, kScaleIn>(map, p, ctas, stream);
+    if (bn == 32) return launch_t<32, kScaleIn>(map, p, ctas, stream);
+    if (bn == 64) return launch_t<64, kScaleIn>(map, p, ctas, stream);
+    if (bn == 128) return launch_t<128, kScaleIn>(map, p, ctas, stream);
+  } else {
+    if (bn == 16) return launch_t<16, kGeneral>(map, p, ctas, stream);
+    if (bn == 32) return launch_t<32, kGeneral>(map, p, ctas, stream);
+    if (bn == 64) return launch_t<64, kGeneral>(map, p, ctas, stream);
+    if (bn == 128) return launch_t<128, kGeneral>(map, p, ctas, stream);
   }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -574,15 +739,15 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
   if (bn == 0) bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
   if (bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
-  const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK);
+  const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK), ks = cdiv(kb, kSB);
   const int64_t tiles = mt * nt;
-  const int64_t units = tiles * kb;
+  const int64_t units = tiles * ks;
   if (tiles > 0x7FFFFFFF || units > (int64_t{1} << 40)) return false;
   int64_t P = ctas > 0 ? ctas : (num_sms > 0 ? num_sms : 148);
   // whole-tile scheduling when every CTA gets many tiles (imbalance <= 1/8) or the tiles divide
-  // evenly; otherwise stream-K over 64-wide K blocks, which needs the partial-tile fixup
+  // evenly; otherwise stream-K over 256-wide K stages, which needs the partial-tile fixup
   bool whole = schedule == 2 || (schedule == 0 && (tiles >= 8 * P || (tiles >= P && tiles % P == 0)));
-  const int64_t gran = whole ? kb : 1;
+  const int64_t gran = whole ? ks : 1;
   const int64_t grains = units / gran;
   P = std::min(P, grains);
   if (!whole) {
@@ -591,8 +756,8 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
     auto max_pieces = [&](int64_t PP) {
       int64_t worst = 1;
       for (int64_t tt = 0; tt < tiles; ++tt) {
-        const int64_t first = ((tt * kb + 1) * PP - 1) / units;
-        const int64_t last = (((tt + 1) * kb) * PP - 1) / units;
+        const int64_t first = ((tt * ks + 1) * PP - 1) / units;
+        const int64_t last = (((tt + 1) * ks) * PP - 1) / units;
         worst = std::max(worst, last - first + 1);
       }
       return worst;
@@ -603,8 +768,10 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
   plan->m_tiles = static_cast<int>(mt);
   plan->n_tiles = static_cast<int>(nt);
   plan->k_blocks = static_cast<int>(kb);
+  plan->k_stages = static_cast<int>(ks);
   plan->ctas = static_cast<int>(P);
   plan->gran = static_cast<int>(gran);
+  plan->whole = whole;
   plan->grains = grains;
   plan->counters_offset = 256;
   const size_t counters_bytes = static_cast<size_t>(cdiv(tiles * 4, 256) * 256);
@@ -618,7 +785,8 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
                         void *workspace, const GemmPlan &plan, cudaStream_t stream, bool *encode_failed) {
   *encode_failed = false;
   CUtensorMap map;
-  if (!make_x_map(&map, x, M, K, plan.block_n)) {
+  bool x3d = K % kTK == 0 && make_x_map(&map, x, M, K, plan.block_n, true);
+  if (!x3d && !make_x_map(&map, x, M, K, plan.block_n, false)) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
@@ -634,16 +802,17 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.g = g;
+  p.gdiv = make_fastdiv(static_cast<uint32_t>(g));
   p.G = static_cast<int>(cdiv(K, g));
   p.NT = plan.n_tiles;
   p.KB = plan.k_blocks;
+  p.KS = plan.k_stages;
   p.MT = plan.m_tiles;
   p.P = plan.ctas;
   p.gran = plan.gran;
+  p.x3d = x3d ? 1 : 0;
   p.grains = plan.grains;
-  const bool general = (g % kTK) != 0;
-  return general ? launch_bn<true>(plan.block_n, map, p, plan.ctas, stream)
-                 : launch_bn<false>(plan.block_n, map, p, plan.ctas, stream);
+  return launch_variant(plan.block_n, gemm_mode(plan.block_n, g), map, p, plan.ctas, stream);
 }
 
 }  // namespace w4

@@ -9,7 +9,7 @@ namespace w4 {
 
 // Tile layout constants (the code tiles and group records of w4_repack).
 constexpr int kTN = 128;         // weight rows per tile (the MMA's M)
-constexpr int kTK = 64;          // codes along K per tile (one pipeline stage)
+constexpr int kTK = 64;          // codes along K per tile (one K block)
 constexpr int kTileBytes = 4096; // 128 rows x 64 codes x 4 bits
 constexpr int kRecBytes = 320;   // 128 fp16 scales + 128 4-bit zeros
 
@@ -22,12 +22,14 @@ cudaError_t launch_repack(const uint32_t *qw, const void *scales, const uint32_t
                           int32_t g, void *packed, cudaStream_t stream);
 
 struct GemmPlan {
-  int block_n;   // activation rows per tile: 16, 32, 64, 128 or 256
+  int block_n;   // activation rows per tile: 16, 32, 64 or 128
   int m_tiles;
   int n_tiles;
   int k_blocks;
+  int k_stages;  // 256-wide K stages (4 K blocks; the last may be shorter)
   int ctas;      // persistent CTAs (one per SM)
-  int gran;      // K blocks per scheduling grain: 1 (stream-K) or k_blocks (whole tiles)
+  int gran;      // K stages per scheduling grain: 1 (stream-K) or k_stages (whole tiles)
+  bool whole;    // whole-tile schedule (no tile is cut between CTAs)
   int64_t grains;
   size_t counters_offset;
   size_t pieces_offset;

@@ -12,17 +12,18 @@ namespace w4 {
 // Device error bits written into the workspace error word.
 constexpr uint32_t kDevErrTimeout = 1u;
 
-// A pipeline wait gives up after this long (ns of %globaltimer).
-constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
+// A pipeline wait gives up after this many SM clock cycles (%clock64, local to
+// the SM and cheap to read: about 1.5 s at the top clock of 2.07 GHz).
+constexpr uint64_t kWaitLimitCycles = 3ull * 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ uint64_t clock_cycles() {
+  uint64_t c;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+  return c;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ----------------------------------------------------------------- mbarrier
@@ -72,32 +73,37 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Waits for the phase of `bar` with the given parity to complete. Returns
 // false (and raises the CTA's abort flag and the device error word) when the
-// wait runs past kWaitLimitNs, or once another thread of the CTA aborted.
-// A waiter that does not succeed at once backs off with __nanosleep (doubling
-// up to `max_sleep_ns`): a polling warp would take issue slots from the few
-// threads that issue the copies and MMAs. The clock and the abort flag are
-// looked at every 16th attempt only.
+// wait runs past kWaitLimitCycles, or once another thread of the CTA aborted.
+// A waiter that does not succeed at once is parked by the hardware
+// (try_wait with a suspend-time hint) until the phase completes or about
+// kSuspendNs pass: it takes no issue slots meanwhile and resumes as soon as
+// the phase completes. The time limit is kept with %clock64: reading the
+// global timer costs a few hundred nanoseconds, too much for a pipeline wait.
+constexpr uint32_t kSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          uint32_t *err_word, uint32_t max_sleep_ns = 128) {
+                                          uint32_t *err_word) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = 0;
-  uint32_t sleep_ns = 16;
-  for (uint32_t n = 1;; ++n) {
-    __nanosleep(sleep_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    sleep_ns = sleep_ns * 2 > max_sleep_ns ? max_sleep_ns : sleep_ns * 2;
-    if ((n & 15) == 0) {
-      if (*abort_flag) return false;
-      const uint64_t now = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
-        *abort_flag = 1u;
-        atomicOr(err_word, kDevErrTimeout);
-        return false;
-      }
+  const uint64_t t0 = clock_cycles();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+    if (*abort_flag) return false;
+    if (clock_cycles() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1u;
+      atomicOr(err_word, kDevErrTimeout);
+      return false;
     }
   }
+}
+
+// ------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: wait until the grids this launch depends on have completed and
+// their memory is visible (returns at once when the launch had no programmatic dependency), and
+// let the next grid in the stream start launching (its CTAs take SMs as this grid's CTAs exit).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------- async copies
@@ -113,6 +119,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (a hint: no data dependency, no completion to wait for).
+// src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared through a tensor map (TMA).
 // c0 is the innermost coordinate; c0 * element size must be a multiple of 16.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
@@ -121,6 +133,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared through a tensor map (TMA); c0 innermost (aligned as above).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
 
@@ -189,6 +211,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
       "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
       "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
       "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// Each thread of the warp stores 16 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
