@@ -11,15 +11,15 @@
 // group records they need and the four x sub-tiles, moved by three copies
 // (one thread can issue a bulk copy only every ~350 cycles, so copies are
 // made large). Warp roles (one CTA per SM):
-//   2 producer warps (lane 0) take the stages in turn: a TMA tensor copy of
-//                   x (128-byte swizzle, zero fill outside [M, K]) and two
-//                   bulk copies (codes, group records) on the stage's mbarrier.
+//   2 producer warps take the stages in turn (lane 0 issues): a TMA tensor
+//                   copy of x (128-byte swizzle, zero fill outside [M, K]) and
+//                   two bulk copies (codes, group records) on the stage's mbarrier.
 //   4 dequant warpgroups: group d turns K block d of every stage into fp16
 //                   w = (q - z) * s in tensor memory (thread r owns weight row
 //                   r; tcgen05.st), the MMA's A operand; shared memory only
 //                   holds 4-bit codes. A group never waits for the MMAs of its
-//                   own block, only for its two tensor-memory slots to come free.
-//   4 MMA warps (2 for BN = 128; lane 0): warp e issues the MMAs of its K
+//                   own block, only for its tensor-memory slots to come free.
+//   4 MMA warps (2 for BN = 128; lane 0 issues): warp e issues the MMAs of its K
 //                   block(s) of every stage into its own accumulator and commits
 //                   once per stage (a thread issues a tcgen05.mma only every
 //                   ~50-130 cycles, so the issue is spread over several warps).
@@ -71,19 +71,24 @@ struct Cfg {
   // two for BN = 128, whose accumulators would not fit four times into tensor memory
   static constexpr int kIssuers = BN == 128 ? 2 : 4;
   static constexpr int kBPI = kSB / kIssuers;  // K blocks per MMA warp and stage
-  static constexpr int kASlots = 2;     // tensor-memory A slots per dequant group (32 columns each)
+  // tensor-memory A slots per dequant group (32 columns each): a group runs this many stages ahead of
+  // its MMA warp. Narrow tiles take a third slot and give up a second accumulator set for it.
+  static constexpr int kASlots = BN <= 32 ? 3 : 2;
   static constexpr int kDStride = BN < 32 ? 32 : BN;
-  static constexpr int kDBufs = BN <= 32 ? 2 : 1;  // accumulator sets (the epilogue overlaps the next tile)
-  static constexpr int kACol0 = 256;
+  static constexpr int kDBufs = (BN <= 32 && kASlots == 2) ? 2 : 1;  // accumulator sets
+  static constexpr int kACol0 = kIssuers * kDBufs * kDStride;  // accumulators first, then the A slots
   static constexpr int kTmemCols = 512;
   static constexpr int kIssuerWarp0 = 2;
   static constexpr int kDqWarp0 = kIssuerWarp0 + kIssuers;
-  static constexpr int kEpiWarp0 = kDqWarp0 + 4 * kSB;
+  static constexpr int kEpiWarp0 = kDqWarp0 + 4 * kSB;  // one dequant warpgroup per K block of a stage
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   static_assert(kStages >= 2, "stage ring");
-  static_assert(kIssuers * kDBufs * kDStride <= kACol0, "accumulators below the A slots");
   static_assert(kACol0 + kSB * kASlots * 32 <= kTmemCols, "tensor memory budget");
+  // a dequant group waits on the MMA-done barrier of stage i - kASlots; the next phase of that barrier
+  // (stage i - kASlots + kStages) needs the group's own arrival for that stage, so it cannot come
+  // before this wait as long as the stage ring is at least as long as the A-slot ring
+  static_assert(kStages >= kASlots, "stage ring at least as long as the A-slot ring");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
 };
 
@@ -355,32 +360,33 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
 
   if (warp < C::kIssuerWarp0) {
     // ------------------------------------------------------------ producers
-    if (lane == 0) {
-      const uint64_t pol_stream = policy_evict_first();
-      if (warp == 0 && nst > 0) {
-        // the codes of the first stages (contiguous within a tile) and their group records
-        StageIter f;
-        f.init(p, u0);
-        const int n0 = min(nst, min(S, p.KS - f.ks));
-        const int kend = min((f.ks + n0) * kStageK, p.K);
-        const int blocks = min((f.ks + n0) * kSB, p.KB) - f.ks * kSB;
-        bulk_prefetch_l2(p.codes + (static_cast<int64_t>(f.t) * p.KB + f.ks * kSB) * kTileBytes, blocks * kTileBytes);
-        const int jlo = p.gdiv.div(f.ks * kStageK);
-        const int jhi = p.gdiv.div(kend - 1);
-        bulk_prefetch_l2(p.meta + (static_cast<int64_t>(f.t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
+    // The whole warp runs the loop and waits together; lane 0 issues the copies.
+    const uint64_t pol_stream = policy_evict_first();
+    if (warp == 0 && lane == 0 && nst > 0) {
+      // the codes of the first stages (contiguous within a tile) and their group records
+      StageIter f;
+      f.init(p, u0);
+      const int n0 = min(nst, min(S, p.KS - f.ks));
+      const int kend = min((f.ks + n0) * kStageK, p.K);
+      const int blocks = min((f.ks + n0) * kSB, p.KB) - f.ks * kSB;
+      bulk_prefetch_l2(p.codes + (static_cast<int64_t>(f.t) * p.KB + f.ks * kSB) * kTileBytes, blocks * kTileBytes);
+      const int jlo = p.gdiv.div(f.ks * kStageK);
+      const int jhi = p.gdiv.div(kend - 1);
+      bulk_prefetch_l2(p.meta + (static_cast<int64_t>(f.t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
+    }
+    griddep_wait();
+    StageIter it;
+    it.init(p, u0 + warp);
+    int i = warp;
+    for (; i < nst; i += 2, it.advance(p, 2)) {
+      const int s = i % S;
+      if (i >= S) {  // every MMA warp is done with the stage this slot held
+        const uint32_t ph = ((i / S) - 1) & 1;
+        bool ok = true;
+        for (int e = 0; e < I && ok; ++e) ok = warp_wait(smem_u32(&mdone_bar[e][s]), ph, abort_flag, p.err);
+        if (!ok) break;
       }
-      griddep_wait();
-      StageIter it;
-      it.init(p, u0 + warp);
-      int i = warp;
-      for (; i < nst; i += 2, it.advance(p, 2)) {
-        const int s = i % S;
-        if (i >= S) {  // every MMA warp is done with the stage this slot held
-          const uint32_t ph = ((i / S) - 1) & 1;
-          bool ok = true;
-          for (int e = 0; e < I && ok; ++e) ok = mbar_wait(smem_u32(&mdone_bar[e][s]), ph, abort_flag, p.err);
-          if (!ok) break;
-        }
+      if (lane == 0) {
         const int nb = stage_blocks(p, it.ks);
         const int k0 = it.ks * kStageK;
         const int jlo = p.gdiv.div(k0);
@@ -401,44 +407,46 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
         bulk_g2s(stage + C::kXBytes + C::kCodeBytes, p.meta + (static_cast<int64_t>(it.t) * p.G + jlo) * kRecBytes,
                  nrec * kRecBytes, bar, pol_stream);
       }
-      if (*abort_flag) {
-        // let every copy this warp issued land before the CTA's shared memory goes away
-        for (int j = i - 2; j >= 0 && j >= i - S; j -= 2) drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1);
-      }
+      __syncwarp();
+    }
+    if (*abort_flag && lane == 0) {
+      // let every copy this warp issued land before the CTA's shared memory goes away
+      for (int j = i - 2; j >= 0 && j >= i - S; j -= 2) drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1);
     }
   } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      const int e = warp - C::kIssuerWarp0;  // blocks e * BPI .. e * BPI + BPI - 1 of every stage
-      constexpr uint32_t idesc = idesc_f16_f32(128, BN);
-      StageIter it;
-      it.init(p, u0);
-      int seg = 0;          // segment (tile) index within the CTA's range
-      int seg_tile = it.tile;
-      int seg_freed = 0;    // segments below this one are known to be read out by the epilogue
-      bool started = false; // this warp issued an MMA into the current segment's accumulator
-      bool ok = true;
-      for (int i = 0; i < nst; ++i, it.advance(p, 1)) {
-        if (it.tile != seg_tile) {
-          mma_commit(smem_u32(&dfull_bar[seg % C::kDBufs]));
-          ++seg;
-          seg_tile = it.tile;
-          started = false;
-        }
-        const int nb = stage_blocks(p, it.ks);
-        if (BPI * e < nb && !started) {
-          // before the first MMA into a reused accumulator set, the epilogue must have read it out:
-          // wait for every earlier segment's release in order, so no parity wait skips a phase
-          for (; ok && seg_freed <= seg - C::kDBufs; ++seg_freed)
-            ok = mbar_wait(smem_u32(&dempty_bar[seg_freed % C::kDBufs]), (seg_freed / C::kDBufs) & 1, abort_flag,
-                           p.err);
-        }
-        const uint32_t dcol = tmem + ((seg % C::kDBufs) * I + e) * C::kDStride;
-        // the dequant groups stored their A operands; they saw the stage land before that, which
-        // orders the x tile's arrival before these MMAs
-        if (ok) ok = mbar_wait(smem_u32(&afull_bar[e][i % C::kASlots]), (i / C::kASlots) & 1, abort_flag, p.err);
-        if (!ok) break;
-        tc_fence_after();
+    // The whole warp runs the loop and waits together; lane 0 issues the MMAs and commits.
+    const int e = warp - C::kIssuerWarp0;  // blocks e * BPI .. e * BPI + BPI - 1 of every stage
+    constexpr uint32_t idesc = idesc_f16_f32(128, BN);
+    StageIter it;
+    it.init(p, u0);
+    int seg = 0;          // segment (tile) index within the CTA's range
+    int seg_tile = it.tile;
+    int seg_freed = 0;    // segments below this one are known to be read out by the epilogue
+    bool started = false; // this warp issued an MMA into the current segment's accumulator
+    bool ok = true;
+    for (int i = 0; i < nst; ++i, it.advance(p, 1)) {
+      if (it.tile != seg_tile) {
+        if (lane == 0) mma_commit(smem_u32(&dfull_bar[seg % C::kDBufs]));
+        ++seg;
+        seg_tile = it.tile;
+        started = false;
+      }
+      const int nb = stage_blocks(p, it.ks);
+      if (BPI * e < nb && !started) {
+        // before the first MMA into a reused accumulator set, the epilogue must have read it out:
+        // wait for every earlier segment's release in order, so no parity wait skips a phase
+        for (; ok && seg_freed <= seg - C::kDBufs; ++seg_freed)
+          ok = warp_wait(smem_u32(&dempty_bar[seg_freed % C::kDBufs]), (seg_freed / C::kDBufs) & 1, abort_flag,
+                         p.err);
+      }
+      const uint32_t dcol = tmem + ((seg % C::kDBufs) * I + e) * C::kDStride;
+      // the dequant groups stored their A operands; they saw the stage land before that, which
+      // orders the x tile's arrival before these MMAs
+      if (ok) ok = warp_wait(smem_u32(&afull_bar[e][i % C::kASlots]), (i / C::kASlots) & 1, abort_flag, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
         const uint32_t xs = smem_base + (i % S) * C::kStageBytes;
 #pragma unroll
         for (int bb = 0; bb < BPI; ++bb) {
@@ -449,13 +457,16 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kTK / 16; ++kk) {
             // A: 128 x 16 fp16 in tensor memory (8 columns per 16 K); B: 16 K-columns of the x block
-            const bool fresh = kk == 0 && !started;
+            const bool fresh = kk == 0 && bb == 0 && !started;
             mma_f16_ts(dcol, acol + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), idesc, fresh ? 0u : 1u);
           }
-          started = true;
         }
         mma_commit(smem_u32(&mdone_bar[e][i % S]));
       }
+      if (BPI * e < nb) started = true;
+      __syncwarp();
+    }
+    if (lane == 0) {
       if (ok && nst > 0) mma_commit(smem_u32(&dfull_bar[seg % C::kDBufs]));
       if (*abort_flag) {
         mma_commit(smem_u32(&drain_bar[e]));
@@ -465,8 +476,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
   } else if (warp < C::kEpiWarp0) {
     // ------------------------------------------------------------ dequant
     // Group d takes K block d of every stage: thread r turns weight row r's 64 codes into the
-    // A slot (d, i % 2), then its warp counts itself in on MMA warp d / BPI's afull barrier. A group
-    // with no block in a (short) stage still takes part in every wait and arrival.
+    // A slot (d, i % kASlots), then its warp counts itself in on MMA warp d / BPI's afull barrier. A
+    // group with no block in a (short) stage still takes part in every wait and arrival.
     const int d = (warp - C::kDqWarp0) / 4;
     const int e = d / BPI;
     const int lq = warp % 4;  // tensor-memory lane quarter this warp may access
@@ -478,7 +489,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
       const int s = i % S;
       if (!warp_wait(smem_u32(&full_bar[s]), (i / S) & 1, abort_flag, p.err)) break;
       const bool have = d < stage_blocks(p, it.ks);
-      // the A slot's previous stage (i - 2) must have gone through its MMAs
+      // the A slot's previous stage (i - kASlots) must have gone through its MMAs
       if (i >= C::kASlots &&
           !warp_wait(smem_u32(&mdone_bar[e][(i - C::kASlots) % S]), ((i - C::kASlots) / S) & 1, abort_flag, p.err))
         break;
@@ -520,8 +531,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
             tmem_st_32x32b_x16(acol + 16 * h, out);
           }
         }
+        tmem_wait_st();
       }
-      if (have) tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&afull_bar[e][i % C::kASlots]));
