@@ -140,7 +140,8 @@ W4_API int w4a16_gemm(const void *x_dev, const void *packed_dev, int64_t M, int6
 
 /*
  * As w4a16_gemm with the schedule forced. block_n: activation rows per output
- * tile (16, 32, 64 or 128; 0 = automatic). ctas: number of persistent
+ * tile (8, 16, 32, 64 or 128; 0 = automatic); 8 runs the decode kernel
+ * (register-operand MMAs), 16..128 the tensor-memory kernel. ctas: number of persistent
  * CTAs (1..65535; 0 = one per SM). schedule: 0 = automatic, 1 = stream-K
  * (CTAs may cut a tile along K; the cut tiles are finished by a fixup through
  * the workspace), 2 = whole tiles per CTA. The workspace must be at least

@@ -63,7 +63,8 @@ def test_workspace_sizes(lib):
     b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 16, P, 1)
     assert b == 256 + 256 + P * 2 * 128 * 16 * 4
     assert w4.w4a16_workspace_bytes(0, 1, 8, 8) == 0
-    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 0, 0) == 0  # block_n must be 16..128, a power of two
+    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 0, 0) == 0  # block_n must be 8..128, a power of two
+    assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 8, 0, 0) > 0
     assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 256, 0, 0) == 0
     assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 16, 0, 3) == 0  # no schedule 3
 

@@ -79,7 +79,7 @@ def test_tile_edges(M):
     check(M, 300, 520, 128)
 
 
-@pytest.mark.parametrize("block_n", [16, 32, 64, 128])
+@pytest.mark.parametrize("block_n", [8, 16, 32, 64, 128])
 @pytest.mark.parametrize("ctas,schedule", [(1, 1), (2, 1), (3, 1), (7, 1), (13, 1), (64, 1), (1, 2), (5, 2)])
 def test_forced_schedules(block_n, ctas, schedule):
     # 3 n-tiles x 8 K stages (x m-tiles): stream-K cuts tiles at many places, incl. one CTA holding
@@ -89,10 +89,12 @@ def test_forced_schedules(block_n, ctas, schedule):
 
 @pytest.mark.parametrize("g", [8, 16, 24, 32, 40, 64, 96, 128, 192, 256, 384, 512, 1024])
 def test_group_sizes(g):
-    # g % 128 == 0 applies the scale outside the MMA (block_n <= 32); g % 64 == 0 inside with one
-    # group per 64-wide block (block_n >= 64); any other g looks the group up per 8 codes.
+    # g % 64 == 0 puts one group in each 64-wide K block: the decode kernel (block_n 8) then scales
+    # the block's fp32 partial sums, the tensor-memory kernel (16..128) scales in the dequant; any
+    # other g looks the group up per 8 codes in both.
     # K = 1000 leaves a partial last group and a last stage of 4 blocks whose last block is ragged.
     check(9, 200, 1000, g)
+    check(5, 200, 1000, g, block_n=8, ctas=3, schedule=1)
     check(9, 200, 1000, g, block_n=16, ctas=3, schedule=1)
     check(30, 200, 1000, g, block_n=32, ctas=5, schedule=1)
     check(70, 200, 1000, g, block_n=64, ctas=4, schedule=1)
@@ -100,11 +102,11 @@ def test_group_sizes(g):
 
 
 @pytest.mark.parametrize("K,g", [(288, 256), (320, 64), (320, 128), (448, 128), (576, 192), (4000, 128), (200, 8)])
-@pytest.mark.parametrize("block_n", [16, 32, 64, 128])
+@pytest.mark.parametrize("block_n", [8, 16, 32, 64, 128])
 def test_short_last_stage(K, g, block_n):
     # A stage is four 64-wide K blocks; these K leave a last stage of 1..3 blocks (K % 64 != 0 also
     # switches x to one tensor copy per block). Forced small grids start CTA ranges on that stage.
-    M = {16: 13, 32: 29, 64: 50, 128: 90}[block_n]
+    M = {8: 7, 16: 13, 32: 29, 64: 50, 128: 90}[block_n]
     check(M, 264, K, g, block_n=block_n)
     for ctas in (2, 3, 5):
         check(M, 264, K, g, block_n=block_n, ctas=ctas, schedule=1)
@@ -119,7 +121,8 @@ def test_one_hot_rows_return_rounded_weights_exactly():
         x[i, k] = 1.0
     wd = oracle.dequant(qw, s, zw, N, K, g)
     expect = wd[:, ks].T.astype(np.float16)  # (q - z) * s is exact in fp64; one rounding to fp16
-    for bn, ctas, sch in [(0, 0, 0), (16, 1, 2), (16, 4, 1), (128, 1, 1), (64, 5, 1), (16, 11, 1), (32, 3, 1)]:
+    for bn, ctas, sch in [(0, 0, 0), (16, 1, 2), (16, 4, 1), (128, 1, 1), (64, 5, 1), (16, 11, 1), (32, 3, 1),
+                          (8, 3, 1), (8, 1, 2)]:
         y = run_gemm(x, packed, N, K, g, bn, ctas, sch)
         assert (y.view(np.uint16) == expect.view(np.uint16)).all(), (bn, ctas, sch)
 
@@ -213,7 +216,8 @@ def test_prefill_layers_sampled(L):
     (10240, 8192, 256, 128, 80, 2), (10240, 8192, 256, 128, 0, 1), (10240, 8192, 256, 64, 0, 1),
     (10240, 8192, 256, 32, 0, 1), (10240, 8192, 256, 16, 0, 1),
     # 172 tiles over 152 CTAs: many CTAs hold a short head or tail segment that some dequant groups skip
-    (22016, 4096, 64, 64, 0, 1), (22016, 4096, 128, 128, 0, 1), (22016, 4096, 16, 16, 0, 1)])
+    (22016, 4096, 64, 64, 0, 1), (22016, 4096, 128, 128, 0, 1), (22016, 4096, 16, 16, 0, 1),
+    (22016, 4096, 8, 8, 0, 1), (4096, 4096, 3, 8, 0, 1)])
 def test_repeated_launches_bit_identical(N, K, M, block_n, ctas, schedule):
     # The schedule is deterministic, so back-to-back launches must agree bit for bit; a pipeline
     # hazard (a stage, slot or accumulator used before it was ready) shows up as a differing launch.

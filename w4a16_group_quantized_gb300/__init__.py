@@ -198,8 +198,9 @@ def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: int, y:
 
 def w4a16_gemm_ex(x, packed, N, K, g, block_n: int = 0, ctas: int = 0, schedule: int = 0, y=None, workspace=None,
                   stream=None):
-    """w4a16_gemm with the schedule forced: block_n in {16,32,64,128}, ctas >= 1, schedule 1 stream-K or
-    2 whole tiles (0 = automatic for each)."""
+    """w4a16_gemm with the schedule forced: block_n in {8,16,32,64,128} (8: the register-operand decode
+    kernel; 16..128: the tensor-memory kernel), ctas >= 1, schedule 1 stream-K or 2 whole tiles (0 = automatic
+    for each)."""
     return _gemm_common(x, packed, N, K, g, y, workspace, block_n, ctas, schedule, stream)
 
 

@@ -43,17 +43,16 @@
 
 #include <mutex>
 
+#include "gemm_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace w4 {
 namespace {
 
-enum Mode { kScaleIn = 1, kGeneral = 2 };  // g % 64 == 0 (one group per K block) or any g
+using namespace detail;
 
-constexpr int kSB = 4;           // 64-wide K blocks per stage
-constexpr int kStageK = kSB * kTK;
-constexpr int kMaxPieces = 8;    // CTAs that may share one output tile (the planner guarantees it)
+enum Mode { kScaleIn = 1, kGeneral = 2 };  // g % 64 == 0 (one group per K block) or any g
 
 template <int BN, int MODE>
 struct Cfg {
@@ -92,150 +91,6 @@ struct Cfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
 };
 
-// Division by the group size g without a divide instruction: Granlund and Montgomery, "Division by
-// invariant integers using multiplication" (PLDI 1994), the round-up method with a 33-bit multiplier
-// split as 2^32 + m: q = (t + ((n - t) >> s1)) >> s2 with t = umulhi(m, n), exact for all n < 2^32.
-struct FastDiv {
-  uint32_t m, s1, s2;
-  __device__ __forceinline__ int div(int n) const {
-    const uint32_t un = static_cast<uint32_t>(n);
-    const uint32_t t = __umulhi(m, un);
-    return static_cast<int>((t + ((un - t) >> s1)) >> s2);
-  }
-};
-
-inline FastDiv make_fastdiv(uint32_t d) {
-  uint32_t l = 0;
-  while ((uint64_t{1} << l) < d) ++l;  // l = ceil(log2 d)
-  FastDiv f;
-  f.m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1);
-  f.s1 = l < 1 ? l : 1;
-  f.s2 = l < 1 ? 0 : l - 1;
-  return f;
-}
-
-// Work decomposition. A unit is one 256-wide K stage of one output tile (128 weight rows x BN
-// activation rows); units are numbered tile-major: u = tile * KS + ks, tile = t * MT + mt.
-// CTA c owns the contiguous units [begin(c), begin(c+1)), cut at multiples of `gran` units
-// (gran = 1: stream-K, any cut; gran = KS: whole tiles only).
-struct Params {
-  const uint8_t *codes;  // tile region of the packed weights
-  const uint8_t *meta;   // group-record region of the packed weights
-  __half *y;
-  float *pieces;         // [P][2][BN][128] fp32 partial tiles (first and last segment of each CTA)
-  uint32_t *counters;    // [tiles] arrivals per split tile
-  uint32_t *err;
-  int M, N, K, g, G, NT, KB, KS, MT;
-  int P;                 // CTAs
-  int gran;              // units per scheduling grain
-  int x3d;               // x tensor map is [KB][M][64] (one copy per stage); else [M][K] (one per block)
-  FastDiv gdiv;          // division by g
-  int64_t grains;        // total units / gran
-};
-
-__device__ __forceinline__ int64_t range_begin(const Params &p, int c) {
-  return static_cast<int64_t>(c) * p.grains / p.P * p.gran;
-}
-
-// The CTA whose range holds unit u: the largest c with range_begin(c) <= u.
-__device__ __forceinline__ int owner_of(const Params &p, int64_t u) {
-  const int64_t v = u / p.gran;
-  return static_cast<int>(((v + 1) * p.P - 1) / p.grains);
-}
-
-// K blocks in stage ks of a tile: 4, except a shorter last stage when KB is not a multiple of 4.
-__device__ __forceinline__ int stage_blocks(const Params &p, int ks) {
-  return ks == p.KS - 1 ? p.KB - kSB * (p.KS - 1) : kSB;
-}
-
-// Walks (tile, ks, t, mt) over a CTA's units without divisions.
-struct StageIter {
-  int tile, ks, t, mt;
-  __device__ __forceinline__ void init(const Params &p, int64_t u) {
-    tile = static_cast<int>(u / p.KS);
-    ks = static_cast<int>(u % p.KS);
-    t = tile / p.MT;
-    mt = tile % p.MT;
-  }
-  __device__ __forceinline__ void advance(const Params &p, int step) {
-    ks += step;
-    while (ks >= p.KS) {
-      ks -= p.KS;
-      ++tile;
-      if (++mt == p.MT) {
-        mt = 0;
-        ++t;
-      }
-    }
-  }
-};
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-
-// Per-(row, group) dequant constants as fp16x2 pairs.
-struct GroupConsts {
-  uint32_t s2;    // (s, s)
-  uint32_t zb2;   // (1024 + z, 1024 + z)
-  uint32_t nz2;   // (-(64 + z), -(64 + z))
-};
-
-__device__ __forceinline__ GroupConsts group_consts(uint32_t sbits, uint32_t z) {
-  GroupConsts c;
-  c.s2 = sbits * 0x00010001u;
-  c.zb2 = (0x6400u + z) * 0x00010001u;          // fp16 1024 + z: exponent of 1024, z in the fraction
-  c.nz2 = (0xD400u + 16u * z) * 0x00010001u;    // fp16 -(64 + z): step of 1/16 at 64
-  return c;
-}
-
-// 8 codes (tile nibble order) -> 4 registers of fp16 pairs (k, k+1) holding q - z exactly.
-// 0x6400 | q is the fp16 1024 + q and 0x6400 | (q << 4) is 1024 + 16 q, both exact; subtracting
-// 1024 + z (or scaling by 1/16 and adding -(64 + z)) leaves the small integer q - z, exact.
-__device__ __forceinline__ void dequant_word_int(uint32_t w, const GroupConsts &c, uint32_t *o) {
-  constexpr uint32_t kInv16x2 = 0x2C002C00u;  // (1/16, 1/16)
-  const uint32_t w8 = w >> 8;
-  o[0] = hsub2_rn(lop3_and_or(w, 0x000F000Fu, 0x64006400u), c.zb2);
-  o[1] = hfma2_rn(lop3_and_or(w, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
-  o[2] = hsub2_rn(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), c.zb2);
-  o[3] = hfma2_rn(lop3_and_or(w8, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
-}
-
-// As dequant_word_int, then one multiply by s: each weight (q - z) * s rounded once to fp16.
-__device__ __forceinline__ void dequant_word(uint32_t w, const GroupConsts &c, uint32_t *o) {
-  dequant_word_int(w, c, o);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = hmul2_rn(o[i], c.s2);
-}
-
-// A wait whose outcome is the same for all 32 lanes: the warp then either executes the
-// following .sync.aligned tcgen05 instructions together or leaves the loop together.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          uint32_t *err) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Waits ignoring the abort flag (used only to drain in-flight copies/MMAs before exit).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = clock_cycles();
-  while (!mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
-    if (clock_cycles() - t0 > kWaitLimitCycles) return;
-  }
-}
-
 // Writes 16 consecutive columns (activation rows m0 + c0 ..) of weight row n of a finished tile
 // segment: to y (fp16, rounded once) for a whole tile, else to the CTA's fp32 piece, which is laid
 // out column by column ([BN][128]) so that a warp's 32 rows make one 128-byte line per column.
@@ -252,39 +107,6 @@ __device__ __forceinline__ void emit16(const Params &p, bool whole, int n, int m
 #pragma unroll
     for (int e = 0; e < 16; ++e) __stcg(piece + (c0 + e) * kTN, v[e]);
   }
-}
-
-// The fixup of a cut tile, done by the last CTA to finish a piece of it.
-struct Fixup {
-  int tile;     // -1: nothing to do
-  int c_first;  // CTA holding the tile's first K stages (piece 0)
-  int npieces;
-  int slot0;    // piece 0 is that CTA's second slot (its range began in an earlier tile)
-};
-
-// y = the pieces added in K order (piece q >= 1 is CTA c_first + q's first slot). nthreads threads
-// from tid = 0 share the work, element by element in the pieces' column-major order, so stores and
-// loads are coalesced and every thread has several independent loads in flight.
-template <int BN>
-__device__ __forceinline__ void reduce_pieces(const Params &p, const Fixup &f, int tid, int nthreads) {
-  const float *src[kMaxPieces];
-#pragma unroll
-  for (int q = 0; q < kMaxPieces; ++q)
-    src[q] = p.pieces + (static_cast<int64_t>(f.c_first + (q < f.npieces ? q : 0)) * 2 + (q == 0 ? f.slot0 : 0)) *
-                            BN * kTN;
-  const int n0 = (f.tile / p.MT) * kTN;
-  const int m0 = (f.tile % p.MT) * BN;
-  const int ncols = min(p.M, m0 + BN) - m0;
-#pragma unroll 4
-  for (int e = tid; e < ncols * kTN; e += nthreads) {
-    float acc = __ldcg(src[0] + e);
-#pragma unroll
-    for (int q = 1; q < kMaxPieces; ++q)
-      if (q < f.npieces) acc += __ldcg(src[q] + e);
-    const int n = n0 + e % kTN;
-    if (n < p.N) p.y[static_cast<int64_t>(m0 + e / kTN) * p.N + n] = __float2half_rn(acc);
-  }
-  if (tid == 0) p.counters[f.tile] = 0u;  // ready for the next call
 }
 
 template <int BN, int MODE>
@@ -360,59 +182,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
 
   if (warp < C::kIssuerWarp0) {
     // ------------------------------------------------------------ producers
-    // The whole warp runs the loop and waits together; lane 0 issues the copies.
-    const uint64_t pol_stream = policy_evict_first();
-    if (warp == 0 && lane == 0 && nst > 0) {
-      // the codes of the first stages (contiguous within a tile) and their group records
-      StageIter f;
-      f.init(p, u0);
-      const int n0 = min(nst, min(S, p.KS - f.ks));
-      const int kend = min((f.ks + n0) * kStageK, p.K);
-      const int blocks = min((f.ks + n0) * kSB, p.KB) - f.ks * kSB;
-      bulk_prefetch_l2(p.codes + (static_cast<int64_t>(f.t) * p.KB + f.ks * kSB) * kTileBytes, blocks * kTileBytes);
-      const int jlo = p.gdiv.div(f.ks * kStageK);
-      const int jhi = p.gdiv.div(kend - 1);
-      bulk_prefetch_l2(p.meta + (static_cast<int64_t>(f.t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
-    }
-    griddep_wait();
-    StageIter it;
-    it.init(p, u0 + warp);
-    int i = warp;
-    for (; i < nst; i += 2, it.advance(p, 2)) {
-      const int s = i % S;
-      if (i >= S) {  // every MMA warp is done with the stage this slot held
-        const uint32_t ph = ((i / S) - 1) & 1;
-        bool ok = true;
-        for (int e = 0; e < I && ok; ++e) ok = warp_wait(smem_u32(&mdone_bar[e][s]), ph, abort_flag, p.err);
-        if (!ok) break;
-      }
-      if (lane == 0) {
-        const int nb = stage_blocks(p, it.ks);
-        const int k0 = it.ks * kStageK;
-        const int jlo = p.gdiv.div(k0);
-        const int jhi = p.gdiv.div(min(k0 + nb * kTK, p.K) - 1);
-        const int nrec = jhi - jlo + 1;
-        const uint32_t stage = smem_base + s * C::kStageBytes;
-        const uint32_t bar = smem_u32(&full_bar[s]);
-        // the 3-D box always lands whole (zero fill past the last K block); the 2-D boxes per block
-        const uint32_t xbytes = p.x3d ? C::kXBytes : nb * C::kXSub;
-        mbar_arrive_expect_tx(bar, xbytes + nb * kTileBytes + nrec * kRecBytes);
-        if (p.x3d) {
-          tma_load_3d(stage, &x_map, 0, it.mt * BN, it.ks * kSB, bar);
-        } else {
-          for (int b = 0; b < nb; ++b) tma_load_2d(stage + b * C::kXSub, &x_map, k0 + b * kTK, it.mt * BN, bar);
-        }
-        bulk_g2s(stage + C::kXBytes, p.codes + (static_cast<int64_t>(it.t) * p.KB + it.ks * kSB) * kTileBytes,
-                 nb * kTileBytes, bar, pol_stream);
-        bulk_g2s(stage + C::kXBytes + C::kCodeBytes, p.meta + (static_cast<int64_t>(it.t) * p.G + jlo) * kRecBytes,
-                 nrec * kRecBytes, bar, pol_stream);
-      }
-      __syncwarp();
-    }
-    if (*abort_flag && lane == 0) {
-      // let every copy this warp issued land before the CTA's shared memory goes away
-      for (int j = i - 2; j >= 0 && j >= i - S; j -= 2) drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1);
-    }
+    produce_stages<BN, S, C::kStageBytes>(&x_map, p, u0, nst, warp, lane, smem_base, full_bar, &mdone_bar[0][0], S,
+                                          I, abort_flag);
   } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------ MMA issue
     // The whole warp runs the loop and waits together; lane 0 issues the MMAs and commits.
@@ -587,19 +358,18 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[db]));
       if (!whole) {
         // the last CTA to finish a piece of this tile adds all pieces in K order and writes y. The
-        // warpgroup's piece stores are ordered before one thread's release (fence, then the count);
-        // the thread that sees the last count acquires (fence) before the pieces are read.
+        // warpgroup's piece stores are ordered (barrier) before one thread's count, an acquire-release
+        // atomic; the thread that sees the last count has acquired the other pieces, and the
+        // barrier after it orders their reads.
         __syncwarp();
         named_bar_sync(1, 128);
         if (r == 0) {
-          __threadfence();
           Fixup f;
           f.c_first = owner_of(p, tile_u0);
           f.npieces = owner_of(p, tile_u0 + p.KS - 1) - f.c_first + 1;
           f.slot0 = range_begin(p, f.c_first) != tile_u0 ? 1 : 0;
-          const uint32_t old = atomicAdd(&p.counters[tile], 1u);
+          const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile]);
           f.tile = old == static_cast<uint32_t>(f.npieces - 1) ? tile : -1;
-          if (f.tile >= 0) __threadfence();
           fix_sh = f;
           // the CTA's last segment: every dequant and epilogue warp is free after it, so they all do
           // this fixup together below
@@ -701,29 +471,11 @@ cudaError_t launch_t(const CUtensorMap &map, const Params &p, int ctas, cudaStre
       if (dev < 64) done_mask |= 1ull << dev;
     }
   }
-  // programmatic stream serialization: the launch may overlap the previous kernel's tail (the kernel
-  // waits for it with griddepcontrol.wait before touching global memory)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, map, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_programmatic(kern, map, p, ctas, C::kThreads, C::kSmemBytes, stream);
 }
 
-// Scale outside needs each 128-wide half-stage inside one quantization group (g % 128 == 0) and
-// BN <= 32; scale inside needs each 64-wide block inside one group (g % 64 == 0).
-int gemm_mode(int bn, int32_t g) {
-  (void)bn;
-  return g % 64 == 0 ? kScaleIn : kGeneral;
-}
+// One group per 64-wide K block (g % 64 == 0) lets the dequant take the block's group once.
+int gemm_mode(int32_t g) { return g % 64 == 0 ? kScaleIn : kGeneral; }
 
 cudaError_t launch_variant(int bn, int mode, const CUtensorMap &map, const Params &p, int ctas,
                            cudaStream_t stream) {
@@ -747,8 +499,8 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
                     int num_sms, GemmPlan *plan) {
   (void)g;
   int bn = block_n;
-  if (bn == 0) bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-  if (bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
+  if (bn == 0) bn = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  if (bn != 8 && bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
   const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK), ks = cdiv(kb, kSB);
   const int64_t tiles = mt * nt;
@@ -823,7 +575,8 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.gran = plan.gran;
   p.x3d = x3d ? 1 : 0;
   p.grains = plan.grains;
-  return launch_variant(plan.block_n, gemm_mode(plan.block_n, g), map, p, plan.ctas, stream);
+  if (plan.block_n == 8) return launch_gemm_rf(map, p, 1, g % kTK != 0, plan.ctas, stream);
+  return launch_variant(plan.block_n, gemm_mode(g), map, p, plan.ctas, stream);
 }
 
 }  // namespace w4

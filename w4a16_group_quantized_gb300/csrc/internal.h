@@ -22,7 +22,7 @@ cudaError_t launch_repack(const uint32_t *qw, const void *scales, const uint32_t
                           int32_t g, void *packed, cudaStream_t stream);
 
 struct GemmPlan {
-  int block_n;   // activation rows per tile: 16, 32, 64 or 128
+  int block_n;   // activation rows per tile: 8 (decode kernel), 16, 32, 64 or 128 (tensor-memory kernel)
   int m_tiles;
   int n_tiles;
   int k_blocks;

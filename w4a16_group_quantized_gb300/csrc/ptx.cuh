@@ -106,6 +106,18 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------- inter-CTA counting
+
+// Adds 1 to a global counter with acquire-release semantics at GPU scope and returns the old
+// value. As release it publishes every store ordered before it (the CTA's own, through a preceding
+// barrier: release is cumulative); as acquire it makes the stores other CTAs published before
+// their own count visible to this thread and, through a following barrier, to its CTA.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *ctr) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------- async copies
 
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
