@@ -55,13 +55,20 @@ def test_repacked_bytes_formula(lib):
 
 
 def test_workspace_sizes(lib):
-    # whole tiles: error word block + per-tile counters only
+    # whole tiles: error word block + per-tile counters only; block_n 128 with M >= 256 schedules
+    # units of two 128-row weight tiles, so 512 x 8192 has 4 x 32 output tiles
     b = w4.w4a16_workspace_bytes_ex(512, 8192, 8192, 128, 128, 0, 2)
-    assert b == 256 + 1024  # 4 x 64 tile counters of 4 bytes
-    # stream-K with P CTAs: plus two fp32 partial tiles (128 x block_n) per CTA
+    assert b == 256 + 512  # 4 x 32 tile counters of 4 bytes
+    b = w4.w4a16_workspace_bytes_ex(512, 8192, 8192, 128, 64, 0, 2)
+    assert b == 256 + 2048  # 8 x 64 tile counters
+    # stream-K with P CTAs: plus two fp32 partial tiles (128 x block_n, two of them for block_n 128)
     M, N, K, P = 16, 300, 1024, 4
     b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 16, P, 1)
     assert b == 256 + 256 + P * 2 * 128 * 16 * 4
+    b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 128, P, 1)  # M < 256: units of one weight tile
+    assert b == 256 + 256 + P * 2 * 128 * 128 * 4
+    b = w4.w4a16_workspace_bytes_ex(256, N, K, 128, 128, P, 1)  # M >= 256: units of two weight tiles
+    assert b == 256 + 256 + P * 2 * 2 * 128 * 128 * 4
     assert w4.w4a16_workspace_bytes(0, 1, 8, 8) == 0
     assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 24, 0, 0) == 0  # block_n must be 8..128, a power of two
     assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 8, 0, 0) > 0

@@ -87,6 +87,19 @@ def test_forced_schedules(block_n, ctas, schedule):
     check(20, 260, 2048, 128, block_n=block_n, ctas=ctas, schedule=schedule)
 
 
+@pytest.mark.parametrize("M,N,K,g,ctas,schedule", [
+    (256, 260, 2048, 128, 0, 0),   # odd number of weight tiles: the last pair's second tile is past N
+    (300, 260, 960, 64, 5, 1),     # 15 K blocks: the last 128-wide stage holds one block
+    (256, 384, 1000, 40, 3, 1),    # g not a multiple of 64: groups looked up per 8 codes
+    (257, 130, 1088, 128, 7, 1),   # a 1-row last token tile, a 2-row last weight tile
+    (512, 260, 960, 128, 0, 2),    # whole tile pairs
+    (256, 1000, 4000, 128, 0, 0),  # the partial-group shape
+])
+def test_two_tile_units(M, N, K, g, ctas, schedule):
+    # block_n 128 from M = 256 up schedules units of two weight tiles on one x tile (128-wide stages)
+    check(M, N, K, g, block_n=128, ctas=ctas, schedule=schedule)
+
+
 @pytest.mark.parametrize("g", [8, 16, 24, 32, 40, 64, 96, 128, 192, 256, 384, 512, 1024])
 def test_group_sizes(g):
     # g % 64 == 0 puts one group in each 64-wide K block: the decode kernel (block_n 8) then scales

@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "gemm_common.cuh"
@@ -54,14 +55,20 @@ using namespace detail;
 
 enum Mode { kScaleIn = 1, kGeneral = 2 };  // g % 64 == 0 (one group per K block) or any g
 
-template <int BN, int MODE>
+template <int BN, int MODE, int TP>
 struct Cfg {
+  // Weight tiles per unit: TP = 2 (BN = 128 only) pairs two 128-row weight tiles on each x tile (half
+  // the x bytes per MMA flop, twice the stages in shared memory); a stage then spans 2 K blocks of
+  // both tiles.
+  static constexpr int kTP = TP;
+  static constexpr int kSBK = kSB / kTP;  // K blocks per stage; kTP * kSBK = 4 A blocks per stage
   static constexpr int kXSub = BN * 128;  // x for one K block: BN rows x 64 fp16 (1024-byte multiple)
-  static constexpr int kXBytes = kSB * kXSub;
+  static constexpr int kXBytes = kSBK * kXSub;
   static constexpr int kCodeBytes = kSB * kTileBytes;
-  // group records one stage can touch: g >= 64 -> at most 256 / 64 + 1; g >= 8 -> 256 / 8 + 1
-  static constexpr int kMaxRecs = MODE == kGeneral ? kStageK / 8 + 1 : kStageK / 64 + 1;
-  static constexpr int kStageBytes = (kXBytes + kCodeBytes + kMaxRecs * kRecBytes + 1023) / 1024 * 1024;
+  // group records one stage can touch per weight tile: g >= 64 -> at most kSBK + 1; g >= 8 -> 8 kSBK + 1
+  static constexpr int kMaxRecs = MODE == kGeneral ? kSBK * kTK / 8 + 1 : kSBK * kTK / 64 + 1;
+  static constexpr int kRecBoxBytes = kTP * kMaxRecs * kRecBytes;
+  static constexpr int kStageBytes = (kXBytes + kCodeBytes + kRecBoxBytes + 1023) / 1024 * 1024;
   static constexpr int kSmemBudget = 224 * 1024;  // one CTA per SM
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes > 8 ? 8 : kSmemBudget / kStageBytes;
   // producer warp w fills the stages i = w (mod 2): an even ring keeps each slot with one producer
@@ -89,6 +96,7 @@ struct Cfg {
   // before this wait as long as the stage ring is at least as long as the A-slot ring
   static_assert(kStages >= kASlots, "stage ring at least as long as the A-slot ring");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
+  static_assert(TP == 1 || (TP == 2 && BN == 128), "two-tile units need both accumulators of BN = 128");
 };
 
 // Writes 16 consecutive columns (activation rows m0 + c0 ..) of weight row n of a finished tile
@@ -109,10 +117,81 @@ __device__ __forceinline__ void emit16(const Params &p, bool whole, int n, int m
   }
 }
 
-template <int BN, int MODE>
-__global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
-    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const Params p) {
-  using C = Cfg<BN, MODE>;
+// The weight-stream producer for units of two weight tiles (BN = 128). A stage is [x: SBK sub-tiles
+// of BN x 64][codes: tile 0's SBK blocks, then tile 1's][records: kMaxRecs per tile from the stage's
+// first group], moved by three tensor copies: x as for one tile, the codes of both tiles as one box
+// of the [NT][16 KB][256 B] view of the tile region, their records as one box of the [NT][G][320 B]
+// view of the record region. A second tile past N, blocks past K and records past G are filled with
+// zeros by the copy (zero codes under a zero scale: A = 0). Otherwise as produce_stages.
+template <int BN, int S, int kStageBytes, int SBK, int kMaxRecs>
+__device__ __forceinline__ void produce_stages_pair(const CUtensorMap *x_map, const CUtensorMap *code_map,
+                                                    const CUtensorMap *rec_map, const Params &p, int64_t u0, int nst,
+                                                    int pw, int lane, uint32_t smem_base, uint64_t *full_bar,
+                                                    uint64_t *rel, int rel_stride, int nrel,
+                                                    volatile uint32_t *abort_flag) {
+  constexpr int kXSub = BN * 128;
+  constexpr int kXBytes = SBK * kXSub;
+  constexpr int kCodeBytes = 2 * SBK * kTileBytes;
+  constexpr int kRecBox = 2 * kMaxRecs * kRecBytes;
+  constexpr int kRowsPerBlock = kTileBytes / 256;  // 256-byte rows of the code view
+  const uint64_t pol_stream = policy_evict_first();
+  if (pw == 0 && lane == 0 && nst > 0) {
+    StageIter f;
+    f.init(p, u0);
+    const int n0 = min(nst, min(S, p.KS - f.ks));  // first stages, contiguous within the first unit
+    const int blocks = min((f.ks + n0) * SBK, p.KB) - f.ks * SBK;
+    const int kend = min((f.ks + n0) * SBK * kTK, p.K);
+    const int jlo = p.gdiv.div(f.ks * SBK * kTK);
+    const int jhi = p.gdiv.div(kend - 1);
+    for (int te = 0; te < 2; ++te) {
+      const int t = 2 * f.t + te;
+      if (t < p.NT) {
+        bulk_prefetch_l2(p.codes + (static_cast<int64_t>(t) * p.KB + f.ks * SBK) * kTileBytes, blocks * kTileBytes);
+        bulk_prefetch_l2(p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
+      }
+    }
+  }
+  griddep_wait();
+  StageIter it;
+  it.init(p, u0 + pw);
+  int i = pw;
+  for (; i < nst; i += 2, it.advance(p, 2)) {
+    const int s = i % S;
+    if (i >= S) {  // the consumers are done with the stage this slot held
+      const uint32_t ph = ((i / S) - 1) & 1;
+      bool ok = true;
+      for (int e = 0; e < nrel && ok; ++e) ok = warp_wait(smem_u32(&rel[e * rel_stride + s]), ph, abort_flag, p.err);
+      if (!ok) break;
+    }
+    if (lane == 0) {
+      const int nb = stage_blocks<SBK>(p, it.ks);
+      const int jlo = p.gdiv.div(it.ks * SBK * kTK);
+      const uint32_t stage = smem_base + s * kStageBytes;
+      const uint32_t bar = smem_u32(&full_bar[s]);
+      // the 3-D boxes always land whole (zero fill outside); the 2-D x boxes per block
+      const uint32_t xbytes = p.x3d ? kXBytes : nb * kXSub;
+      mbar_arrive_expect_tx(bar, xbytes + kCodeBytes + kRecBox);
+      if (p.x3d) {
+        tma_load_3d(stage, x_map, 0, it.mt * BN, it.ks * SBK, bar);
+      } else {
+        for (int b = 0; b < nb; ++b) tma_load_2d(stage + b * kXSub, x_map, (it.ks * SBK + b) * kTK, it.mt * BN, bar);
+      }
+      tma_load_3d_hint(stage + kXBytes, code_map, 0, it.ks * SBK * kRowsPerBlock, 2 * it.t, bar, pol_stream);
+      tma_load_3d_hint(stage + kXBytes + kCodeBytes, rec_map, 0, jlo, 2 * it.t, bar, pol_stream);
+    }
+    __syncwarp();
+  }
+  if (*abort_flag && lane == 0) {
+    // let every copy this warp issued land before the CTA's shared memory goes away
+    for (int j = i - 2; j >= 0 && j >= i - S; j -= 2) drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1);
+  }
+}
+
+template <int BN, int MODE, int TP>
+__global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap code_map,
+                      const __grid_constant__ CUtensorMap rec_map, const Params p) {
+  using C = Cfg<BN, MODE, TP>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   // Per-stage barriers (ring index = local stage index i mod the ring size; every waiter waits on
@@ -166,7 +245,13 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
     tmem_alloc(smem_u32(&tmem_base_sh), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) prefetch_tensormap(&x_map);
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&x_map);
+    if (C::kTP == 2) {
+      prefetch_tensormap(&code_map);
+      prefetch_tensormap(&rec_map);
+    }
+  }
   tc_fence_before();
   __syncwarp();
   cta_sync_all();
@@ -182,12 +267,20 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
 
   if (warp < C::kIssuerWarp0) {
     // ------------------------------------------------------------ producers
-    produce_stages<BN, S, C::kStageBytes>(&x_map, p, u0, nst, warp, lane, smem_base, full_bar, &mdone_bar[0][0], S,
-                                          I, abort_flag);
+    if (C::kTP == 2)
+      produce_stages_pair<BN, S, C::kStageBytes, C::kSBK, C::kMaxRecs>(&x_map, &code_map, &rec_map, p, u0, nst, warp,
+                                                                       lane, smem_base, full_bar, &mdone_bar[0][0], S,
+                                                                       I, abort_flag);
+    else
+      produce_stages<BN, S, C::kStageBytes>(&x_map, p, u0, nst, warp, lane, smem_base, full_bar, &mdone_bar[0][0], S,
+                                            I, abort_flag);
   } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------ MMA issue
     // The whole warp runs the loop and waits together; lane 0 issues the MMAs and commits.
-    const int e = warp - C::kIssuerWarp0;  // blocks e * BPI .. e * BPI + BPI - 1 of every stage
+    // blocks (A slots of dequant groups) e * BPI .. e * BPI + BPI - 1 of every stage: K blocks of the
+    // stage's one tile, or (kTP = 2) all K blocks of the stage's weight tile e
+    const int e = warp - C::kIssuerWarp0;
+    const int b0 = C::kTP == 2 ? 0 : BPI * e;  // this warp's first K block (x sub-tile) in a stage
     constexpr uint32_t idesc = idesc_f16_f32(128, BN);
     StageIter it;
     it.init(p, u0);
@@ -203,8 +296,9 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
         seg_tile = it.tile;
         started = false;
       }
-      const int nb = stage_blocks(p, it.ks);
-      if (BPI * e < nb && !started) {
+      const int nb = stage_blocks<C::kSBK>(p, it.ks);
+      const bool has = b0 < nb;
+      if (has && !started) {
         // before the first MMA into a reused accumulator set, the epilogue must have read it out:
         // wait for every earlier segment's release in order, so no parity wait skips a phase
         for (; ok && seg_freed <= seg - C::kDBufs; ++seg_freed)
@@ -221,10 +315,10 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
         const uint32_t xs = smem_base + (i % S) * C::kStageBytes;
 #pragma unroll
         for (int bb = 0; bb < BPI; ++bb) {
-          const int b = BPI * e + bb;
+          const int b = b0 + bb;
           if (b >= nb) break;
           const uint64_t bdesc = sw128_kmajor_desc(xs + b * C::kXSub);
-          const uint32_t acol = tmem + C::kACol0 + (b * C::kASlots + i % C::kASlots) * 32;
+          const uint32_t acol = tmem + C::kACol0 + ((BPI * e + bb) * C::kASlots + i % C::kASlots) * 32;
 #pragma unroll
           for (int kk = 0; kk < kTK / 16; ++kk) {
             // A: 128 x 16 fp16 in tensor memory (8 columns per 16 K); B: 16 K-columns of the x block
@@ -234,7 +328,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
         }
         mma_commit(smem_u32(&mdone_bar[e][i % S]));
       }
-      if (BPI * e < nb) started = true;
+      if (has) started = true;
       __syncwarp();
     }
     if (lane == 0) {
@@ -251,6 +345,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
     // group with no block in a (short) stage still takes part in every wait and arrival.
     const int d = (warp - C::kDqWarp0) / 4;
     const int e = d / BPI;
+    const int te = C::kTP == 2 ? d / C::kSBK : 0;  // weight tile of the unit
+    const int b = C::kTP == 2 ? d % C::kSBK : d;   // K block of the stage
     const int lq = warp % 4;  // tensor-memory lane quarter this warp may access
     const int r = lq * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
@@ -259,7 +355,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
     for (int i = 0; i < nst; ++i, it.advance(p, 1)) {
       const int s = i % S;
       if (!warp_wait(smem_u32(&full_bar[s]), (i / S) & 1, abort_flag, p.err)) break;
-      const bool have = d < stage_blocks(p, it.ks);
+      const bool have = b < stage_blocks<C::kSBK>(p, it.ks);
       // the A slot's previous stage (i - kASlots) must have gone through its MMAs
       if (i >= C::kASlots &&
           !warp_wait(smem_u32(&mdone_bar[e][(i - C::kASlots) % S]), ((i - C::kASlots) / S) & 1, abort_flag, p.err))
@@ -267,12 +363,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
       if (have) {
         const uint32_t stage = smem_base + s * C::kStageBytes;
         const uint32_t codes = stage + C::kXBytes + d * kTileBytes;
-        const uint32_t recs = stage + C::kXBytes + C::kCodeBytes;
+        const uint32_t recs = stage + C::kXBytes + C::kCodeBytes + te * C::kMaxRecs * kRecBytes;
         const uint4 w0 = lds128(codes + r * 16);
         const uint4 w1 = lds128(codes + 2048 + r * 16);
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const int kfirst = (it.ks * kSB + d) * kTK;
-        const int jlo = p.gdiv.div(it.ks * kStageK);
+        const int kfirst = (it.ks * C::kSBK + b) * kTK;
+        const int jlo = p.gdiv.div(it.ks * C::kSBK * kTK);
         const uint32_t acol = tmem + lane_addr + C::kACol0 + (d * C::kASlots + i % C::kASlots) * 32;
         tc_fence_after();
         if (MODE != kGeneral) {
@@ -326,32 +422,38 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
       const int t = tile / p.MT;
       const int m0 = (tile % p.MT) * BN;
       const int m_end = min(p.M, m0 + BN);
-      const int n = t * kTN + r;
-      float *piece = p.pieces + (static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * BN * kTN + r;
       const int db = seg % C::kDBufs;
-      // MMA warp e took part iff some stage of the segment has more than BPI * e K blocks (only a
-      // tile's last stage can be short)
-      const int nparts = ks_first < ks_last ? I : (stage_blocks(p, ks_last) + BPI - 1) / BPI;
+      // kTP = 1: MMA warp e took part iff some stage of the segment has more than BPI * e K blocks
+      // (only a tile's last stage can be short), and the parts are added. kTP = 2: MMA warp e's
+      // accumulator is weight tile e of the unit.
+      const int nparts =
+          C::kTP == 2 ? 1 : (ks_first < ks_last ? I : (stage_blocks<C::kSBK>(p, ks_last) + BPI - 1) / BPI);
       const bool ok = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err);
       if (!named_bar_and(1, 128, ok)) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
-        uint32_t v[16];
-        const uint32_t dbase = tmem + lane_addr + db * I * C::kDStride + c0;
-        tmem_ld_32x32b_x16(dbase, v);
-        tmem_wait_ld();
-        float f[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) f[q] = __uint_as_float(v[q]);
+      for (int te = 0; te < C::kTP; ++te) {
+        const int n = (t * C::kTP + te) * kTN + r;
+        float *piece =
+            p.pieces + ((static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * C::kTP + te) * BN * kTN + r;
 #pragma unroll 1
-        for (int e = 1; e < nparts; ++e) {  // the MMA warps' partial sums, in a fixed order
-          tmem_ld_32x32b_x16(dbase + e * C::kDStride, v);
+        for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
+          uint32_t v[16];
+          const uint32_t dbase = tmem + lane_addr + (db * I + te) * C::kDStride + c0;
+          tmem_ld_32x32b_x16(dbase, v);
           tmem_wait_ld();
+          float f[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) f[q] += __uint_as_float(v[q]);
+          for (int q = 0; q < 16; ++q) f[q] = __uint_as_float(v[q]);
+#pragma unroll 1
+          for (int e = 1; e < nparts; ++e) {  // the MMA warps' partial sums, in a fixed order
+            tmem_ld_32x32b_x16(dbase + e * C::kDStride, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 16; ++q) f[q] += __uint_as_float(v[q]);
+          }
+          emit16<BN>(p, whole, n, m0, m_end, c0, f, piece);
         }
-        emit16<BN>(p, whole, n, m0, m_end, c0, f, piece);
       }
       tc_fence_before();
       __syncwarp();
@@ -377,7 +479,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
         }
         __syncwarp();
         named_bar_sync(1, 128);
-        if (fix_sh.tile >= 0 && seg_end != u_end) reduce_pieces<BN>(p, fix_sh, r, 128);
+        if (fix_sh.tile >= 0 && seg_end != u_end) reduce_pieces<BN, C::kTP>(p, fix_sh, r, 128);
       }
       u = seg_end;
     }
@@ -391,7 +493,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE>::kThreads, 1)
     named_bar_sync(3, kFixThreads);
     if (final_fix_sh.tile >= 0) {
       griddep_wait();  // (already resolved: the epilogue waited before its first store)
-      reduce_pieces<BN>(p, final_fix_sh, static_cast<int>(threadIdx.x) - 32 * C::kDqWarp0, kFixThreads);
+      reduce_pieces<BN, C::kTP>(p, final_fix_sh, static_cast<int>(threadIdx.x) - 32 * C::kDqWarp0, kFixThreads);
     }
   }
 
@@ -427,10 +529,10 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 // x [M, K] fp16 row-major, 128-byte swizzle, zero fill outside, in one of two views:
-//  3-D [K/64][M][64] (K a multiple of 64): one box {64, BN, 4} is a whole stage, four BN x 64
+//  3-D [K/64][M][64] (K a multiple of 64): one box {64, BN, sbk} is a whole stage, sbk BN x 64
 //      sub-tiles one after another, each laid out as the MMA reads it;
 //  2-D [M][K]: one box {64, BN} per K block.
-bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, bool three_d) {
+bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, int sbk, bool three_d) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   if (three_d) {
@@ -438,7 +540,7 @@ bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, b
                                 static_cast<cuuint64_t>(K / kTK)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(kTK) * 2};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(kTK), static_cast<cuuint32_t>(bn),
-                               static_cast<cuuint32_t>(kSB)};
+                               static_cast<cuuint32_t>(sbk)};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(x), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -453,10 +555,39 @@ bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE>
-cudaError_t launch_t(const CUtensorMap &map, const Params &p, int ctas, cudaStream_t stream) {
-  using C = Cfg<BN, MODE>;
-  auto kern = w4a16_gemm_kernel<BN, MODE>;
+// The packed weights as two 3-D tensors of 32-bit words for the two-tile units (no swizzle, zero fill
+// outside): the tile region [NT][KB * 16][64] (a 4 KB code block is 16 rows of 256 bytes), one box
+// {64, 16 sbk, 2} = sbk blocks of two consecutive tiles; the record region [NT][G][80], one box
+// {80, recs, 2} = recs consecutive group records of both tiles.
+bool make_weight_maps(CUtensorMap *code_map, CUtensorMap *rec_map, const void *packed, int64_t NT, int64_t KB,
+                      int64_t G, int sbk, int recs) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const uint8_t *codes = static_cast<const uint8_t *>(packed);
+  const uint8_t *meta = codes + NT * KB * kTileBytes;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  {
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(KB * (kTileBytes / 256)), static_cast<cuuint64_t>(NT)};
+    const cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(KB * kTileBytes)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(sbk * (kTileBytes / 256)), 2};
+    if (enc(code_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t *>(codes), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  const cuuint64_t dims[3] = {kRecBytes / 4, static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(NT)};
+  const cuuint64_t strides[2] = {kRecBytes, static_cast<cuuint64_t>(G * kRecBytes)};
+  const cuuint32_t box[3] = {kRecBytes / 4, static_cast<cuuint32_t>(recs), 2};
+  return enc(rec_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t *>(meta), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int MODE, int TP>
+cudaError_t launch_t(const CUtensorMap &map, const CUtensorMap &code_map, const CUtensorMap &rec_map, const Params &p,
+                     int ctas, cudaStream_t stream) {
+  using C = Cfg<BN, MODE, TP>;
+  auto kern = w4a16_gemm_kernel<BN, MODE, TP>;
   // the dynamic shared-memory opt-in is a per-device function attribute
   static uint64_t done_mask = 0;
   static std::mutex mu;
@@ -471,24 +602,26 @@ cudaError_t launch_t(const CUtensorMap &map, const Params &p, int ctas, cudaStre
       if (dev < 64) done_mask |= 1ull << dev;
     }
   }
-  return launch_programmatic(kern, map, p, ctas, C::kThreads, C::kSmemBytes, stream);
+  return launch_programmatic(kern, ctas, C::kThreads, C::kSmemBytes, stream, map, code_map, rec_map, p);
 }
 
 // One group per 64-wide K block (g % 64 == 0) lets the dequant take the block's group once.
 int gemm_mode(int32_t g) { return g % 64 == 0 ? kScaleIn : kGeneral; }
 
-cudaError_t launch_variant(int bn, int mode, const CUtensorMap &map, const Params &p, int ctas,
-                           cudaStream_t stream) {
+cudaError_t launch_variant(int bn, int mode, int tp, const CUtensorMap &map, const CUtensorMap &code_map,
+                           const CUtensorMap &rec_map, const Params &p, int ctas, cudaStream_t stream) {
   if (mode == kScaleIn) {
-    if (bn == 16) return launch_t<16, kScaleIn>(map, p, ctas, stream);
-    if (bn == 32) return launch_t<32, kScaleIn>(map, p, ctas, stream);
-    if (bn == 64) return launch_t<64, kScaleIn>(map, p, ctas, stream);
-    if (bn == 128) return launch_t<128, kScaleIn>(map, p, ctas, stream);
+    if (bn == 16) return launch_t<16, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 32) return launch_t<32, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 64) return launch_t<64, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 1) return launch_t<128, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 2) return launch_t<128, kScaleIn, 2>(map, code_map, rec_map, p, ctas, stream);
   } else {
-    if (bn == 16) return launch_t<16, kGeneral>(map, p, ctas, stream);
-    if (bn == 32) return launch_t<32, kGeneral>(map, p, ctas, stream);
-    if (bn == 64) return launch_t<64, kGeneral>(map, p, ctas, stream);
-    if (bn == 128) return launch_t<128, kGeneral>(map, p, ctas, stream);
+    if (bn == 16) return launch_t<16, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 32) return launch_t<32, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 64) return launch_t<64, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 1) return launch_t<128, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 2) return launch_t<128, kGeneral, 2>(map, code_map, rec_map, p, ctas, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -502,8 +635,13 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
   if (bn == 0) bn = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
   if (bn != 8 && bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
-  const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK), ks = cdiv(kb, kSB);
-  const int64_t tiles = mt * nt;
+  // Units of two weight tiles and 128-wide K stages for block_n 128 from M = 256 up (two or more
+  // token tiles, so each CTA holds long runs of units and a tile pair is cut at most a few times);
+  // below that the pieces of a cut pair (two 64 KB tiles) make the fixup costlier than the x traffic
+  // it saves. Otherwise one tile and 256-wide stages.
+  const int tp = bn == 128 && M >= 256 ? 2 : 1;
+  const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK), ks = cdiv(kb, kSB / tp);
+  const int64_t tiles = mt * cdiv(nt, tp);  // output tiles of the schedule (units along K: ks each)
   const int64_t units = tiles * ks;
   if (tiles > 0x7FFFFFFF || units > (int64_t{1} << 40)) return false;
   int64_t P = ctas > 0 ? ctas : (num_sms > 0 ? num_sms : 148);
@@ -532,6 +670,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
   plan->n_tiles = static_cast<int>(nt);
   plan->k_blocks = static_cast<int>(kb);
   plan->k_stages = static_cast<int>(ks);
+  plan->tiles_per_unit = tp;
   plan->ctas = static_cast<int>(P);
   plan->gran = static_cast<int>(gran);
   plan->whole = whole;
@@ -539,7 +678,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
   plan->counters_offset = 256;
   const size_t counters_bytes = static_cast<size_t>(cdiv(tiles * 4, 256) * 256);
   plan->pieces_offset = plan->counters_offset + counters_bytes;
-  const size_t piece_bytes = whole ? 0 : static_cast<size_t>(P * 2 * kTN * bn * 4);
+  const size_t piece_bytes = whole ? 0 : static_cast<size_t>(P * 2 * tp * kTN * bn * 4);
   plan->workspace_bytes = plan->pieces_offset + piece_bytes;
   return true;
 }
@@ -548,10 +687,21 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
                         void *workspace, const GemmPlan &plan, cudaStream_t stream, bool *encode_failed) {
   *encode_failed = false;
   CUtensorMap map;
-  bool x3d = K % kTK == 0 && make_x_map(&map, x, M, K, plan.block_n, true);
-  if (!x3d && !make_x_map(&map, x, M, K, plan.block_n, false)) {
+  const int sbk = kSB / plan.tiles_per_unit;
+  bool x3d = K % kTK == 0 && make_x_map(&map, x, M, K, plan.block_n, sbk, true);
+  if (!x3d && !make_x_map(&map, x, M, K, plan.block_n, sbk, false)) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
+  }
+  CUtensorMap code_map, rec_map;  // the weights as tensors, for units of two weight tiles
+  std::memset(&code_map, 0, sizeof(code_map));
+  std::memset(&rec_map, 0, sizeof(rec_map));
+  if (plan.tiles_per_unit == 2) {
+    const int recs = gemm_mode(g) == kGeneral ? sbk * kTK / 8 + 1 : sbk * kTK / 64 + 1;
+    if (!make_weight_maps(&code_map, &rec_map, packed, plan.n_tiles, plan.k_blocks, cdiv(K, g), sbk, recs)) {
+      *encode_failed = true;
+      return cudaErrorInvalidValue;
+    }
   }
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   Params p;
@@ -576,7 +726,8 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.x3d = x3d ? 1 : 0;
   p.grains = plan.grains;
   if (plan.block_n == 8) return launch_gemm_rf(map, p, 1, g % kTK != 0, plan.ctas, stream);
-  return launch_variant(plan.block_n, gemm_mode(g), map, p, plan.ctas, stream);
+  return launch_variant(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p, plan.ctas,
+                        stream);
 }
 
 }  // namespace w4

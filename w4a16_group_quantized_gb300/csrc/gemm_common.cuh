@@ -67,9 +67,10 @@ __device__ __forceinline__ int owner_of(const Params &p, int64_t u) {
   return static_cast<int>(((v + 1) * p.P - 1) / p.grains);
 }
 
-// K blocks in stage ks of a tile: 4, except a shorter last stage when KB is not a multiple of 4.
+// K blocks in stage ks of a tile: SBK, except a shorter last stage when KB is not a multiple of SBK.
+template <int SBK = kSB>
 __device__ __forceinline__ int stage_blocks(const Params &p, int ks) {
-  return ks == p.KS - 1 ? p.KB - kSB * (p.KS - 1) : kSB;
+  return ks == p.KS - 1 ? p.KB - SBK * (p.KS - 1) : SBK;
 }
 
 // Walks (tile, ks, t, mt) over a CTA's units without divisions.
@@ -168,27 +169,32 @@ struct Fixup {
   int slot0;    // piece 0 is that CTA's second slot (its range began in an earlier tile)
 };
 
-// y = the pieces added in K order (piece q >= 1 is CTA c_first + q's first slot). nthreads threads
-// from tid = 0 share the work, element by element in the pieces' column-major order, so stores and
-// loads are coalesced and every thread has several independent loads in flight.
-template <int BN>
+// y = the pieces added in K order (piece q >= 1 is CTA c_first + q's first slot). A piece covers TP
+// weight tiles: [TP][BN][128] fp32. nthreads threads from tid = 0 share the work, element by element
+// in the pieces' column-major order, so stores and loads are coalesced and every thread has several
+// independent loads in flight.
+template <int BN, int TP = 1>
 __device__ __forceinline__ void reduce_pieces(const Params &p, const Fixup &f, int tid, int nthreads) {
   const float *src[kMaxPieces];
 #pragma unroll
   for (int q = 0; q < kMaxPieces; ++q)
     src[q] = p.pieces + (static_cast<int64_t>(f.c_first + (q < f.npieces ? q : 0)) * 2 + (q == 0 ? f.slot0 : 0)) *
-                            BN * kTN;
-  const int n0 = (f.tile / p.MT) * kTN;
+                            TP * BN * kTN;
+  const int n0 = (f.tile / p.MT) * TP * kTN;
   const int m0 = (f.tile % p.MT) * BN;
   const int ncols = min(p.M, m0 + BN) - m0;
-#pragma unroll 4
-  for (int e = tid; e < ncols * kTN; e += nthreads) {
-    float acc = __ldcg(src[0] + e);
 #pragma unroll
-    for (int q = 1; q < kMaxPieces; ++q)
-      if (q < f.npieces) acc += __ldcg(src[q] + e);
-    const int n = n0 + e % kTN;
-    if (n < p.N) p.y[static_cast<int64_t>(m0 + e / kTN) * p.N + n] = __float2half_rn(acc);
+  for (int te = 0; te < TP; ++te) {
+#pragma unroll 4
+    for (int e = tid; e < ncols * kTN; e += nthreads) {
+      const int o = te * BN * kTN + e;
+      float acc = __ldcg(src[0] + o);
+#pragma unroll
+      for (int q = 1; q < kMaxPieces; ++q)
+        if (q < f.npieces) acc += __ldcg(src[q] + o);
+      const int n = n0 + te * kTN + e % kTN;
+      if (n < p.N) p.y[static_cast<int64_t>(m0 + e / kTN) * p.N + n] = __float2half_rn(acc);
+    }
   }
   if (tid == 0) p.counters[f.tile] = 0u;  // ready for the next call
 }
@@ -262,9 +268,9 @@ __device__ __forceinline__ void produce_stages(const CUtensorMap *x_map, const P
 
 // Launch with programmatic stream serialization: the launch may overlap the previous kernel's tail;
 // the kernels wait for it (griddepcontrol.wait) before touching global memory it may have written.
-template <typename Kernel>
-cudaError_t launch_programmatic(Kernel kern, const CUtensorMap &map, const Params &p, int ctas, int threads,
-                                int smem_bytes, cudaStream_t stream) {
+template <typename Kernel, typename... Args>
+cudaError_t launch_programmatic(Kernel kern, int ctas, int threads, int smem_bytes, cudaStream_t stream,
+                                const Args &...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(static_cast<unsigned>(threads));
@@ -275,7 +281,7 @@ cudaError_t launch_programmatic(Kernel kern, const CUtensorMap &map, const Param
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -402,7 +402,7 @@ cudaError_t launch_rf_t(const CUtensorMap &map, const Params &p, int ctas, cudaS
       if (dev < 64) done_mask |= 1ull << dev;
     }
   }
-  return launch_programmatic(kern, map, p, ctas, C::kThreads, C::kSmemBytes, stream);
+  return launch_programmatic(kern, ctas, C::kThreads, C::kSmemBytes, stream, map, p);
 }
 
 }  // namespace

@@ -26,7 +26,8 @@ struct GemmPlan {
   int m_tiles;
   int n_tiles;
   int k_blocks;
-  int k_stages;  // 256-wide K stages (4 K blocks; the last may be shorter)
+  int k_stages;  // K stages per output tile (4 K blocks, or 2 for two-tile units; the last may be shorter)
+  int tiles_per_unit;  // weight tiles per unit: 2 for block_n 128 (one x tile serves both), else 1
   int ctas;      // persistent CTAs (one per SM)
   int gran;      // K stages per scheduling grain: 1 (stream-K) or k_stages (whole tiles)
   bool whole;    // whole-tile schedule (no tile is cut between CTAs)
