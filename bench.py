@@ -8,8 +8,10 @@ M in {1, 4, 8, 16, 32, 64, 128} against each of the four layers
 synthetic fp16 (weights ~ N(0, 0.02^2) quantized by w4_pack/w4_repack,
 activations ~ N(0, 1)), resident in HBM before the timed region.
 
-The step is captured once as a CUDA graph (host launch cost is larger than
-a decode GEMM) and replayed; each layer has three weight copies used in turn
+The step is captured as two CUDA graphs (host launch cost is larger than a
+decode GEMM), the M <= 8 GEMMs first: CUDA events around each graph time the
+step and, inside it, the dominant kernel (the register-operand decode kernel)
+whose roofline is reported. Each layer has three weight copies used in turn
 inside a step and L2 is flushed (a write of a buffer larger than L2) between
 timed replays, so weights stream from HBM. Prints one JSON line.
 
@@ -21,6 +23,7 @@ cores) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -44,6 +47,12 @@ WORKLOAD = ("llama2-7b decode sweep, g=128: M in {1,4,8,16,32,64,128} x "
             "[12288x4096 qkv, 4096x4096 o_proj, 22016x4096 gate_up, 4096x11008 down] (28 GEMMs/step)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
+# The step's dominant kernel by device time: the register-operand decode kernel, which runs the
+# GEMMs with M <= DOM_M (12 of the 28 launches); its roofline is reported, timed inside the step.
+DOM_M = 8
+DOM_KERNEL = "w4a16_gemm_rf_kernel"
+DOM_SOURCES = ("gemm_rf.cu", "gemm_common.cuh", "ptx.cuh")
+TRAFFIC_FILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "decode_kernel_traffic.json")
 
 
 def sweep():
@@ -62,6 +71,24 @@ def alg_bytes(m, n, k, g):
 
 def gemm_flops(m, n, k):
     return 2.0 * m * n * k
+
+
+def dom_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu capture, or None when the
+    kernel's sources changed since the counters were taken (their SHA-256 is stored beside them)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "w4a16_group_quantized_gb300", "csrc")
+    for name in DOM_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    if rec.get("sources_sha256") != h.hexdigest():
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def load_peaks():
@@ -247,20 +274,27 @@ def run_gpu(args):
     ws = torch.zeros(ws_need, dtype=torch.uint8, device=dev)
     flush = torch.empty(max(L2_FLUSH_BYTES, 2 * l2), dtype=torch.uint8, device=dev)
 
-    def step_eager(rot=0):
+    def step_eager(part=None, rot=0):
+        # part 0: the GEMMs of the dominant kernel (M <= DOM_M), part 1: the others, None: all of them
         use = {L.name: rot for L in layers}
         for m, L in sweep():
             c = copies[L.name]
-            w4.w4a16_gemm(xs[m][L.k], c[use[L.name] % 3], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
+            if part is None or (m <= DOM_M) == (part == 0):
+                w4.w4a16_gemm(xs[m][L.k], c[use[L.name] % 3], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
             use[L.name] += 1
 
     # warm-up launches outside capture (per-device kernel attributes), then capture the step
     with torch.cuda.stream(stream):
         step_eager()
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step_eager()
+    # the step as two graphs, the dominant kernel's launches first, so that events between them time
+    # that kernel inside the timed region
+    graphs = []
+    for part in (0, 1):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step_eager(part)
+        graphs.append(gr)
     torch.cuda.synchronize()
     assert w4.w4_last_device_error(ws) == 0
 
@@ -270,11 +304,13 @@ def run_gpu(args):
 
     # ---- timed region
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             flush.zero_()
-            graph.replay()
+            graphs[0].replay()
+            graphs[1].replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -287,7 +323,9 @@ def run_gpu(args):
             for i in range(args.steps):
                 flush.zero_()  # L2 flush between timed steps (outside the events)
                 starts[i].record(stream)
-                graph.replay()
+                graphs[0].replay()
+                mids[i].record(stream)
+                graphs[1].replay()
                 ends[i].record(stream)
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
@@ -295,6 +333,7 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dom_ms = sum(s.elapsed_time(e) for s, e in zip(starts, mids)) / args.steps
     total_ms = sum(step_ms)
     if dist:
         t = torch.tensor([total_ms], device=dev)
@@ -409,6 +448,9 @@ def run_gpu(args):
                "sample": "the whole decode sweep (28 GEMMs) through the fp64 oracle, timed once",
                "seconds": round(t, 2)}
 
+    dom = [(m, L) for m, L in sweep() if m <= DOM_M]
+    dom_bytes = sum(alg_bytes(m, L.n, L.k, L.g) for m, L in dom)
+    dom_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9  # = bytes per average launch / its average duration
     t_roof = sum(max(alg_bytes(m, L.n, L.k, L.g) / (peaks["hbm_gbs"] * 1e9),
                      gemm_flops(m, L.n, L.k) / (peaks["bf16_tflops"] * 1e12)) for m, L in sweep())
     achieved = bytes_step / (ms_per_step * 1e-3) / 1e9
@@ -421,13 +463,18 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "gemms_per_step": len(sweep()),
                    "l2": "flushed between timed steps (512 MB write); 3 weight copies per layer rotate within a step",
-                   "timing": "step captured as one CUDA graph, CUDA events per replay, max over ranks",
+                   "timing": "step captured as two CUDA graphs (the M <= 8 GEMMs, then the rest); CUDA events "
+                             "around each per replay; max over ranks",
                    "parallelism": f"replicas x{world}"},
         "weight_gbs": round(wbytes_step / (ms_per_step * 1e-3) / 1e9, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
-                     "time_frac": round(t_roof / (ms_per_step * 1e-3), 4),
+        "roofline": {"bound": "hbm", "achieved": round(dom_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(dom_achieved / peaks["hbm_gbs"], 4), "traffic": dom_traffic(),
+                     "kernel": f"{DOM_KERNEL} (the {len(dom)} GEMMs with M <= {DOM_M})",
+                     "launches_per_step": len(dom), "alg_bytes_per_launch": round(dom_bytes / len(dom)),
+                     "us_per_launch": round(dom_ms * 1e3 / len(dom), 3),
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                     "step": {"achieved": round(achieved, 1), "frac": round(achieved / peaks["hbm_gbs"], 4),
+                              "time_frac": round(t_roof / (ms_per_step * 1e-3), 4)},
                      "decode_m_le_16": {"achieved": round(dec_bytes / dec_time / 1e9, 1),
                                         "frac": round(dec_bytes / dec_time / 1e9 / peaks["hbm_gbs"], 4)}},
         "cpu_baseline": cpu,

@@ -100,6 +100,17 @@ def test_two_tile_units(M, N, K, g, ctas, schedule):
     check(M, N, K, g, block_n=128, ctas=ctas, schedule=schedule)
 
 
+@pytest.mark.parametrize("M,N,K,g,block_n,ctas", [
+    (300, 1000, 1024, 128, 64, 7),  # 5 token tiles x 8 weight tiles over 7 CTAs: uneven tile counts
+    (512, 700, 960, 128, 128, 5),   # two-tile units, a ragged pair, a one-block last stage
+    (100, 300, 520, 40, 32, 3),     # per-word group lookup
+    (40, 260, 256, 128, 16, 9),     # one K stage per tile: consecutive units are different tiles
+])
+def test_interleaved_whole_tiles(M, N, K, g, block_n, ctas):
+    # whole tiles of several token tiles go round-robin: CTA c takes tiles c, c + P, c + 2P, ...
+    check(M, N, K, g, block_n=block_n, ctas=ctas, schedule=2)
+
+
 @pytest.mark.parametrize("g", [8, 16, 24, 32, 40, 64, 96, 128, 192, 256, 384, 512, 1024])
 def test_group_sizes(g):
     # g % 64 == 0 puts one group in each 64-wide K block: the decode kernel (block_n 8) then scales

@@ -134,7 +134,9 @@ __device__ __forceinline__ void produce_stages_pair(const CUtensorMap *x_map, co
   constexpr int kCodeBytes = 2 * SBK * kTileBytes;
   constexpr int kRecBox = 2 * kMaxRecs * kRecBytes;
   constexpr int kRowsPerBlock = kTileBytes / 256;  // 256-byte rows of the code view
-  const uint64_t pol_stream = policy_evict_first();
+  // weights read once (one token tile) stream through L2 (evict first, so x stays); with several
+  // token tiles the CTA reads each weight tile again for the next token tile, so they stay cached
+  const uint64_t pol_stream = p.MT == 1 ? policy_evict_first() : policy_evict_normal();
   if (pw == 0 && lane == 0 && nst > 0) {
     StageIter f;
     f.init(p, u0);
@@ -153,7 +155,8 @@ __device__ __forceinline__ void produce_stages_pair(const CUtensorMap *x_map, co
   }
   griddep_wait();
   StageIter it;
-  it.init(p, u0 + pw);
+  it.init(p, u0);
+  it.advance(p, pw);
   int i = pw;
   for (; i < nst; i += 2, it.advance(p, 2)) {
     const int s = i % S;
@@ -221,8 +224,9 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
   volatile uint32_t *abort_flag = &abort_sh;
 
   const int cta = blockIdx.x;
-  const int64_t u0 = range_begin(p, cta);
-  const int nst = static_cast<int>(range_begin(p, cta + 1) - u0);
+  int64_t u0;
+  int nst;
+  cta_units(p, cta, &u0, &nst);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -409,15 +413,16 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
     const int lq = warp % 4;
     const int r = lq * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
-    const int64_t u_end = u0 + nst;
     griddep_wait();  // y and the workspace may still be in use by the previous grid
     int seg = 0;
-    for (int64_t u = u0; u < u_end; ++seg) {
+    for (int ul = 0; ul < nst; ++seg) {  // local units ul .. ul + seg_len - 1: one tile segment
+      const int64_t u = unit_at(p, cta, u0, ul);
       const int tile = static_cast<int>(u / p.KS);
       const int64_t tile_u0 = static_cast<int64_t>(tile) * p.KS;
-      const int64_t seg_end = min(u_end, tile_u0 + p.KS);
       const int ks_first = static_cast<int>(u - tile_u0);
-      const int ks_last = static_cast<int>(seg_end - 1 - tile_u0);
+      const int seg_len = min(nst - ul, p.KS - ks_first);
+      const int ks_last = ks_first + seg_len - 1;
+      const bool last_seg = ul + seg_len == nst;
       const bool whole = ks_first == 0 && ks_last == p.KS - 1;
       const int t = tile / p.MT;
       const int m0 = (tile % p.MT) * BN;
@@ -475,13 +480,13 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
           fix_sh = f;
           // the CTA's last segment: every dequant and epilogue warp is free after it, so they all do
           // this fixup together below
-          if (seg_end == u_end) final_fix_sh = f;
+          if (last_seg) final_fix_sh = f;
         }
         __syncwarp();
         named_bar_sync(1, 128);
-        if (fix_sh.tile >= 0 && seg_end != u_end) reduce_pieces<BN, C::kTP>(p, fix_sh, r, 128);
+        if (fix_sh.tile >= 0 && !last_seg) reduce_pieces<BN, C::kTP>(p, fix_sh, r, 128);
       }
-      u = seg_end;
+      ul += seg_len;
     }
   }
 
@@ -674,6 +679,9 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
   plan->ctas = static_cast<int>(P);
   plan->gran = static_cast<int>(gran);
   plan->whole = whole;
+  // whole tiles of several token tiles are dealt out round-robin, so that the CTAs running together
+  // read the same weight tiles (one DRAM read, the rest L2 hits)
+  plan->interleave = whole && mt > 1;
   plan->grains = grains;
   plan->counters_offset = 256;
   const size_t counters_bytes = static_cast<size_t>(cdiv(tiles * 4, 256) * 256);
@@ -724,6 +732,7 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.P = plan.ctas;
   p.gran = plan.gran;
   p.x3d = x3d ? 1 : 0;
+  p.tstride = plan.interleave ? plan.ctas : 1;
   p.grains = plan.grains;
   if (plan.block_n == 8) return launch_gemm_rf(map, p, 1, g % kTK != 0, plan.ctas, stream);
   return launch_variant(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p, plan.ctas,

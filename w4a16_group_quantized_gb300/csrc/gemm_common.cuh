@@ -38,10 +38,12 @@ inline FastDiv make_fastdiv(uint32_t d) {
   return f;
 }
 
-// Work decomposition. A unit is one 256-wide K stage of one output tile (128 weight rows x BN
-// activation rows); units are numbered tile-major: u = tile * KS + ks, tile = t * MT + mt.
+// Work decomposition. A unit is one K stage of one output tile (128 weight rows, or 256 for two-tile
+// units, x BN activation rows); units are numbered tile-major: u = tile * KS + ks, tile = t * MT + mt.
 // CTA c owns the contiguous units [begin(c), begin(c+1)), cut at multiples of `gran` units
-// (gran = 1: stream-K, any cut; gran = KS: whole tiles only).
+// (gran = 1: stream-K, any cut; gran = KS: whole tiles only); or, for whole tiles of several token
+// tiles (tstride = P), the tiles c, c + P, c + 2P, ...: the CTAs running at one time then share
+// weight tiles (tile t * MT + mt for consecutive mt), whose re-reads hit L2.
 struct Params {
   const uint8_t *codes;  // tile region of the packed weights
   const uint8_t *meta;   // group-record region of the packed weights
@@ -53,6 +55,7 @@ struct Params {
   int P;                 // CTAs
   int gran;              // units per scheduling grain
   int x3d;               // x tensor map is [KB][M][64] (one copy per stage); else [M][K] (one per block)
+  int tstride;           // tiles between a CTA's consecutive tiles: 1 (contiguous ranges) or P
   FastDiv gdiv;          // division by g
   int64_t grains;        // total units / gran
 };
@@ -61,7 +64,24 @@ __device__ __forceinline__ int64_t range_begin(const Params &p, int c) {
   return static_cast<int64_t>(c) * p.grains / p.P * p.gran;
 }
 
-// The CTA whose range holds unit u: the largest c with range_begin(c) <= u.
+// CTA c's first unit and its number of units (stages).
+__device__ __forceinline__ void cta_units(const Params &p, int c, int64_t *u0, int *nst) {
+  if (p.tstride == 1) {
+    *u0 = range_begin(p, c);
+    *nst = static_cast<int>(range_begin(p, c + 1) - *u0);
+  } else {  // whole tiles c, c + P, ...: p.grains tiles
+    *u0 = static_cast<int64_t>(c) * p.KS;
+    *nst = c < p.grains ? static_cast<int>((p.grains - c + p.P - 1) / p.P) * p.KS : 0;
+  }
+}
+
+// The global unit of CTA c's local unit ul (its first unit u0).
+__device__ __forceinline__ int64_t unit_at(const Params &p, int c, int64_t u0, int ul) {
+  if (p.tstride == 1) return u0 + ul;
+  return (static_cast<int64_t>(c) + static_cast<int64_t>(ul / p.KS) * p.tstride) * p.KS + ul % p.KS;
+}
+
+// The CTA whose range holds unit u: the largest c with range_begin(c) <= u (contiguous ranges).
 __device__ __forceinline__ int owner_of(const Params &p, int64_t u) {
   const int64_t v = u / p.gran;
   return static_cast<int>(((v + 1) * p.P - 1) / p.grains);
@@ -73,7 +93,8 @@ __device__ __forceinline__ int stage_blocks(const Params &p, int ks) {
   return ks == p.KS - 1 ? p.KB - SBK * (p.KS - 1) : SBK;
 }
 
-// Walks (tile, ks, t, mt) over a CTA's units without divisions.
+// Walks (tile, ks, t, mt) over a CTA's units (without divisions for contiguous ranges). Every step
+// stays within the CTA's own units: ranges are whole tiles whenever tstride > 1.
 struct StageIter {
   int tile, ks, t, mt;
   __device__ __forceinline__ void init(const Params &p, int64_t u) {
@@ -86,10 +107,16 @@ struct StageIter {
     ks += step;
     while (ks >= p.KS) {
       ks -= p.KS;
-      ++tile;
-      if (++mt == p.MT) {
-        mt = 0;
-        ++t;
+      if (p.tstride == 1) {
+        ++tile;
+        if (++mt == p.MT) {
+          mt = 0;
+          ++t;
+        }
+      } else {
+        tile += p.tstride;
+        t = tile / p.MT;
+        mt = tile % p.MT;
       }
     }
   }
@@ -213,7 +240,9 @@ __device__ __forceinline__ void produce_stages(const CUtensorMap *x_map, const P
   constexpr int kXSub = BN * 128;
   constexpr int kXBytes = kSB * kXSub;
   constexpr int kCodeBytes = kSB * kTileBytes;
-  const uint64_t pol_stream = policy_evict_first();
+  // weights read once (one token tile) stream through L2 (evict first, so x stays); with several
+  // token tiles the CTA reads each weight tile again for the next token tile, so they stay cached
+  const uint64_t pol_stream = p.MT == 1 ? policy_evict_first() : policy_evict_normal();
   if (pw == 0 && lane == 0 && nst > 0) {
     StageIter f;
     f.init(p, u0);
@@ -227,7 +256,8 @@ __device__ __forceinline__ void produce_stages(const CUtensorMap *x_map, const P
   }
   griddep_wait();
   StageIter it;
-  it.init(p, u0 + pw);
+  it.init(p, u0);
+  it.advance(p, pw);
   int i = pw;
   for (; i < nst; i += 2, it.advance(p, 2)) {
     const int s = i % S;

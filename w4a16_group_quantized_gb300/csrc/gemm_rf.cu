@@ -211,8 +211,9 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
   volatile uint32_t *abort_flag = &abort_sh;
 
   const int cta = blockIdx.x;
-  const int64_t u0 = range_begin(p, cta);
-  const int nst = static_cast<int>(range_begin(p, cta + 1) - u0);
+  int64_t u0;
+  int nst;
+  cta_units(p, cta, &u0, &nst);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {

@@ -31,6 +31,7 @@ struct GemmPlan {
   int ctas;      // persistent CTAs (one per SM)
   int gran;      // K stages per scheduling grain: 1 (stream-K) or k_stages (whole tiles)
   bool whole;    // whole-tile schedule (no tile is cut between CTAs)
+  bool interleave;  // whole tiles dealt out round-robin (CTA c: tiles c, c + ctas, ...), else ranges
   int64_t grains;
   size_t counters_offset;
   size_t pieces_offset;
