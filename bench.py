@@ -493,6 +493,59 @@ def run_gpu(args):
     return 0
 
 
+def run_prefill(args):
+    """The prefill config: M in {256, 512, 1024, 4096} x the four Llama-2-70B-shaped layers (g = 128,
+    outlier activations), each GEMM launched back to back (CUDA events, after warm-up) beside a dense
+    fp16 torch.matmul of the same shape; prints one JSON line with TFLOP/s and the fraction of the
+    measured bf16 tensor peak."""
+    import torch
+
+    import w4a16_group_quantized_gb300 as w4
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    reps = max(3, args.steps // 2)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / reps
+
+    rows = []
+    for L in workloads.PREFILL_LAYERS:
+        W = torch.from_numpy(workloads.weights_f16(L.n, L.k)).to(dev)
+        qw, sc, zw = w4.w4_pack(W, L.g)
+        packed = w4.w4_repack(qw, sc, zw, L.n, L.k, L.g)
+        del qw, sc, zw
+        for m in workloads.PREFILL_MS:
+            x = torch.from_numpy(workloads.activations_f16(m, L.k, outliers=True)).to(dev)
+            y = torch.empty((m, L.n), dtype=torch.float16, device=dev)
+            ws = torch.zeros(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g), dtype=torch.uint8, device=dev)
+            t = timed(lambda: w4.w4a16_gemm(x, packed, L.n, L.k, L.g, y=y, workspace=ws))
+            assert w4.w4_last_device_error(ws) == 0
+            td = timed(lambda: torch.matmul(x, W.t()))
+            f = gemm_flops(m, L.n, L.k)
+            bn, ctas, sched = w4.w4a16_gemm_plan(m, L.n, L.k, L.g)
+            rows.append({"M": m, "layer": L.name, "us": round(t * 1e6, 2), "tflops": round(f / t / 1e12, 1),
+                         "tensor_frac": round(f / t / 1e12 / peaks["bf16_tflops"], 3),
+                         "dense_us": round(td * 1e6, 2), "dense_tflops": round(f / td / 1e12, 1),
+                         "block_n": bn, "ctas": ctas, "schedule": "stream-K" if sched == 1 else "whole tiles"})
+            del x, y, ws
+        del W, packed
+    print(json.dumps({"prefill": rows, "peak_tflops": peaks["bf16_tflops"],
+                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst)",
+                      "timing": f"{reps} back-to-back launches after {args.warmup} warm-ups, CUDA events"}))
+    return 0
+
+
 def run_case(args):
     """One GEMM configuration launched --steps times (for focused profiling); prints a short JSON line."""
     import torch
@@ -538,12 +591,15 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense fp16 comparison")
     ap.add_argument("--case", default=None, help="M:layer_name - run only that GEMM (for profiling)")
+    ap.add_argument("--prefill", action="store_true", help="time the prefill config instead of the decode step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
     if args.case:
         return run_case(args)
+    if args.prefill:
+        return run_prefill(args)
     return run_gpu(args)
 
 

@@ -34,10 +34,11 @@
 // TMA/mbarrier ring, each x tile is reused by all 128 weight rows, and the
 // dequant warps run ahead of the asynchronous MMAs through tensor-memory slots.
 //
-// Fixup of a cut tile: each CTA holding a piece writes it (fp32) to the
-// workspace and counts itself in on the tile's counter; the last to arrive
-// adds the pieces in K order (deterministic) and writes y. Nothing ever waits
-// on another CTA. Every mbarrier wait is bounded (ptx.cuh).
+// A tile cut between CTAs is finished by its owner, the CTA holding its first
+// K stages: the others store their fp32 pieces to the workspace and count
+// themselves in early in their ranges; the owner adds the pieces to its own
+// partial sums in K order (deterministic) and writes y (gemm_common.cuh).
+// Every wait is bounded (ptx.cuh).
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -196,6 +197,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
                       const __grid_constant__ CUtensorMap rec_map, const Params p) {
   using C = Cfg<BN, MODE, TP>;
   constexpr int S = C::kStages;
+  // the owner of a cut tile parks its sums ([kTP][BN][128] fp32) in the idle stage ring
+  constexpr bool kOwnInSmem = C::kTP * BN * kTN * 4 <= S * C::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   // Per-stage barriers (ring index = local stage index i mod the ring size; every waiter waits on
   // every phase of the barriers it uses, in order, so no parity wait can skip a phase):
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
   __shared__ __align__(8) uint64_t drain_bar[I];
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t abort_sh;
-  __shared__ Fixup fix_sh;        // the fixup of the segment the epilogue just finished
-  __shared__ Fixup final_fix_sh;  // the fixup all dequant and epilogue warps do at the end
+  __shared__ int npieces_sh;      // pieces of the cut tile the epilogue's segment owns
+  __shared__ int own_tile_sh;     // the cut tile the CTA's last segment owns, or -1
 
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x / 32;
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       mbar_init(smem_u32(&dempty_bar[d]), 4);
     }
     abort_sh = 0;
-    final_fix_sh.tile = -1;
+    own_tile_sh = -1;
     fence_mbar_init();
   }
   if (warp == C::kDqWarp0) {
@@ -422,7 +425,6 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       const int ks_first = static_cast<int>(u - tile_u0);
       const int seg_len = min(nst - ul, p.KS - ks_first);
       const int ks_last = ks_first + seg_len - 1;
-      const bool last_seg = ul + seg_len == nst;
       const bool whole = ks_first == 0 && ks_last == p.KS - 1;
       const int t = tile / p.MT;
       const int m0 = (tile % p.MT) * BN;
@@ -433,9 +435,25 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       // accumulator is weight tile e of the unit.
       const int nparts =
           C::kTP == 2 ? 1 : (ks_first < ks_last ? I : (stage_blocks<C::kSBK>(p, ks_last) + BPI - 1) / BPI);
-      const bool ok = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err);
-      if (!named_bar_and(1, 128, ok)) break;
+      // a cut tile: its owner (the segment holds the tile's first stages) waits for the other pieces
+      // before the accumulators are done, so the wait overlaps its last stages; any other piece is
+      // stored and counted in (gemm_common.cuh)
+      const bool owner = !whole && ks_first == 0;
+      bool ok = true;
+      if (owner && r == 0) {
+        const int np = tile_pieces(p, tile, cta);
+        ok = wait_pieces(p, tile, np, abort_flag);
+        npieces_sh = np;
+      }
+      const bool landed = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err);
+      if (!named_bar_and(1, 128, ok && landed)) break;  // (also publishes npieces_sh)
       tc_fence_after();
+      // With four or more pieces the owner's own sums go to shared memory (the stage ring is idle:
+      // every MMA is done), where all dequant and epilogue warps add the other pieces below; with
+      // fewer the epilogue adds them itself (measured on the 7B decode shapes: the extra barrier and
+      // round trip through shared memory cost more than the wider reduction saves below four).
+      const bool shared_fix = kOwnInSmem && owner && npieces_sh >= 4;
+      float *own = reinterpret_cast<float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
 #pragma unroll 1
       for (int te = 0; te < C::kTP; ++te) {
         const int n = (t * C::kTP + te) * kTN + r;
@@ -457,48 +475,64 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 16; ++q) f[q] += __uint_as_float(v[q]);
           }
-          emit16<BN>(p, whole, n, m0, m_end, c0, f, piece);
+          if (shared_fix) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) own[(te * BN + c0 + q) * kTN + r] = f[q];
+          } else {
+            if (owner) {  // the epilogue adds the later pieces in K order
+#pragma unroll 1
+              for (int pc = 1; pc < npieces_sh; ++pc) {
+                const float *src = piece_of<BN, C::kTP>(p, cta + pc, 0) + (te * BN + c0) * kTN + r;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) f[q] += __ldcg(src + q * kTN);
+              }
+            }
+            emit16<BN>(p, whole || owner, n, m0, m_end, c0, f, piece);
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[db]));
-      if (!whole) {
-        // the last CTA to finish a piece of this tile adds all pieces in K order and writes y. The
-        // warpgroup's piece stores are ordered (barrier) before one thread's count, an acquire-release
-        // atomic; the thread that sees the last count has acquired the other pieces, and the
-        // barrier after it orders their reads.
+      if (!whole && !owner) {
+        // a later piece of a cut tile: the warpgroup's stores are ordered (barrier) before one
+        // thread's release count
         __syncwarp();
         named_bar_sync(1, 128);
-        if (r == 0) {
-          Fixup f;
-          f.c_first = owner_of(p, tile_u0);
-          f.npieces = owner_of(p, tile_u0 + p.KS - 1) - f.c_first + 1;
-          f.slot0 = range_begin(p, f.c_first) != tile_u0 ? 1 : 0;
-          const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile]);
-          f.tile = old == static_cast<uint32_t>(f.npieces - 1) ? tile : -1;
-          fix_sh = f;
-          // the CTA's last segment: every dequant and epilogue warp is free after it, so they all do
-          // this fixup together below
-          if (last_seg) final_fix_sh = f;
-        }
-        __syncwarp();
-        named_bar_sync(1, 128);
-        if (fix_sh.tile >= 0 && !last_seg) reduce_pieces<BN, C::kTP>(p, fix_sh, r, 128);
+        if (r == 0) red_add_release_gpu(&p.counters[tile]);
       }
+      if (shared_fix && r == 0) own_tile_sh = tile;  // (the owner's segment is the CTA's last)
       ul += seg_len;
     }
   }
 
   if (warp >= C::kDqWarp0) {
-    // the dequant warps (past their last stage) and the epilogue warpgroup (past its last segment)
-    // do the fixup of the CTA's last segment together, if this CTA finished that tile last
+    // the owner's fixup: every dequant and epilogue warp is idle now; they add the later pieces to
+    // the owner's sums in K order and write y
     constexpr int kFixThreads = 32 * (C::kEpiWarp0 + 4 - C::kDqWarp0);
     __syncwarp();
     named_bar_sync(3, kFixThreads);
-    if (final_fix_sh.tile >= 0) {
-      griddep_wait();  // (already resolved: the epilogue waited before its first store)
-      reduce_pieces<BN, C::kTP>(p, final_fix_sh, static_cast<int>(threadIdx.x) - 32 * C::kDqWarp0, kFixThreads);
+    const int tile = own_tile_sh;
+    if (tile >= 0) {
+      const float *own = reinterpret_cast<const float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
+      const int npieces = npieces_sh;
+      const int n0 = (tile / p.MT) * C::kTP * kTN;
+      const int m0 = (tile % p.MT) * BN;
+      const int ncols = min(p.M, m0 + BN) - m0;
+      const int tid = static_cast<int>(threadIdx.x) - 32 * C::kDqWarp0;
+#pragma unroll
+      for (int te = 0; te < C::kTP; ++te) {
+#pragma unroll 2
+        for (int e = tid; e < ncols * kTN; e += kFixThreads) {
+          const int o = te * BN * kTN + e;
+          float acc = own[o];
+#pragma unroll
+          for (int pc = 1; pc < kMaxPieces; ++pc)
+            if (pc < npieces) acc += __ldcg(piece_of<BN, C::kTP>(p, cta + pc, 0) + o);
+          const int n = n0 + te * kTN + e % kTN;
+          if (n < p.N) p.y[static_cast<int64_t>(m0 + e / kTN) * p.N + n] = __float2half_rn(acc);
+        }
+      }
     }
   }
 

@@ -188,42 +188,42 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// The fixup of a cut tile, done by the last CTA to finish a piece of it.
-struct Fixup {
-  int tile;     // -1: nothing to do
-  int c_first;  // CTA holding the tile's first K stages (piece 0)
-  int npieces;
-  int slot0;    // piece 0 is that CTA's second slot (its range began in an earlier tile)
-};
+// Tiles cut between CTAs (stream-K). A cut tile's owner is the CTA holding its first K stages;
+// those are always the last units of the owner's range (ranges are contiguous and the tile goes on
+// past the range's end). Every other CTA holding a piece of the tile holds it in its first (or
+// only) segment: it stores the piece ([TP][BN][128] fp32, slot 0 of its two) and counts itself in
+// with a release add. The owner, when its own part is done, waits (bounded) until all the others
+// have counted in, adds their pieces to its own partial sums in K order and writes y; it leaves the
+// counter at 0. Only owners wait, and only for pieces that the other CTAs produce without waiting,
+// so the schedule cannot deadlock however the CTAs are scheduled.
 
-// y = the pieces added in K order (piece q >= 1 is CTA c_first + q's first slot). A piece covers TP
-// weight tiles: [TP][BN][128] fp32. nthreads threads from tid = 0 share the work, element by element
-// in the pieces' column-major order, so stores and loads are coalesced and every thread has several
-// independent loads in flight.
-template <int BN, int TP = 1>
-__device__ __forceinline__ void reduce_pieces(const Params &p, const Fixup &f, int tid, int nthreads) {
-  const float *src[kMaxPieces];
-#pragma unroll
-  for (int q = 0; q < kMaxPieces; ++q)
-    src[q] = p.pieces + (static_cast<int64_t>(f.c_first + (q < f.npieces ? q : 0)) * 2 + (q == 0 ? f.slot0 : 0)) *
-                            TP * BN * kTN;
-  const int n0 = (f.tile / p.MT) * TP * kTN;
-  const int m0 = (f.tile % p.MT) * BN;
-  const int ncols = min(p.M, m0 + BN) - m0;
-#pragma unroll
-  for (int te = 0; te < TP; ++te) {
-#pragma unroll 4
-    for (int e = tid; e < ncols * kTN; e += nthreads) {
-      const int o = te * BN * kTN + e;
-      float acc = __ldcg(src[0] + o);
-#pragma unroll
-      for (int q = 1; q < kMaxPieces; ++q)
-        if (q < f.npieces) acc += __ldcg(src[q] + o);
-      const int n = n0 + te * kTN + e % kTN;
-      if (n < p.N) p.y[static_cast<int64_t>(m0 + e / kTN) * p.N + n] = __float2half_rn(acc);
+// The piece CTA c keeps in slot `slot` (0: its first segment, 1: its last).
+template <int BN, int TP>
+__device__ __forceinline__ const float *piece_of(const Params &p, int c, int slot) {
+  return p.pieces + (static_cast<int64_t>(c) * 2 + slot) * TP * BN * kTN;
+}
+
+// The owner's wait for the other npieces - 1 pieces of its tile (one thread; the caller's barrier
+// after it orders the other threads' piece reads). Resets the counter. False on abort or timeout.
+__device__ __forceinline__ bool wait_pieces(const Params &p, int tile, int npieces, volatile uint32_t *abort_flag) {
+  const uint32_t target = static_cast<uint32_t>(npieces - 1);
+  const uint64_t t0 = clock_cycles();
+  while (ld_acquire_gpu(&p.counters[tile]) < target) {
+    if (*abort_flag) return false;
+    if (clock_cycles() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1u;
+      atomicOr(p.err, kDevErrTimeout);
+      return false;
     }
+    __nanosleep(100);
   }
-  if (tid == 0) p.counters[f.tile] = 0u;  // ready for the next call
+  p.counters[tile] = 0u;  // every other piece has counted in; ready for the next call
+  return true;
+}
+
+// Pieces of tile `tile` (owned by CTA `owner`): the owner's own plus the others'.
+__device__ __forceinline__ int tile_pieces(const Params &p, int tile, int owner) {
+  return owner_of(p, static_cast<int64_t>(tile) * p.KS + p.KS - 1) - owner + 1;
 }
 
 // The weight-stream producer. Producer warp pw (of two) fills the stages i = pw, pw + 2, ... of the

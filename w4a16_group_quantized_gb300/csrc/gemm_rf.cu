@@ -23,8 +23,8 @@
 // rounds (q - z) * s to fp16 per 8 codes, looking the group up per code word.
 //
 // At the end of a tile segment the two warps of a slab add their partials through shared memory
-// (set 0 + set 1: deterministic) and write y, or an fp32 piece of a tile cut between CTAs
-// (the fixup of gemm_common.cuh). This is the split-K-in-the-CTA, stream-K-across-CTAs decode
+// (set 0 + set 1: deterministic) and write y, or an fp32 piece of a tile cut between CTAs; the
+// owner of a cut tile adds the other CTAs' pieces first (gemm_common.cuh). This is the split-K-in-the-CTA, stream-K-across-CTAs decode
 // path; Marlin's register-level dequant into MMA fragments (Marlin post) on sm_103a.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -201,8 +201,9 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[S];
   __shared__ __align__(8) uint64_t empty_bar[S];
+  __shared__ __align__(8) uint64_t own_bar;  // the owner's wait for the other pieces is over
   __shared__ uint32_t abort_sh;
-  __shared__ Fixup fix_sh;
+  __shared__ int npieces_sh;  // pieces of the cut tile the CTA's last segment owns (-1: failed)
 
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   float *red = reinterpret_cast<float *>(smem_raw + (smem_base - smem_u32(smem_raw)) + S * C::kStageBytes);
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), C::kSetWarps);  // one arrival per warp of the stage's set
     }
+    mbar_init(smem_u32(&own_bar), 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -233,6 +235,17 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
   if (warp < C::kConsumerWarp0) {
     produce_stages<BN, S, C::kStageBytes>(&x_map, p, u0, nst, warp, lane, smem_base, full_bar, empty_bar, 0, 1,
                                           abort_flag);
+    // The CTA's last segment owns a cut tile when it holds the tile's first stages but not its last
+    // (gemm_common.cuh). Producer 0, idle once its copies are issued, waits for the tile's other
+    // pieces while the consumers finish, so the owner's epilogue does not wait.
+    const int64_t ulast = u0 + nst - 1;
+    const int64_t lt0 = nst > 0 ? ulast / p.KS * p.KS : 0;
+    if (warp == 0 && lane == 0 && nst > 0 && lt0 >= u0 && ulast < lt0 + p.KS - 1) {
+      const int tile = static_cast<int>(ulast / p.KS);
+      const int np = tile_pieces(p, tile, cta);
+      npieces_sh = wait_pieces(p, tile, np, abort_flag) ? np : -1;
+      mbar_arrive(smem_u32(&own_bar));
+    }
   } else {
     const int cw = warp - C::kConsumerWarp0;
     const int q = (cw >> 2) & 1;                 // stage set: stages of parity q (two warps per SMSP)
@@ -326,8 +339,8 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
       // one decision for all consumer warps: go on together or stop together (never leave a warp
       // waiting at a barrier the others no longer reach)
       if (!named_bar_and(1, 32 * C::kConsumers, ok)) break;  // also: the previous partials were read
-      const int64_t tile_u0 = static_cast<int64_t>(tile) * p.KS;
       const bool whole = ks0 == 0 && seg_len == p.KS;
+      const bool owner = !whole && ks0 == 0;  // holds a cut tile's first stages (the CTA's last segment)
       // the warps of set 1 hand their partial sums to the warp of set 0 of their slab
       float *mine = red + sl * 32 * C::kVals + lane;
       if (q == 1) {
@@ -336,7 +349,11 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) mine[(nb * 4 + cc) * 32] = tot[nb][cc];
       }
-      named_bar_sync(1, 32 * C::kConsumers);
+      bool have_pieces = true;
+      if (owner && tid == 0)
+        have_pieces = mbar_wait(smem_u32(&own_bar), 0, abort_flag, p.err) && npieces_sh > 0;
+      if (!named_bar_and(1, 32 * C::kConsumers, have_pieces)) break;
+      const int npieces = owner ? npieces_sh : 1;
       if (q == 0) {
         const int m0 = (tile % p.MT) * BN;
         const int n0 = (tile / p.MT) * kTN;
@@ -345,10 +362,12 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
         for (int nb = 0; nb < NB8; ++nb) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const float v = tot[nb][c] + mine[(nb * 4 + c) * 32];
+            float v = tot[nb][c] + mine[(nb * 4 + c) * 32];
             const int row = row0 + 8 * (c >> 1);
             const int tok = 8 * nb + 2 * t + (c & 1);
-            if (whole) {
+            for (int pc = 1; pc < npieces; ++pc)  // the owner adds the later pieces in K order
+              v += __ldcg(piece_of<BN, 1>(p, cta + pc, 0) + tok * kTN + row);
+            if (whole || owner) {
               if (n0 + row < p.N && m0 + tok < p.M)
                 p.y[static_cast<int64_t>(m0 + tok) * p.N + n0 + row] = __float2half_rn(v);
             } else {
@@ -357,23 +376,10 @@ __global__ void __launch_bounds__(RfCfg<NB8, MODE>::kThreads, 1)
           }
         }
       }
-      if (!whole) {
-        // the last CTA to finish a piece of this tile adds all pieces in K order and writes y: the
-        // piece stores are ordered (barrier) before one thread's count, an acquire-release atomic;
-        // the thread that sees the last count has acquired the other pieces, and the barrier after
-        // it orders their reads
+      if (!whole && !owner) {
+        // a later piece of a cut tile: its stores are ordered (barrier) before one thread's release count
         named_bar_sync(1, 32 * C::kConsumers);
-        if (tid == 0) {
-          Fixup f;
-          f.c_first = owner_of(p, tile_u0);
-          f.npieces = owner_of(p, tile_u0 + p.KS - 1) - f.c_first + 1;
-          f.slot0 = range_begin(p, f.c_first) != tile_u0 ? 1 : 0;
-          const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile]);
-          f.tile = old == static_cast<uint32_t>(f.npieces - 1) ? tile : -1;
-          fix_sh = f;
-        }
-        named_bar_sync(1, 32 * C::kConsumers);
-        if (fix_sh.tile >= 0) reduce_pieces<BN>(p, fix_sh, tid, 32 * C::kConsumers);
+        if (tid == 0) red_add_release_gpu(&p.counters[tile]);
       }
       zero_acc<NB8>(tot);
       i += seg_len;

@@ -108,14 +108,17 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // ------------------------------------------------------------- inter-CTA counting
 
-// Adds 1 to a global counter with acquire-release semantics at GPU scope and returns the old
-// value. As release it publishes every store ordered before it (the CTA's own, through a preceding
-// barrier: release is cumulative); as acquire it makes the stores other CTAs published before
-// their own count visible to this thread and, through a following barrier, to its CTA.
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *ctr) {
-  uint32_t old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
-  return old;
+// Adds 1 to a global counter with release semantics at GPU scope: every store ordered before it
+// (the CTA's own, through a preceding barrier: release is cumulative) is visible to a thread that
+// reads the new value with acquire semantics.
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *ctr) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // ------------------------------------------------------------- async copies
