@@ -357,6 +357,11 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
     const int lq = warp % 4;  // tensor-memory lane quarter this warp may access
     const int r = lq * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(lq * 32) << 16;
+    // g % 64 == 0 and g dividing the stage's K (or the stage lying in one group): block b's group is
+    // the stage's first plus the same b * 64 / g in every stage, so its record sits at a fixed place
+    constexpr int kStageKHere = C::kSBK * kTK;
+    const bool fixed_rec = kStageKHere % p.g == 0 || p.g % kStageKHere == 0;
+    const uint32_t fixed_rec_off = kStageKHere % p.g == 0 ? (b * kTK) / p.g * kRecBytes : 0u;
     StageIter it;
     it.init(p, u0);
     for (int i = 0; i < nst; ++i, it.advance(p, 1)) {
@@ -375,11 +380,13 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
         const uint4 w1 = lds128(codes + 2048 + r * 16);
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         const int kfirst = (it.ks * C::kSBK + b) * kTK;
-        const int jlo = p.gdiv.div(it.ks * C::kSBK * kTK);
         const uint32_t acol = tmem + lane_addr + C::kACol0 + (d * C::kASlots + i % C::kASlots) * 32;
         tc_fence_after();
         if (MODE != kGeneral) {
-          const uint32_t rec = recs + (p.gdiv.div(kfirst) - jlo) * kRecBytes;  // g % 64 == 0: one group per block
+          // g % 64 == 0: one group per block
+          const uint32_t rec =
+              recs + (fixed_rec ? fixed_rec_off
+                                : (p.gdiv.div(kfirst) - p.gdiv.div(it.ks * kStageKHere)) * kRecBytes);
           const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
           const GroupConsts gc = group_consts(lds16(rec + 2 * r), z);
 #pragma unroll
@@ -390,6 +397,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
             tmem_st_32x32b_x16(acol + 16 * h, out);
           }
         } else {
+          const int jlo = p.gdiv.div(it.ks * kStageKHere);
           int j = p.gdiv.div(kfirst);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
