@@ -562,6 +562,78 @@ def run_prefill(args):
     return 0
 
 
+def run_stack(args):
+    """The decode-stack config: the 225 linears of a random-init 32-layer Llama-2-7B-shaped decoder
+    (q, k, v, o 4096x4096; gate, up 11008x4096; down 4096x11008 per layer; lm_head 32000x4096), all
+    W4A16 g = 128, run back to back on one stream for M in {1, 16, 128} tokens per step (each step one
+    CUDA graph replay; 3.3 GB of packed weights, far beyond L2), beside the same stack with dense fp16
+    weights through torch.matmul. Prints one JSON line with tokens/s."""
+    import torch
+
+    import w4a16_group_quantized_gb300 as w4
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    layers = [L for _ in range(workloads.STACK_LAYERS) for L in workloads.STACK_LAYER] + [workloads.STACK_HEAD]
+    packed, dense = [], []
+    for L in layers:  # weights ~ N(0, 0.02^2) drawn on the device (seeded), quantized by w4_pack
+        W = (torch.randn(L.n, L.k, device=dev, generator=gen) * 0.02).to(torch.float16)
+        qw, sc, zw = w4.w4_pack(W, L.g)
+        packed.append(w4.w4_repack(qw, sc, zw, L.n, L.k, L.g))
+        dense.append(W)
+        del qw, sc, zw
+    torch.cuda.synchronize()
+    wbytes = sum(weight_bytes(L.n, L.k, L.g) for L in layers)
+    stream = torch.cuda.Stream(dev)
+    rows = []
+    for m in workloads.STACK_MS:
+        xs = {k: (torch.randn(m, k, device=dev, generator=gen)).to(torch.float16) for k in {L.k for L in layers}}
+        ys = [torch.empty((m, L.n), dtype=torch.float16, device=dev) for L in layers]
+        ws = torch.zeros(max(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g) for L in layers), dtype=torch.uint8,
+                         device=dev)
+
+        def ours():
+            for L, pk, y in zip(layers, packed, ys):
+                w4.w4a16_gemm(xs[L.k], pk, L.n, L.k, L.g, y=y, workspace=ws)
+
+        def theirs():
+            for L, W, y in zip(layers, dense, ys):
+                torch.matmul(xs[L.k], W.t(), out=y)
+
+        res = {}
+        for name, fn in (("w4a16", ours), ("dense_fp16", theirs)):
+            with torch.cuda.stream(stream):
+                fn()
+            stream.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    gr.replay()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    gr.replay()
+                e1.record(stream)
+            stream.synchronize()
+            res[name] = e0.elapsed_time(e1) / args.steps
+            del gr
+        assert w4.w4_last_device_error(ws) == 0
+        rows.append({"M": m, "ms_per_step": round(res["w4a16"], 4), "tokens_per_s": round(m / (res["w4a16"] * 1e-3), 1),
+                     "weight_gbs": round(wbytes / (res["w4a16"] * 1e-3) / 1e9, 1),
+                     "dense_ms_per_step": round(res["dense_fp16"], 4),
+                     "dense_tokens_per_s": round(m / (res["dense_fp16"] * 1e-3), 1),
+                     "speedup_vs_dense": round(res["dense_fp16"] / res["w4a16"], 3)})
+        del xs, ys, ws
+    print(json.dumps({"stack": rows, "gemms_per_step": len(layers), "packed_weight_bytes": wbytes,
+                      "timing": f"one CUDA graph per step, {args.steps} replays after {args.warmup} warm-ups, "
+                                "CUDA events; weights stream from HBM (3.3 GB packed, 13 GB dense)"}))
+    return 0
+
+
 def run_case(args):
     """One GEMM configuration launched --steps times (for focused profiling); prints a short JSON line."""
     import torch
@@ -608,6 +680,7 @@ def main():
     ap.add_argument("--no-dense", action="store_true", help="skip the dense fp16 comparison")
     ap.add_argument("--case", default=None, help="M:layer_name - run only that GEMM (for profiling)")
     ap.add_argument("--prefill", action="store_true", help="time the prefill config instead of the decode step")
+    ap.add_argument("--stack", action="store_true", help="time the 225-GEMM decode stack instead of the decode step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
@@ -616,6 +689,8 @@ def main():
         return run_case(args)
     if args.prefill:
         return run_prefill(args)
+    if args.stack:
+        return run_stack(args)
     return run_gpu(args)
 
 
