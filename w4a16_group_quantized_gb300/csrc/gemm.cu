@@ -679,7 +679,14 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
                     int num_sms, GemmPlan *plan) {
   (void)g;
   int bn = block_n;
-  if (bn == 0) bn = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  if (bn == 0) {
+    bn = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    // 65..128 tokens on a layer with fewer 128-row weight tiles than SMs: two token tiles of 64
+    // give twice the output tiles (cut less often) at one extra, mostly L2-served, pass over the
+    // weights; measured faster on the 4096- to 12288-row 7B layers, slower on the 22016-row one
+    const int sms = num_sms > 0 ? num_sms : 148;
+    if (bn == 128 && M <= 128 && cdiv(N, kTN) < sms) bn = 64;
+  }
   if (bn != 8 && bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
   // Units of two weight tiles and 128-wide K stages for block_n 128 from M = 256 up (two or more
