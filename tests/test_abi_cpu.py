@@ -76,6 +76,23 @@ def test_workspace_sizes(lib):
     assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 16, 0, 3) == 0  # no schedule 3
 
 
+def test_automatic_block_n(lib):
+    # 65..128 tokens: block_n 64 (two token tiles) on layers with fewer 128-row weight tiles than
+    # SMs, else 128; the workspace size shows the choice (stream-K, 100 CTAs: two fp32 partial
+    # tiles of 128 x block_n per CTA, one counter per output tile)
+    P = 100
+    b = w4.w4a16_workspace_bytes_ex(128, 4096, 4096, 128, 0, P, 1)  # 32 weight tiles
+    assert b == 256 + 256 + P * 2 * 128 * 64 * 4
+    b = w4.w4a16_workspace_bytes_ex(96, 12288, 4096, 128, 0, P, 1)  # 96 weight tiles
+    assert b == 256 + 768 + P * 2 * 128 * 64 * 4  # 2 x 96 counters
+    b = w4.w4a16_workspace_bytes_ex(128, 22016, 4096, 128, 0, P, 1)  # 172 weight tiles
+    assert b == 256 + 768 + P * 2 * 128 * 128 * 4
+    b = w4.w4a16_workspace_bytes_ex(200, 4096, 4096, 128, 0, P, 1)  # more than 128 tokens
+    assert b == 256 + 256 + P * 2 * 128 * 128 * 4
+    b = w4.w4a16_workspace_bytes_ex(8, 4096, 4096, 128, 0, P, 1)  # the decode kernel's 8-token tiles
+    assert b == 256 + 256 + P * 2 * 128 * 8 * 4
+
+
 def _vp(v):
     return ctypes.c_void_p(v)
 
