@@ -1,31 +1,34 @@
-// w4a16_gemm: y[M,N] = x[M,K] . dequant(Wq)[N,K]^T on sm_103a tensor cores.
+// w4a16_gemm: y[M,N] = x[M,K] . dequant(Wq)[N,K]^T on sm_103a tensor cores (M >= 9; the
+// register-operand decode kernel, gemm_rf.cu, takes M <= 8).
 //
 // Output tiles are 128 (weight rows n) x BN (activation rows m) tiles of y^T
 // ("swap-AB": the weights sit on the MMA's M = 128 side, the tokens on its N
-// side, so a batch of 1..16 tokens still fills an MMA). The kernel is
-// persistent: one CTA per SM walks a contiguous range of (tile, 256-wide K
-// stage) units, so the work is split evenly whatever the number of tiles
-// (stream-K); a tile cut between CTAs is finished by a fixup (below).
+// side, so a decode batch still fills an MMA). The kernel is persistent: one
+// CTA per SM walks its units (tile, K stage) -- a contiguous range (stream-K,
+// so the work is split evenly whatever the number of tiles) or whole tiles
+// dealt out round-robin (gemm_common.cuh).
 //
-// A stage is four 64-wide K blocks of one tile: 16 KB of 4-bit codes, the
-// group records they need and the four x sub-tiles, moved by three copies
-// (one thread can issue a bulk copy only every ~350 cycles, so copies are
-// made large). Warp roles (one CTA per SM):
+// A stage is four 64-wide K blocks of one tile, or (TP = 2: BN = 128 from
+// M = 256) two K blocks of two weight tiles sharing one x tile: 16 KB of 4-bit
+// codes, the group records they need and the x sub-tiles, moved by three
+// copies (one thread can issue a bulk copy only every ~350 cycles, so copies
+// are made large). Warp roles (one CTA per SM):
 //   2 producer warps take the stages in turn (lane 0 issues): a TMA tensor
 //                   copy of x (128-byte swizzle, zero fill outside [M, K]) and
-//                   two bulk copies (codes, group records) on the stage's mbarrier.
-//   4 dequant warpgroups: group d turns K block d of every stage into fp16
+//                   two copies (codes, group records) on the stage's mbarrier.
+//   4 dequant warpgroups: group d turns A block d of every stage into fp16
 //                   w = (q - z) * s in tensor memory (thread r owns weight row
 //                   r; tcgen05.st), the MMA's A operand; shared memory only
 //                   holds 4-bit codes. A group never waits for the MMAs of its
 //                   own block, only for its tensor-memory slots to come free.
-//   4 MMA warps (2 for BN = 128; lane 0 issues): warp e issues the MMAs of its K
+//   4 MMA warps (2 for BN = 128; lane 0 issues): warp e issues the MMAs of its
 //                   block(s) of every stage into its own accumulator and commits
 //                   once per stage (a thread issues a tcgen05.mma only every
 //                   ~50-130 cycles, so the issue is spread over several warps).
 //   1 epilogue warpgroup: adds the MMA warps' accumulators of a finished tile
-//                   segment in a fixed order and writes y, or an fp32 partial
-//                   tile when the tile was cut between CTAs.
+//                   segment in a fixed order (TP = 1; with TP = 2 each MMA warp
+//                   owns one weight tile) and writes y, or an fp32 piece when
+//                   the tile was cut between CTAs.
 // When g is not a multiple of 64 the dequant looks the group up per 8 codes.
 //
 // This is the GB300 form of the techniques the Marlin post lists (prefetch,

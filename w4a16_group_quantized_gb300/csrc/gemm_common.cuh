@@ -1,6 +1,6 @@
-// Pieces shared by the GEMM kernels: the schedule (persistent stream-K over (tile, 256-wide K
-// stage) units), the weight-stream producer, the fp16 dequant of 8 packed codes, bounded waits and
-// the fixup of tiles cut between CTAs.
+// Pieces shared by the GEMM kernels: the schedule (persistent CTAs over (tile, K stage) units:
+// stream-K ranges or round-robin whole tiles), the one-tile weight-stream producer, the fp16
+// dequant of 8 packed codes, bounded waits and the owner-reduces finish of tiles cut between CTAs.
 #pragma once
 
 #include <cuda.h>
