@@ -73,6 +73,23 @@ def gemm_flops(m, n, k):
     return 2.0 * m * n * k
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's value (a job's time is its slowest rank's); value itself
+    without a process group."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job throughput of `world` replicas that each ran `steps` steps in (at most) total_ms."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def dom_traffic():
     """DRAM bytes per launch of the dominant kernel from the committed ncu capture, or None when the
     kernel's sources changed since the counters were taken (their SHA-256 is stored beside them)."""
@@ -334,13 +351,11 @@ def run_gpu(args):
     torch.cuda.synchronize()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     dom_ms = sum(s.elapsed_time(e) for s, e in zip(starts, mids)) / args.steps
+    dom_ms = max_over_ranks(dom_ms, dist, dev)
     total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, args.steps, total_ms)
     clocks = clk.summary()
 
     # ---- per-(M, layer): back-to-back launches over rotating copies, captured as one graph each
@@ -416,11 +431,8 @@ def run_gpu(args):
         e1.record(stream)
     stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = job_tflops(world, flops_step, args.steps, e2e_ms)
 
     # ---- dense fp16 torch.matmul on the same shapes (cuBLAS), for comparison
     dense = None
