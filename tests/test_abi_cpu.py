@@ -93,6 +93,17 @@ def test_automatic_block_n(lib):
     assert b == 256 + 256 + P * 2 * 128 * 8 * 4
 
 
+def test_grid_shrinks_to_the_piece_bound(lib):
+    # one weight tile of 16 K stages: stream-K over more than 8 CTAs would cut it into more than 8
+    # pieces, so the planner shrinks the grid to 8 CTAs (8 x two 128 x 8 fp32 partial tiles)
+    for schedule in (0, 1):
+        assert w4.w4a16_workspace_bytes_ex(8, 128, 4096, 128, 0, 0, schedule) == 256 + 256 + 8 * 2 * 128 * 8 * 4
+    # two-tile units (M >= 256, block_n 128): 4 token tiles x 4 tile pairs = 16 output tiles over
+    # 10 CTAs, not a multiple: stream-K with partial tiles of 2 x 128 x 128 fp32
+    b = w4.w4a16_workspace_bytes_ex(512, 1024, 1024, 128, 128, 10, 0)
+    assert b == 256 + 256 + 10 * 2 * 2 * 128 * 128 * 4
+
+
 def _vp(v):
     return ctypes.c_void_p(v)
 
