@@ -166,7 +166,9 @@ W4_API int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g,
  * Reads and clears the device error word that GEMM kernels write into the
  * workspace. SYNCHRONISES `stream`. Returns W4_OK, W4_ERR_TIMEOUT (a
  * pipeline wait inside a kernel gave up after about a second and the kernel
- * returned early; y is then undefined) or W4_ERR_CUDA.
+ * returned early; y is then undefined, and so are the workspace's tile
+ * counters: zero the whole workspace before the next GEMM uses it) or
+ * W4_ERR_CUDA.
  */
 W4_API int w4_last_device_error(void *workspace_dev, void *stream);
 

@@ -205,6 +205,7 @@ def w4a16_gemm_ex(x, packed, N, K, g, block_n: int = 0, ctas: int = 0, schedule:
 
 
 def w4_last_device_error(workspace, stream=None) -> int:
-    """Reads and clears the workspace's device error word (synchronises the stream)."""
+    """Reads and clears the workspace's device error word (synchronises the stream). After
+    W4_ERR_TIMEOUT the workspace's tile counters are undefined too: zero it before reuse."""
     ws = workspace.buf if isinstance(workspace, Workspace) else workspace
     return int(load().w4_last_device_error(_dev(ws, "workspace"), _stream(stream)))
