@@ -10,8 +10,9 @@ activations ~ N(0, 1)), resident in HBM before the timed region.
 
 The step is captured as two CUDA graphs (host launch cost is larger than a
 decode GEMM), the M <= 8 GEMMs first: CUDA events around each graph time the
-step and, inside it, the dominant kernel (the register-operand decode kernel)
-whose roofline is reported. Each layer has three weight copies used in turn
+step and, inside it, the dominant kernel (the decode kernel: register-operand
+MMAs, K split across the CTAs of a thread-block cluster) whose roofline is
+reported. Each layer has three weight copies used in turn
 inside a step and L2 is flushed (a write of a buffer larger than L2) between
 timed replays, so weights stream from HBM. Prints one JSON line.
 
@@ -50,8 +51,8 @@ L2_FLUSH_BYTES = 512 << 20
 # The step's dominant kernel by device time: the register-operand decode kernel, which runs the
 # GEMMs with M <= DOM_M (12 of the 28 launches); its roofline is reported, timed inside the step.
 DOM_M = 8
-DOM_KERNEL = "w4a16_gemm_rf_kernel"
-DOM_SOURCES = ("gemm_rf.cu", "gemm_common.cuh", "ptx.cuh")
+DOM_KERNEL = "w4a16_gemm_dec_kernel"
+DOM_SOURCES = ("gemm_dec.cu", "gemm_common.cuh", "ptx.cuh")
 TRAFFIC_FILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "decode_kernel_traffic.json")
 
 
@@ -332,8 +333,7 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    uuid = str(getattr(props, "uuid", "") or "")
-    gpu_id = ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(torch.cuda.current_device())
+    gpu_id = gpu_uuid(dev)
     with ClockSampler(gpu_id) as clk:
         torch.cuda.nvtx.range_push("w4a16_timed")
         with torch.cuda.stream(stream):
@@ -476,6 +476,9 @@ def run_gpu(args):
                "sample": "the whole decode sweep (28 GEMMs) through the fp64 oracle, timed once",
                "seconds": round(t, 2)}
 
+    # ---- the prefill config (M >= 256 on the 70B shapes), with its own clock record
+    prefill = None if args.no_prefill else prefill_block(args, dev, gpu_id, peaks)
+
     dom = [(m, L) for m, L in sweep() if m <= DOM_M]
     dom_bytes = sum(alg_bytes(m, L.n, L.k, L.g) for m, L in dom)
     dom_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9  # = bytes per average launch / its average duration
@@ -513,6 +516,7 @@ def run_gpu(args):
         "dense_fp16": dense,
         "offline": offline,
         "per_launch": per,
+        "prefill": prefill,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -521,56 +525,87 @@ def run_gpu(args):
     return 0
 
 
-def run_prefill(args):
+def prefill_block(args, dev, gpu_id, peaks):
     """The prefill config: M in {256, 512, 1024, 4096} x the four Llama-2-70B-shaped layers (g = 128,
-    outlier activations), each GEMM launched back to back (CUDA events, after warm-up) beside a dense
-    fp16 torch.matmul of the same shape; prints one JSON line with TFLOP/s and the fraction of the
-    measured bf16 tensor peak."""
+    1 % outlier channels x20 in the activations). Each GEMM is launched back to back over rotating
+    weight copies (more than 2.2x L2 of packed bytes, so weights come from HBM), CUDA events after
+    warm-up, beside a dense fp16 torch.matmul of the same shape; SM clocks and throttle reasons are
+    sampled over the whole timed region. Weights are drawn on the device (seeded) and quantized by
+    w4_pack / w4_repack. Returns the block for the JSON line."""
     import torch
 
     import w4a16_group_quantized_gb300 as w4
 
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    peaks = load_peaks()
-    reps = max(3, args.steps // 2)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 << 20) or (126 << 20))
+    reps = max(3, args.prefill_reps)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(workloads.SEED_W)
 
-    def timed(fn):
-        for _ in range(args.warmup):
-            fn()
+    def timed(fn, nrot):
+        for i in range(args.warmup):
+            fn(i % nrot)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(reps):
-            fn()
+        for i in range(reps):
+            fn(i % nrot)
         e1.record()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e-3 / reps
 
     rows = []
-    for L in workloads.PREFILL_LAYERS:
-        W = torch.from_numpy(workloads.weights_f16(L.n, L.k)).to(dev)
-        qw, sc, zw = w4.w4_pack(W, L.g)
-        packed = w4.w4_repack(qw, sc, zw, L.n, L.k, L.g)
-        del qw, sc, zw
-        for m in workloads.PREFILL_MS:
-            x = torch.from_numpy(workloads.activations_f16(m, L.k, outliers=True)).to(dev)
-            y = torch.empty((m, L.n), dtype=torch.float16, device=dev)
-            ws = torch.zeros(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g), dtype=torch.uint8, device=dev)
-            t = timed(lambda: w4.w4a16_gemm(x, packed, L.n, L.k, L.g, y=y, workspace=ws))
-            assert w4.w4_last_device_error(ws) == 0
-            td = timed(lambda: torch.matmul(x, W.t()))
-            f = gemm_flops(m, L.n, L.k)
-            bn, ctas, sched = w4.w4a16_gemm_plan(m, L.n, L.k, L.g)
-            rows.append({"M": m, "layer": L.name, "us": round(t * 1e6, 2), "tflops": round(f / t / 1e12, 1),
-                         "tensor_frac": round(f / t / 1e12 / peaks["bf16_tflops"], 3),
-                         "dense_us": round(td * 1e6, 2), "dense_tflops": round(f / td / 1e12, 1),
-                         "block_n": bn, "ctas": ctas, "schedule": "stream-K" if sched == 1 else "whole tiles"})
-            del x, y, ws
-        del W, packed
-    print(json.dumps({"prefill": rows, "peak_tflops": peaks["bf16_tflops"],
-                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst)",
-                      "timing": f"{reps} back-to-back launches after {args.warmup} warm-ups, CUDA events"}))
+    with ClockSampler(gpu_id) as clk:
+        for L in workloads.PREFILL_LAYERS:
+            W = (torch.randn(L.n, L.k, device=dev, generator=gen, dtype=torch.float32) * 0.02).to(torch.float16)
+            qw, sc, zw = w4.w4_pack(W, L.g)
+            packed = w4.w4_repack(qw, sc, zw, L.n, L.k, L.g)
+            del qw, sc, zw
+            nb = weight_bytes(L.n, L.k, L.g)
+            pk = [packed] + [packed.clone() for _ in range(max(1, math.ceil(2.2 * l2 / nb)) - 1)]
+            dn = [W] + [W.clone() for _ in range(max(1, math.ceil(2.2 * l2 / (2 * L.n * L.k))) - 1)]
+            for m in workloads.PREFILL_MS:
+                x = torch.from_numpy(workloads.activations_f16(m, L.k, outliers=True)).to(dev)
+                y = torch.empty((m, L.n), dtype=torch.float16, device=dev)
+                ws = torch.zeros(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g), dtype=torch.uint8, device=dev)
+                t = timed(lambda i: w4.w4a16_gemm(x, pk[i], L.n, L.k, L.g, y=y, workspace=ws), len(pk))
+                assert w4.w4_last_device_error(ws) == 0
+                td = timed(lambda i: torch.matmul(x, dn[i].t(), out=y), len(dn))
+                f = gemm_flops(m, L.n, L.k)
+                bn, ctas, sched = w4.w4a16_gemm_plan(m, L.n, L.k, L.g)
+                rows.append({"M": m, "layer": L.name, "us": round(t * 1e6, 2), "tflops": round(f / t / 1e12, 1),
+                             "weight_gbs": round(nb / t / 1e9, 1),
+                             "tensor_frac": round(f / t / 1e12 / peaks["bf16_tflops"], 3),
+                             "dense_us": round(td * 1e6, 2), "dense_tflops": round(f / td / 1e12, 1),
+                             "vs_dense": round(td / t, 3),
+                             "block_n": bn, "ctas": ctas, "schedule": "stream-K" if sched == 1 else "whole tiles"})
+                del x, y, ws
+            del W, packed, pk, dn
+            torch.cuda.empty_cache()
+    big = [r for r in rows if r["M"] >= 512]
+    return {"rows": rows, "peak_tflops": peaks["bf16_tflops"],
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst)",
+            "min_tensor_frac_m_ge_512": min(r["tensor_frac"] for r in big),
+            "clocks": clk.summary(),
+            "timing": f"{reps} back-to-back launches over rotating weight copies (> 2.2x L2) after "
+                      f"{args.warmup} warm-ups, CUDA events"}
+
+
+def gpu_uuid(dev):
+    import torch
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    return ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(dev.index or 0)
+
+
+def run_prefill(args):
+    """Only the prefill block (bench.py --prefill): prints one JSON line."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    print(json.dumps({"prefill": prefill_block(args, dev, gpu_uuid(dev), load_peaks())}))
     return 0
 
 
@@ -600,6 +635,7 @@ def run_stack(args):
     wbytes = sum(weight_bytes(L.n, L.k, L.g) for L in layers)
     stream = torch.cuda.Stream(dev)
     rows = []
+    clk = ClockSampler(gpu_uuid(dev)).__enter__()
     for m in workloads.STACK_MS:
         xs = {k: (torch.randn(m, k, device=dev, generator=gen)).to(torch.float16) for k in {L.k for L in layers}}
         ys = [torch.empty((m, L.n), dtype=torch.float16, device=dev) for L in layers]
@@ -640,7 +676,9 @@ def run_stack(args):
                      "dense_tokens_per_s": round(m / (res["dense_fp16"] * 1e-3), 1),
                      "speedup_vs_dense": round(res["dense_fp16"] / res["w4a16"], 3)})
         del xs, ys, ws
-    print(json.dumps({"stack": rows, "gemms_per_step": len(layers), "packed_weight_bytes": wbytes,
+    clk.__exit__(None, None, None)
+    print(json.dumps({"stack": rows, "clocks": clk.summary(), "gemms_per_step": len(layers),
+                      "packed_weight_bytes": wbytes,
                       "timing": f"one CUDA graph per step, {args.steps} replays after {args.warmup} warm-ups, "
                                 "CUDA events; weights stream from HBM (3.3 GB packed, 13 GB dense)"}))
     return 0
@@ -693,6 +731,8 @@ def main():
     ap.add_argument("--case", default=None, help="M:layer_name - run only that GEMM (for profiling)")
     ap.add_argument("--prefill", action="store_true", help="time the prefill config instead of the decode step")
     ap.add_argument("--stack", action="store_true", help="time the 225-GEMM decode stack instead of the decode step")
+    ap.add_argument("--no-prefill", action="store_true", help="leave the prefill block out of the default line")
+    ap.add_argument("--prefill-reps", type=int, default=6, help="timed launches per prefill GEMM")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

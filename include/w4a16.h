@@ -155,6 +155,58 @@ W4_API size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t 
                                 int32_t block_n, int32_t ctas, int32_t schedule);
 
 /*
+ * Options of w4a16_gemm_opts. Zero-initialise the struct (every zero field
+ * means "automatic" / "off"), then set what you need.
+ *
+ * kernel     0 automatic (the decode kernel for M <= 8, else the tensor-memory
+ *            kernel); 1 the decode kernel (register-operand tensor-core MMAs,
+ *            M <= 16; the K range of every weight tile may be split between
+ *            the CTAs of a thread-block cluster and reduced in distributed
+ *            shared memory, so its workspace is the 256-byte error word
+ *            alone); 2 the tensor-memory kernel (tcgen05, any M).
+ * block_n    tokens per output tile, 0 automatic: decode kernel 8 or 16
+ *            (M <= block_n); tensor-memory kernel 16, 32, 64 or 128.
+ * ctas       0 automatic. Tensor-memory kernel: persistent CTAs (1..65535).
+ *            Decode kernel: clusters (each takes the weight tiles q, q + ctas,
+ *            ...).
+ * schedule   tensor-memory kernel: 0 automatic, 1 stream-K (a tile may be cut
+ *            along K between CTAs and finished through the workspace), 2 whole
+ *            tiles per CTA.
+ * cluster    decode kernel: CTAs per cluster that split each tile along K:
+ *            0 automatic, 1, 2, 4 or 8 (at most the tile's number of 256-wide
+ *            K stages, ceil(K / 256)).
+ * flags      W4_FLAG_WEIGHTS_STATIC: the caller states that the kernel
+ *            launched just before this call on `stream` does not write the
+ *            packed weights (true once a model is loaded). The decode kernel
+ *            then starts copying its first weight tiles before that kernel
+ *            has finished; x is still read only after it.
+ * wait_limit_cycles  0: about 1.5 s. A pipeline wait inside the kernels gives
+ *            up after this many SM clock cycles, sets the workspace error
+ *            word (W4_ERR_TIMEOUT from w4_last_device_error) and the kernel
+ *            returns early. For tests of that path.
+ */
+#define W4_FLAG_WEIGHTS_STATIC 1u
+typedef struct {
+    int32_t kernel;
+    int32_t block_n;
+    int32_t ctas;
+    int32_t schedule;
+    int32_t cluster;
+    uint32_t flags;
+    uint64_t wait_limit_cycles;
+} w4a16_options;
+
+/* w4a16_gemm with options (NULL = all automatic). The workspace must be at
+ * least w4a16_workspace_bytes_opts(M, N, K, g, opts) bytes. Results are
+ * identical up to fp32 summation order across options; for fixed options
+ * they are deterministic run to run on one device. */
+W4_API int w4a16_gemm_opts(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K,
+                           int32_t g, void *y_dev, void *workspace_dev, size_t workspace_bytes,
+                           const w4a16_options *opts, void *stream);
+W4_API size_t w4a16_workspace_bytes_opts(int64_t M, int64_t N, int64_t K, int32_t g,
+                                         const w4a16_options *opts);
+
+/*
  * The schedule w4a16_gemm picks on the current device: writes block_n, the
  * number of CTAs and the schedule (1 stream-K, 2 whole tiles).
  * Returns W4_OK or an error status.
@@ -177,24 +229,24 @@ W4_API int w4_last_device_error(void *workspace_dev, void *stream);
  * memory. The pages have no counterpart to this call; it exists for users of
  * this library.
  *
- * Some callers have no way to hand the GEMM a workspace: code that runs while
- * a stream is being captured into a CUDA graph (cudaMalloc is refused there
- * and cudaFree would synchronise the device), engines that plan every device
- * buffer up front and give kernels no scratch, and plug-ins that only see
- * their input and output tensors. This call takes the same inputs and output
- * as w4a16_gemm (same checks, same automatic schedule, same results) but keeps
- * its scratch -- the error word, the per-tile counters and the fp32 partial
- * tiles of tiles split between CTAs -- in a device array inside the library,
- * W4A16_NOALLOC_SCRATCH_BYTES long. It calls no cudaMalloc, cudaFree or other
- * allocating routine.
+ * Some callers have no way to hand the GEMM a workspace: inference engines
+ * that reserve all device memory when they start and give each kernel only
+ * its inputs and outputs, and plug-ins running inside such engines, which see
+ * their input and output tensors but no allocator. This call takes the same
+ * inputs and output as w4a16_gemm (same checks, same automatic schedule, same
+ * results, bit for bit) but keeps its scratch -- the error word, the per-tile
+ * counters and the fp32 partial tiles of tiles split between CTAs -- in a
+ * device array inside the library, W4A16_NOALLOC_SCRATCH_BYTES long. It calls
+ * no cudaMalloc, cudaFree or other allocating routine.
  *
  *  - Every GPU on which the library is loaded holds that array until the
  *    process exits.
- *  - A problem whose workspace would not fit
- *    (w4a16_workspace_bytes(M, N, K, g) > W4A16_NOALLOC_SCRATCH_BYTES; on
- *    GB300 that is M > 32, unless the layer has at least 8 output tiles of
- *    128 rows x 128 tokens per SM) is refused with W4_ERR_WORKSPACE_TOO_SMALL
- *    before anything is enqueued.
+ *  - A problem is refused with W4_ERR_WORKSPACE_TOO_SMALL, before anything is
+ *    enqueued, exactly when w4a16_workspace_bytes(M, N, K, g) >
+ *    W4A16_NOALLOC_SCRATCH_BYTES. For example, on GB300 (152 SMs) a layer
+ *    of N <= 10^6 rows fits for every M <= 32 (at most 4.8 MB of partial
+ *    tiles plus 4 bytes per output tile), while M = 64 on a 4096 x 4096
+ *    layer needs 9.5 MB and is refused.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture begins.

@@ -89,19 +89,40 @@ def test_automatic_block_n(lib):
     assert b == 256 + 768 + P * 2 * 128 * 128 * 4
     b = w4.w4a16_workspace_bytes_ex(200, 4096, 4096, 128, 0, P, 1)  # more than 128 tokens
     assert b == 256 + 256 + P * 2 * 128 * 128 * 4
-    b = w4.w4a16_workspace_bytes_ex(8, 4096, 4096, 128, 0, P, 1)  # the decode kernel's 8-token tiles
-    assert b == 256 + 256 + P * 2 * 128 * 8 * 4
+    # the decode kernel (8-token tiles) reduces its split along K in distributed shared memory: its
+    # workspace is the error word alone
+    assert w4.w4a16_workspace_bytes_ex(8, 4096, 4096, 128, 0, P, 1) == 256
+    assert w4.w4a16_workspace_bytes(1, 22016, 4096, 128) == 256
 
 
 def test_grid_shrinks_to_the_piece_bound(lib):
     # one weight tile of 16 K stages: stream-K over more than 8 CTAs would cut it into more than 8
     # pieces, so the planner shrinks the grid to 8 CTAs (8 x two 128 x 8 fp32 partial tiles)
     for schedule in (0, 1):
-        assert w4.w4a16_workspace_bytes_ex(8, 128, 4096, 128, 0, 0, schedule) == 256 + 256 + 8 * 2 * 128 * 8 * 4
+        assert w4.w4a16_workspace_bytes_ex(16, 128, 4096, 128, 16, 0, schedule) == 256 + 256 + 8 * 2 * 128 * 16 * 4
     # two-tile units (M >= 256, block_n 128): 4 token tiles x 4 tile pairs = 16 output tiles over
     # 10 CTAs, not a multiple: stream-K with partial tiles of 2 x 128 x 128 fp32
     b = w4.w4a16_workspace_bytes_ex(512, 1024, 1024, 128, 128, 10, 0)
     assert b == 256 + 256 + 10 * 2 * 2 * 128 * 128 * 4
+
+
+def test_options_validation(lib):
+    O = w4.Options
+    # the decode kernel: up to 16 tokens (block_n 8 or 16, M <= block_n); clusters of 1, 2, 4 or 8 CTAs,
+    # at most the number of 256-wide K stages of a tile
+    assert w4.w4a16_workspace_bytes_opts(16, 4096, 4096, 128, O(1, 16, 0, 0, 4, 0, 0)) == 256
+    assert w4.w4a16_workspace_bytes_opts(9, 4096, 4096, 128, O(1, 8, 0, 0, 0, 0, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(17, 4096, 4096, 128, O(1, 0, 0, 0, 0, 0, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(1, 32, 0, 0, 0, 0, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(1, 8, 0, 0, 3, 0, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 1024, 128, O(1, 8, 0, 0, 8, 0, 0)) == 0  # 4 K stages
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 1024, 128, O(1, 8, 0, 0, 4, 0, 0)) == 256
+    # the tensor-memory kernel takes no 8-token tiles; unknown flags and kernels are refused
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(2, 8, 0, 0, 0, 0, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(2, 16, 4, 1, 0, 0, 0)) == 256 + 256 + 4 * 2 * 128 * 16 * 4
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 2, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(3, 0, 0, 0, 0, 0, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 1, 0)) == 256
 
 
 def _vp(v):

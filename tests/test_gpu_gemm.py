@@ -59,6 +59,30 @@ def check(M, N, K, g, block_n=0, ctas=0, schedule=0, rows=None, outliers=False, 
                                    f"M={M} N={N} K={K} g={g} bn={block_n} ctas={ctas} schedule={schedule}")
 
 
+def _dec_clusters(K, M):
+    """Cluster sizes the decode kernel takes for this K and M: at most the number of 256-wide K stages,
+    and enough CTAs that each one's K range of x (M rows of 512 bytes per stage, at most 48 stages)
+    fits its 96 KB of shared memory."""
+    stages = -(-K // 256)
+    per_cta_max = min(48, 96 * 1024 // (512 * M))
+    return [c for c in (1, 2, 4, 8) if c <= stages and -(-stages // c) <= per_cta_max]
+
+
+def check_opts(M, N, K, g, rows=None, outliers=False, seed_x=1, **opts):
+    """As check, through w4a16_gemm_opts with the given options."""
+    qw, s, zw, packed, wn = layer(N, K, g)
+    x = workloads.activations_f16(M, K, seed=seed_x, outliers=outliers)
+    ws = w4.Workspace()
+    y = w4.w4a16_gemm_opts(torch.from_numpy(x).cuda(), packed, N, K, g, workspace=ws, **opts)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_error(ws) == 0
+    if rows is None:
+        rows = np.arange(M)
+    yref = oracle.gemm(x, qw, s, zw, N, K, g, rows=rows)
+    tol = gemm_tolerance(x[rows], wn)
+    return assert_within_tolerance(y.cpu().numpy()[rows], yref, tol, f"M={M} N={N} K={K} g={g} {opts}")
+
+
 # ------------------------------------------------------------ small, every element
 
 
@@ -83,8 +107,10 @@ def test_tile_edges(M):
 @pytest.mark.parametrize("ctas,schedule", [(1, 1), (2, 1), (3, 1), (7, 1), (13, 1), (64, 1), (1, 2), (5, 2)])
 def test_forced_schedules(block_n, ctas, schedule):
     # 3 n-tiles x 8 K stages (x m-tiles): stream-K cuts tiles at many places, incl. one CTA holding
-    # the tail of one tile and the head of the next, and CTAs whose whole range sits inside one tile
-    check(20, 260, 2048, 128, block_n=block_n, ctas=ctas, schedule=schedule)
+    # the tail of one tile and the head of the next, and CTAs whose whole range sits inside one tile.
+    # block_n 8 is the decode kernel (at most 8 tokens): ctas counts its clusters, schedule 2 runs
+    # whole tiles, schedule 1 splits tiles along K between the CTAs of a cluster.
+    check(20 if block_n > 8 else 8, 260, 2048, 128, block_n=block_n, ctas=ctas, schedule=schedule)
 
 
 @pytest.mark.parametrize("M,N,K,g,ctas,schedule", [
@@ -125,6 +151,48 @@ def test_group_sizes(g):
     check(100, 200, 1000, g, block_n=128, ctas=3, schedule=1)
 
 
+@pytest.mark.parametrize("block_n", [8, 16])
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+def test_decode_kernel_clusters(block_n, cluster):
+    # The decode kernel splits each weight tile's K stages between the CTAs of a cluster and sums the
+    # partials in distributed shared memory. N = 300: three weight tiles, the last one 44 rows;
+    # K = 2048: eight 256-wide stages, split 1, 2, 4 or 8 ways. ctas = 1: one cluster takes all three
+    # tiles in turn (three reductions through the same slots); ctas = 2: rounds of unequal count.
+    for M in sorted({1, 5, block_n}):
+        for ctas in (0, 1, 2):
+            check_opts(M, 300, 2048, 128, kernel=1, block_n=block_n, cluster=cluster, ctas=ctas)
+
+
+@pytest.mark.parametrize("g", [8, 24, 40, 64, 128, 192, 256, 512, 1024])
+@pytest.mark.parametrize("cluster", [1, 4])
+def test_decode_kernel_group_modes(g, cluster):
+    # g % 256 == 0: a stage lies in one group; g == 128: two groups per stage; other multiples of 64:
+    # one group per 64-wide block; any other g: (q - z) * s per 8 codes. K = 1000: a partial last group,
+    # a last stage of 4 blocks whose last block is ragged (K % 64 != 0: x comes in per-block copies).
+    check_opts(7, 200, 1000, g, kernel=1, block_n=8, cluster=cluster)
+    check_opts(13, 200, 1000, g, kernel=1, block_n=16, cluster=cluster)
+
+
+@pytest.mark.parametrize("M,N,K,g,block_n", [(1, 4096, 4096, 128, 8), (8, 12288, 4096, 128, 8),
+                                             (16, 4096, 11008, 128, 16), (3, 700, 960, 64, 8),
+                                             (11, 288, 288, 256, 16)])
+def test_decode_kernel_weights_static(M, N, K, g, block_n):
+    # W4_FLAG_WEIGHTS_STATIC: the first stages' weight copies start before the previous grid is
+    # waited for; results must not change, launch after launch
+    rows = _sample_rows(M, 16)
+    for cluster in [0] + _dec_clusters(K, M):
+        check_opts(M, N, K, g, rows=rows, kernel=1, block_n=block_n, cluster=cluster, flags=w4.FLAG_WEIGHTS_STATIC)
+    qw, s, zw, packed, wn = layer(N, K, g)
+    x = torch.from_numpy(workloads.activations_f16(M, K)).cuda()
+    ws = w4.Workspace()
+    first = w4.w4a16_gemm_opts(x, packed, N, K, g, kernel=1, block_n=block_n, workspace=ws)
+    for _ in range(20):
+        y = w4.w4a16_gemm_opts(x, packed, N, K, g, kernel=1, block_n=block_n, flags=w4.FLAG_WEIGHTS_STATIC,
+                               workspace=ws)
+        assert torch.equal(y, first)
+    assert w4.w4_last_device_error(ws) == 0
+
+
 @pytest.mark.parametrize("K,g", [(288, 256), (320, 64), (320, 128), (448, 128), (576, 192), (4000, 128), (200, 8)])
 @pytest.mark.parametrize("block_n", [8, 16, 32, 64, 128])
 def test_short_last_stage(K, g, block_n):
@@ -145,10 +213,13 @@ def test_one_hot_rows_return_rounded_weights_exactly():
         x[i, k] = 1.0
     wd = oracle.dequant(qw, s, zw, N, K, g)
     expect = wd[:, ks].T.astype(np.float16)  # (q - z) * s is exact in fp64; one rounding to fp16
-    for bn, ctas, sch in [(0, 0, 0), (16, 1, 2), (16, 4, 1), (128, 1, 1), (64, 5, 1), (16, 11, 1), (32, 3, 1),
-                          (8, 3, 1), (8, 1, 2)]:
+    for bn, ctas, sch in [(0, 0, 0), (16, 1, 2), (16, 4, 1), (128, 1, 1), (64, 5, 1), (16, 11, 1), (32, 3, 1)]:
         y = run_gemm(x, packed, N, K, g, bn, ctas, sch)
         assert (y.view(np.uint16) == expect.view(np.uint16)).all(), (bn, ctas, sch)
+    for bn, cluster in [(8, 1), (8, 2), (16, 1), (16, 2)]:  # the decode kernel, K split 1 or 2 ways
+        xs = torch.from_numpy(x[: min(bn, len(ks))]).cuda()
+        y = w4.w4a16_gemm_opts(xs, packed, N, K, g, kernel=1, block_n=bn, cluster=cluster).cpu().numpy()
+        assert (y.view(np.uint16) == expect[: xs.shape[0]].view(np.uint16)).all(), (bn, cluster)
 
 
 def test_q_equal_z_gives_exact_zero():
@@ -164,6 +235,9 @@ def test_q_equal_z_gives_exact_zero():
     x = workloads.activations_f16(17, K)
     y = run_gemm(x, packed, N, K, g)
     assert (y == 0).all()
+    for bn, m in ((8, 7), (16, 16)):  # the decode kernel, K split 2 ways
+        y = w4.w4a16_gemm_opts(torch.from_numpy(x[:m]).cuda(), packed, N, K, g, kernel=1, block_n=bn, cluster=2)
+        assert (y == 0).all()
 
 
 def test_deterministic_and_workspace_reuse():
@@ -232,8 +306,19 @@ def test_decode_sweep_layers(L):
 
 @pytest.mark.parametrize("L", workloads.PREFILL_LAYERS, ids=lambda L: L.name)
 def test_prefill_layers_sampled(L):
-    for M in (256, 4096):
+    # every prefill batch size: M = 512 and 1024 run stream-K over two-tile units and interleaved
+    # whole tiles, the schedules the prefill measurements come from
+    for M in workloads.PREFILL_MS:
         check(M, L.n, L.k, L.g, rows=_sample_rows(M, 8), outliers=True)
+
+
+@pytest.mark.parametrize("L", [workloads.STACK_LAYER[4], workloads.STACK_HEAD], ids=lambda L: L.name)
+def test_stack_only_layers(L):
+    # the decode stack's shapes that the decode sweep does not have: the unfused 11008 x 4096 gate/up
+    # projection and the 32000 x 4096 lm_head (250 weight tiles: more than one per SM); every row at
+    # M <= 16, sampled rows at M = 128
+    for M in workloads.STACK_MS:
+        check(M, L.n, L.k, L.g, rows=None if M <= 16 else _sample_rows(M, 16))
 
 
 @pytest.mark.parametrize("N,K,M,block_n,ctas,schedule", [

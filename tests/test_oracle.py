@@ -223,6 +223,34 @@ def test_repack_golden_tile_words():
         assert int(buf[4096:4098].view(np.uint16)[0]) == 0x3C00
 
 
+def test_repack_golden_positions():
+    # one non-zero code, scale or zero at a time in a 300 x 200, g = 24 layer: the repacked buffer
+    # must hold it at the hand-derived byte (and nibble half) and be zero everywhere else; the cases
+    # cover rows r > 0, the second K half h = 1, words i > 0, K blocks b > 0, weight tiles t > 0 and
+    # odd rows' zero nibbles
+    N, K, g = 300, 200, 24
+    G = oracle.ngroups(K, g)
+    for kind, n, kj, byte, half in _read_golden("tile_positions.txt"):
+        n, kj, byte = int(n), int(kj), int(byte)
+        q = np.zeros((N, K), np.uint8)
+        z = np.zeros((N, G), np.uint8)
+        s = np.zeros((N, G), np.float16)
+        if kind == "code":
+            q[n, kj] = 0xB
+        elif kind == "zero":
+            z[n, kj] = 0xB
+        else:
+            s[n, kj] = np.uint16(0x1234).view(np.float16)
+        buf = oracle.repack(oracle.pack_nibbles(q), s, oracle.pack_nibbles(z), N, K, g)
+        assert buf.size == 57792
+        nz = np.flatnonzero(buf)
+        if kind == "scale":
+            assert list(nz) == [byte, byte + 1] and buf[byte] == 0x34 and buf[byte + 1] == 0x12, (kind, n, kj)
+        else:
+            assert list(nz) == [byte], (kind, n, kj, nz[:4])
+            assert buf[byte] == (0x0B if half == "low" else 0xB0), (kind, n, kj, hex(buf[byte]))
+
+
 @pytest.mark.parametrize("N,K,g", [(1, 8, 8), (130, 72, 8), (288, 288, 256), (256, 512, 128), (200, 4000 // 10, 128),
                                    (129, 136, 24)])
 def test_repack_is_a_zero_padded_permutation(N, K, g):

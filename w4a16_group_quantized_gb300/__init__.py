@@ -23,9 +23,22 @@ import torch
 
 __all__ = [
     "W4Error", "lib_path", "load", "w4_pack", "w4_repack", "w4_repacked_bytes", "w4a16_gemm",
-    "w4a16_gemm_ex", "w4a16_workspace_bytes", "w4a16_workspace_bytes_ex", "w4a16_gemm_plan",
-    "w4_last_device_error", "w4_status_string", "Workspace", "STATUS",
+    "w4a16_gemm_ex", "w4a16_gemm_opts", "w4a16_workspace_bytes", "w4a16_workspace_bytes_ex",
+    "w4a16_workspace_bytes_opts", "w4a16_gemm_plan", "w4_last_device_error", "w4_status_string", "Workspace",
+    "Options", "STATUS", "KERNEL_DECODE", "KERNEL_TMEM", "FLAG_WEIGHTS_STATIC",
 ]
+
+KERNEL_DECODE = 1
+KERNEL_TMEM = 2
+FLAG_WEIGHTS_STATIC = 1
+
+
+class Options(ctypes.Structure):
+    """w4a16_options of the C ABI (all zero: automatic)."""
+
+    _fields_ = [("kernel", ctypes.c_int32), ("block_n", ctypes.c_int32), ("ctas", ctypes.c_int32),
+                ("schedule", ctypes.c_int32), ("cluster", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("wait_limit_cycles", ctypes.c_uint64)]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libw4a16.so")
@@ -67,6 +80,8 @@ def load() -> ctypes.CDLL:
             "w4a16_gemm_plan": ([I64, I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                                  ctypes.POINTER(I32)], ctypes.c_int),
             "w4_last_device_error": ([P, P], ctypes.c_int),
+            "w4a16_gemm_opts": ([P, P, I64, I64, I64, I32, P, P, SZ, ctypes.POINTER(Options), P], ctypes.c_int),
+            "w4a16_workspace_bytes_opts": ([I64, I64, I64, I32, ctypes.POINTER(Options)], SZ),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -144,6 +159,10 @@ def w4a16_workspace_bytes_ex(M: int, N: int, K: int, g: int, block_n: int, ctas:
     return int(load().w4a16_workspace_bytes_ex(M, N, K, g, block_n, ctas, schedule))
 
 
+def w4a16_workspace_bytes_opts(M: int, N: int, K: int, g: int, opts: Options) -> int:
+    return int(load().w4a16_workspace_bytes_opts(M, N, K, g, ctypes.byref(opts)))
+
+
 def w4a16_gemm_plan(M: int, N: int, K: int, g: int):
     """(block_n, ctas, schedule) that w4a16_gemm picks on the current device (schedule 1 stream-K, 2 whole tiles)."""
     b, s, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
@@ -191,9 +210,40 @@ def _gemm_common(x, packed, N, K, g, y, workspace, block_n, ctas, schedule, stre
 
 
 def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: int, y: torch.Tensor | None = None,
-               workspace=None, stream=None) -> torch.Tensor:
-    """y fp16 [M,N] = x fp16 [M,K] . dequant(packed)^T. ``workspace``: a Workspace or a zeroed uint8 tensor."""
+               workspace=None, stream=None, weights_static: bool = False) -> torch.Tensor:
+    """y fp16 [M,N] = x fp16 [M,K] . dequant(packed)^T. ``workspace``: a Workspace or a zeroed uint8 tensor.
+    ``weights_static``: the kernel launched just before this call on the stream does not write ``packed``
+    (W4_FLAG_WEIGHTS_STATIC: the decode kernel may then fetch weights before that kernel ends)."""
+    if weights_static:
+        return w4a16_gemm_opts(x, packed, N, K, g, flags=FLAG_WEIGHTS_STATIC, y=y, workspace=workspace,
+                               stream=stream)
     return _gemm_common(x, packed, N, K, g, y, workspace, 0, 0, 0, stream)
+
+
+def w4a16_gemm_opts(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: int, *, kernel: int = 0,
+                    block_n: int = 0, ctas: int = 0, schedule: int = 0, cluster: int = 0, flags: int = 0,
+                    wait_limit_cycles: int = 0, y: torch.Tensor | None = None, workspace=None,
+                    stream=None) -> torch.Tensor:
+    """w4a16_gemm with the options of w4a16_options (see include/w4a16.h)."""
+    if x.dtype != torch.float16 or x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be fp16 [M, K]")
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    elif y.dtype != torch.float16 or tuple(y.shape) != (M, N):
+        raise ValueError("y must be fp16 [M, N]")
+    o = Options(kernel, block_n, ctas, schedule, cluster, flags, wait_limit_cycles)
+    need = w4a16_workspace_bytes_opts(M, N, K, g, o)
+    if need == 0:
+        raise W4Error(1, "w4a16_workspace_bytes_opts")
+    if workspace is None:
+        workspace = Workspace(x.device)
+    ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    nbytes = ws.numel() * ws.element_size()
+    rc = load().w4a16_gemm_opts(_dev(x, "x"), _dev(packed, "packed"), M, N, K, g, _dev(y, "y"),
+                                _dev(ws, "workspace"), nbytes, ctypes.byref(o), _stream(stream))
+    _check(rc, "w4a16_gemm_opts")
+    return y
 
 
 def w4a16_gemm_ex(x, packed, N, K, g, block_n: int = 0, ctas: int = 0, schedule: int = 0, y=None, workspace=None,

@@ -42,19 +42,56 @@ int check_gemm_args(const void *x, const void *packed, int64_t M, int64_t N, int
   return W4_OK;
 }
 
+// The C options struct -> the library's options (false: a field out of range).
+bool to_options(const w4a16_options *o, w4::GemmOptions *out) {
+  *out = w4::GemmOptions{};
+  if (!o) return true;
+  if (o->flags & ~W4_FLAG_WEIGHTS_STATIC) return false;
+  out->kernel = o->kernel;
+  out->block_n = o->block_n;
+  out->ctas = o->ctas;
+  out->schedule = o->schedule;
+  out->cluster = o->cluster;
+  out->weights_static = (o->flags & W4_FLAG_WEIGHTS_STATIC) != 0;
+  out->wait_limit = o->wait_limit_cycles;
+  return true;
+}
+
+// w4a16_gemm_ex's (block_n, ctas, schedule): block_n 8 is the decode kernel, whose schedule 2 runs
+// whole tiles per CTA (clusters of 1) and whose ctas counts clusters.
+w4::GemmOptions ex_options(int32_t block_n, int32_t ctas, int32_t schedule) {
+  w4::GemmOptions o;
+  o.block_n = block_n;
+  o.ctas = ctas;
+  if (block_n == 8) {
+    o.kernel = w4::kKernelDecode;
+    o.cluster = schedule == 2 ? 1 : 0;
+  } else {
+    o.kernel = block_n == 0 ? w4::kKernelAuto : w4::kKernelTmem;
+    o.schedule = schedule;
+  }
+  return o;
+}
+
 int gemm_impl(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y, void *ws,
-              size_t ws_bytes, int32_t block_n, int32_t ctas, int32_t schedule, void *stream) {
+              size_t ws_bytes, const w4::GemmOptions &opt, void *stream) {
   const int rc = check_gemm_args(x, packed, M, N, K, g, y, ws);
   if (rc != W4_OK) return rc;
   w4::GemmPlan plan;
-  if (!w4::make_gemm_plan(M, N, K, g, block_n, ctas, schedule, num_sms_current_device(), &plan))
-    return W4_ERR_INVALID_ARG;
+  if (!w4::make_gemm_plan(M, N, K, g, opt, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
   if (ws_bytes < plan.workspace_bytes) return W4_ERR_WORKSPACE_TOO_SMALL;
   bool encode_failed = false;
   const cudaError_t e =
-      w4::launch_gemm(x, packed, M, N, K, g, y, ws, plan, static_cast<cudaStream_t>(stream), &encode_failed);
+      w4::launch_gemm(x, packed, M, N, K, g, y, ws, plan, opt, static_cast<cudaStream_t>(stream), &encode_failed);
   if (encode_failed) return W4_ERR_CUDA;
   return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+size_t workspace_impl(int64_t M, int64_t N, int64_t K, int32_t g, const w4::GemmOptions &opt) {
+  if (M < 1 || N < 1 || K < 1 || !valid_group(g) || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
+  w4::GemmPlan plan;
+  if (!w4::make_gemm_plan(M, N, K, g, opt, num_sms_current_device(), &plan)) return 0;
+  return plan.workspace_bytes;
 }
 
 }  // namespace
@@ -106,14 +143,17 @@ int w4_repack(const uint32_t *qw_dev, const void *scales_dev, const uint32_t *ze
 
 size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t g, int32_t block_n, int32_t ctas,
                                 int32_t schedule) {
-  if (M < 1 || N < 1 || K < 1 || !valid_group(g) || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
-  w4::GemmPlan plan;
-  if (!w4::make_gemm_plan(M, N, K, g, block_n, ctas, schedule, num_sms_current_device(), &plan)) return 0;
-  return plan.workspace_bytes;
+  return workspace_impl(M, N, K, g, ex_options(block_n, ctas, schedule));
 }
 
 size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t g) {
-  return w4a16_workspace_bytes_ex(M, N, K, g, 0, 0, 0);
+  return workspace_impl(M, N, K, g, w4::GemmOptions{});
+}
+
+size_t w4a16_workspace_bytes_opts(int64_t M, int64_t N, int64_t K, int32_t g, const w4a16_options *opts) {
+  w4::GemmOptions o;
+  if (!to_options(opts, &o)) return 0;
+  return workspace_impl(M, N, K, g, o);
 }
 
 int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int32_t *block_n, int32_t *ctas,
@@ -122,7 +162,8 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int32_t *block_n
   if (M < 1 || N < 1 || K < 1 || !valid_group(g) || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return W4_ERR_INVALID_ARG;
   w4::GemmPlan plan;
-  if (!w4::make_gemm_plan(M, N, K, g, 0, 0, 0, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
+  if (!w4::make_gemm_plan(M, N, K, g, w4::GemmOptions{}, num_sms_current_device(), &plan))
+    return W4_ERR_INVALID_ARG;
   *block_n = plan.block_n;
   *ctas = plan.ctas;
   *schedule = plan.whole ? 2 : 1;
@@ -131,14 +172,21 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int32_t *block_n
 
 int w4a16_gemm(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g, void *y_dev,
                void *workspace_dev, size_t workspace_bytes, void *stream) {
-  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, 0, 0, 0, stream);
+  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, w4::GemmOptions{}, stream);
 }
 
 int w4a16_gemm_ex(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g, void *y_dev,
                   void *workspace_dev, size_t workspace_bytes, int32_t block_n, int32_t ctas, int32_t schedule,
                   void *stream) {
-  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, block_n, ctas, schedule,
-                   stream);
+  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes,
+                   ex_options(block_n, ctas, schedule), stream);
+}
+
+int w4a16_gemm_opts(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K, int32_t g,
+                    void *y_dev, void *workspace_dev, size_t workspace_bytes, const w4a16_options *opts, void *stream) {
+  w4::GemmOptions o;
+  if (!to_options(opts, &o)) return W4_ERR_INVALID_ARG;
+  return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, o, stream);
 }
 
 int w4_last_device_error(void *workspace_dev, void *stream) {
@@ -202,7 +250,8 @@ int w4a16_gemm_noalloc(const void *x_dev, const void *packed_dev, int64_t M, int
   int rc = check_gemm_args(x_dev, packed_dev, M, N, K, g, y_dev, reinterpret_cast<void *>(uintptr_t{256}));
   if (rc != W4_OK) return rc;
   w4::GemmPlan plan;
-  if (!w4::make_gemm_plan(M, N, K, g, 0, 0, 0, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
+  const w4::GemmOptions opt;
+  if (!w4::make_gemm_plan(M, N, K, g, opt, num_sms_current_device(), &plan)) return W4_ERR_INVALID_ARG;
   if (plan.workspace_bytes > W4A16_NOALLOC_SCRATCH_BYTES) return W4_ERR_WORKSPACE_TOO_SMALL;
   void *scratch = noalloc_scratch_address(&rc);
   if (rc != W4_OK) return rc;
@@ -210,7 +259,8 @@ int w4a16_gemm_noalloc(const void *x_dev, const void *packed_dev, int64_t M, int
   // the array keeps the previous call's contents: the error word and the tile counters must start at zero
   if (cudaMemsetAsync(scratch, 0, plan.pieces_offset, st) != cudaSuccess) return W4_ERR_CUDA;
   bool encode_failed = false;
-  const cudaError_t e = w4::launch_gemm(x_dev, packed_dev, M, N, K, g, y_dev, scratch, plan, st, &encode_failed);
+  const cudaError_t e =
+      w4::launch_gemm(x_dev, packed_dev, M, N, K, g, y_dev, scratch, plan, opt, st, &encode_failed);
   if (encode_failed) return W4_ERR_CUDA;
   return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }

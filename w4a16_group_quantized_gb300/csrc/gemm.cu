@@ -1,5 +1,5 @@
-// w4a16_gemm: y[M,N] = x[M,K] . dequant(Wq)[N,K]^T on sm_103a tensor cores (M >= 9; the
-// register-operand decode kernel, gemm_rf.cu, takes M <= 8).
+// w4a16_gemm: y[M,N] = x[M,K] . dequant(Wq)[N,K]^T on sm_103a tensor cores (M >= 9 by default; the
+// register-operand decode kernel, gemm_dec.cu, takes M <= 8).
 //
 // Output tiles are 128 (weight rows n) x BN (activation rows m) tiles of y^T
 // ("swap-AB": the weights sit on the MMA's M = 128 side, the tokens on its N
@@ -678,9 +678,46 @@ cudaError_t launch_variant(int bn, int mode, int tp, const CUtensorMap &map, con
 
 }  // namespace
 
-bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int ctas, int schedule,
-                    int num_sms, GemmPlan *plan) {
+bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOptions &opt, int num_sms,
+                    GemmPlan *plan) {
   (void)g;
+  const int block_n = opt.block_n, ctas = opt.ctas, schedule = opt.schedule;
+  if (opt.kernel < kKernelAuto || opt.kernel > kKernelTmem) return false;
+  if (opt.cluster != 0 && opt.cluster != 1 && opt.cluster != 2 && opt.cluster != 4 && opt.cluster != 8) return false;
+  // The decode kernel: M <= 8 by default, or on request with block_n 8 or 16 and M <= block_n. Its
+  // workspace is the error word alone (the split along K is reduced in distributed shared memory).
+  // Each CTA keeps its K range of x in shared memory, so K may be split at most 8 ways into ranges of
+  // dec_x_stages_max stages; longer K goes to the tensor-memory kernel when the choice is automatic.
+  const int64_t ks_dec = cdiv(cdiv(K, kTK), kSB);
+  const bool dec_fits = dec_x_fits(ks_dec, 8, M);
+  const bool dec = opt.kernel == kKernelDecode ||
+                   (opt.kernel == kKernelAuto && (block_n == 8 || (block_n == 0 && M <= 8 && dec_fits)));
+  if (dec) {
+    const int bn = block_n == 0 ? (M <= 8 ? 8 : 16) : block_n;
+    if ((bn != 8 && bn != 16) || M > bn || ctas < 0 || ctas > 65535) return false;
+    const int64_t nt = cdiv(N, kTN), kb = cdiv(K, kTK), ks = cdiv(kb, kSB);
+    if (nt > 0x7FFFFFFF || (opt.cluster > 1 && opt.cluster > ks)) return false;
+    // clusters below this size cannot hold x
+    if (!dec_x_fits(ks, 8, M) || (opt.cluster > 0 && !dec_x_fits(ks, opt.cluster, M))) return false;
+    *plan = GemmPlan{};
+    plan->kernel = kKernelDecode;
+    plan->cluster = opt.cluster;
+    plan->block_n = bn;
+    plan->m_tiles = 1;
+    plan->n_tiles = static_cast<int>(nt);
+    plan->k_blocks = static_cast<int>(kb);
+    plan->k_stages = static_cast<int>(ks);
+    plan->tiles_per_unit = 1;
+    plan->ctas = ctas;  // clusters (0: as many as fit)
+    plan->gran = static_cast<int>(ks);
+    plan->whole = opt.cluster == 1;
+    plan->grains = nt;
+    plan->counters_offset = 256;
+    plan->pieces_offset = 256;
+    plan->workspace_bytes = 256;
+    return true;
+  }
+  if (opt.kernel == kKernelTmem && block_n == 8) return false;
   int bn = block_n;
   if (bn == 0) {
     bn = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
@@ -690,7 +727,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
     const int sms = num_sms > 0 ? num_sms : 148;
     if (bn == 128 && M <= 128 && cdiv(N, kTN) < sms) bn = 64;
   }
-  if (bn != 8 && bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
+  if (bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
   // Units of two weight tiles and 128-wide K stages for block_n 128 from M = 256 up (two or more
   // token tiles, so each CTA holds long runs of units and a tile pair is cut at most a few times);
@@ -722,6 +759,8 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
     };
     while (P > 1 && max_pieces(P) > kMaxPieces) --P;
   }
+  plan->kernel = kKernelTmem;
+  plan->cluster = 0;
   plan->block_n = bn;
   plan->m_tiles = static_cast<int>(mt);
   plan->n_tiles = static_cast<int>(nt);
@@ -744,9 +783,32 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int
 }
 
 cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y,
-                        void *workspace, const GemmPlan &plan, cudaStream_t stream, bool *encode_failed) {
+                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, cudaStream_t stream,
+                        bool *encode_failed) {
   *encode_failed = false;
   CUtensorMap map;
+  if (plan.kernel == kKernelDecode) {
+    DecParams p;
+    p.x = static_cast<const __half *>(x);
+    p.codes = static_cast<const uint8_t *>(packed);
+    p.meta = p.codes + static_cast<int64_t>(plan.n_tiles) * plan.k_blocks * kTileBytes;
+    p.y = static_cast<__half *>(y);
+    p.err = static_cast<uint32_t *>(workspace);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.g = g;
+    p.G = static_cast<int>(cdiv(K, g));
+    p.NT = plan.n_tiles;
+    p.KB = plan.k_blocks;
+    p.KS = plan.k_stages;
+    p.C = 0;
+    p.Q = 0;
+    p.early = opt.weights_static ? 1 : 0;
+    p.gdiv = make_fastdiv(static_cast<uint32_t>(g));
+    p.wait_limit = opt.wait_limit ? opt.wait_limit : kWaitLimitCycles;
+    return launch_gemm_dec(p, plan.block_n / 8, plan.ctas, plan.cluster, stream);
+  }
   const int sbk = kSB / plan.tiles_per_unit;
   bool x3d = K % kTK == 0 && make_x_map(&map, x, M, K, plan.block_n, sbk, true);
   if (!x3d && !make_x_map(&map, x, M, K, plan.block_n, sbk, false)) {
@@ -786,7 +848,6 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.x3d = x3d ? 1 : 0;
   p.tstride = plan.interleave ? plan.ctas : 1;
   p.grains = plan.grains;
-  if (plan.block_n == 8) return launch_gemm_rf(map, p, 1, g % kTK != 0, plan.ctas, stream);
   return launch_variant(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p, plan.ctas,
                         stream);
 }

@@ -316,9 +316,25 @@ cudaError_t launch_programmatic(Kernel kern, int ctas, int threads, int smem_byt
   return cudaGetLastError();
 }
 
-// The decode kernel (gemm_rf.cu): register-operand MMAs, tiles of 8 * nb8 tokens.
-cudaError_t launch_gemm_rf(const CUtensorMap &map, const Params &p, int nb8, bool general, int ctas,
-                           cudaStream_t stream);
+// Parameters of the cluster decode kernel (gemm_dec.cu): M <= 8 * nb8 tokens, one token tile.
+struct DecParams {
+  const __half *x;       // [M, K] activations
+  const uint8_t *codes;  // tile region of the packed weights
+  const uint8_t *meta;   // group-record region of the packed weights
+  __half *y;
+  uint32_t *err;
+  int M, N, K, g, G, NT, KB, KS;
+  int C;                 // CTAs per cluster; each takes a contiguous K range of every tile of the cluster
+  int Q;                 // clusters; cluster q takes the weight tiles q, q + Q, ...
+  int xslice;            // 256-wide K stages of x each CTA keeps in shared memory (its longest K range)
+  int S;                 // stages in the weight ring (even)
+  int early;             // issue the first stages' weight copies before waiting for the previous grid
+  FastDiv gdiv;          // division by g
+  uint64_t wait_limit;   // cycles a pipeline wait may take before the kernel gives up
+};
+
+// Launches the decode kernel with `clusters` clusters of `cluster` CTAs (0: chosen for the layer).
+cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int clusters, int cluster, cudaStream_t stream);
 
 }  // namespace detail
 }  // namespace w4

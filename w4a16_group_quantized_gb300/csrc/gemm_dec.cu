@@ -1,0 +1,761 @@
+// w4a16_gemm for decode batches (M <= 16 tokens): the dequantized weights go straight into the A
+// fragments of register-operand tensor-core MMAs (mma.sync m16n8k16, fp16 in, fp32 accumulate), so a
+// weight is read once as a 4-bit code, turned into fp16 in registers and consumed there.
+//
+// Work split: the weight tiles (128 rows each) are dealt out to thread-block clusters round-robin
+// (cluster q: tiles q, q + Q, ...). The C CTAs of a cluster split every tile along K: CTA rank k
+// takes the 256-wide K stages [k KS / C, (k + 1) KS / C) of it. At the end of a tile the CTAs
+// reduce-scatter their fp32 partial sums through distributed shared memory: CTA j sums rows
+// [j 128 / C, (j + 1) 128 / C) of the tile over all C CTAs (in a fixed order: deterministic) and
+// writes them to y. Nothing waits across clusters and nothing goes through global memory but the
+// weights, x and y. The cluster size is chosen per layer for the best balance (a small layer's 16
+// stages per tile split 4 ways keeps 128 SMs busy on a 32-tile layer; a large layer runs whole
+// tiles, C = 1).
+//
+// Warp roles (one CTA per SM):
+//   2 producer warps take the CTA's stages in turn; lane 0 issues per stage one tensor copy of x
+//                   (128-byte swizzle, zero fill outside [M, K]) and two bulk copies: 16 KB of codes
+//                   and the group records the stage needs. With `early` set the first stages' weight
+//                   copies are issued before the wait for the previous grid (the weights are
+//                   read-only), and x after it.
+//   16 consumer warps in two sets of 8 that take the stages in turn (even / odd): warp (set, slab)
+//                   covers weight rows 16 slab .. 16 slab + 15 over the stage's four 64-wide K blocks.
+//                   Per block a lane loads two rows' 16-code spans (one 8-byte load each), the x
+//                   fragments of its token (two 16-byte loads) and issues 4 k16 steps x NB8 MMAs.
+//                   With g a multiple of 64 the MMAs run on the exact integers q - z and each group's
+//                   fp32 partial is scaled by its s once per row; any other g rounds (q - z) * s to
+//                   fp16 per 8 codes. At a tile's end a warp stores its rows' partial sums into the
+//                   shared memory of the CTA that sums them and arrives on that CTA's barrier.
+//   1 reducer warp sums the partial sums of this CTA's rows of each finished tile over the cluster
+//                   and writes y, while the consumers already work on the next tile.
+//
+// The 16 k of one MMA step are taken in a permuted order, the same on both operands (the dot
+// product is unchanged): lane (g, t) holds in step p the code pairs of its rows at k = 16t + 4p, +1 and
+// 16t + 4p + 2, +3 of the block and the matching x pairs, which the tile layout of w4_repack and the
+// 128-byte swizzle of x serve without shuffles, register moves or bank conflicts on x.
+//
+// This is Marlin's register-level dequant into MMA fragments (Marlin post) carried to sm_103a, with
+// TMA/mbarrier staging, clusters and distributed shared memory for the split along K.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "gemm_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace w4 {
+namespace {
+
+using namespace detail;
+
+enum DecMode { kDecG256 = 0, kDecG128 = 1, kDecG64 = 2, kDecGen = 3 };
+
+template <int NB8, int MODE>
+struct DecCfg {
+  static constexpr int BN = 8 * NB8;  // tokens per tile (the MMA's N, or two of them)
+  // The CTA's K range of x stays in shared memory for the whole launch, M token rows of 128 bytes per
+  // 64-wide K block (512 M bytes per stage), at most kXSlice stages and kDecXRegionBytes.
+  static constexpr int kXSlice = kDecXSliceMax;
+  static constexpr int kCodeBytes = kSB * kTileBytes;
+  // group records a 256-wide stage can touch: one when g % 256 == 0, two for g == 128, five for other
+  // multiples of 64, 33 for any g
+  static constexpr int kMaxRecs = MODE == kDecGen ? kStageK / 8 + 1 : MODE == kDecG64 ? 5 : MODE == kDecG128 ? 2 : 1;
+  static constexpr int kStageBytes = (kCodeBytes + kMaxRecs * kRecBytes + 127) / 128 * 128;
+  static constexpr int kProducers = 2;
+  static constexpr int kConsumers = 16;
+  static constexpr int kSetWarps = kConsumers / 2;
+  static constexpr int kReducerWarp = kProducers + kConsumers;
+  static constexpr int kThreads = (kReducerWarp + 1) * 32;
+  // Shared memory: [x: the CTA's K range][ring: S stages of weights][partial sums a CTA receives per tile:
+  // [C senders][2 sets][M tokens][128 / C rows] fp32, 1 KB per token]. The ring takes whatever x leaves
+  // (S even, for the two producers, at most kMaxStages).
+  static constexpr int kSmemMax = 226 * 1024;
+  static constexpr int kMaxStages = 14;
+  static int x_bytes(int xslice, int m) { return xslice * kSB * m * 128; }
+  static int ring_stages(int xslice, int m) {
+    const int s = (kSmemMax - 1024 - 1024 * m - x_bytes(xslice, m)) / kStageBytes;
+    return (s > kMaxStages ? kMaxStages : s) / 2 * 2;
+  }
+  static int smem_bytes(int xslice, int m, int stages) {
+    return 1024 + x_bytes(xslice, m) + stages * kStageBytes + 1024 * m;
+  }
+  static_assert(kDecXRegionBytes + 4 * kStageBytes + 1024 * BN + 1024 <= kSmemMax, "shared memory");
+  static_assert(NB8 == 1 || NB8 == 2, "tokens per tile");
+};
+
+template <int OFF>
+__device__ __forceinline__ uint32_t lds16_at(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1+%2];" : "=h"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t lds8_at(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1+%2];" : "=h"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 lds64_at(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(addr), "n"(OFF));
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
+template <int OFF>
+__device__ __forceinline__ uint4 lds128_at(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr), "n"(OFF));
+  return v;
+}
+
+// D (+)= A . B, m16n8k16, A row-major fp16 (4 regs), B column-major fp16 (2 regs), fp32 D.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The two rows a lane serves in a slab (rows R and R + 8): dequant constants and fp32 scales.
+struct SlabConsts {
+  GroupConsts a, b;
+  float sa, sb;
+};
+
+// Integer path: zero points of rows R, R + 8 from the record at `rec`, scales as fp32.
+__device__ __forceinline__ SlabConsts slab_consts_int(uint32_t rec, uint32_t zero_off, uint32_t zero_shift,
+                                                      uint32_t scale_off) {
+  SlabConsts c;
+  c.a = group_consts(0u, (lds8_at<0>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.b = group_consts(0u, (lds8_at<4>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.sa = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at<0>(rec + scale_off))));
+  c.sb = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at<16>(rec + scale_off))));
+  return c;
+}
+
+// Scaled path: the full constants (scale applied in the dequant) of rows R, R + 8.
+__device__ __forceinline__ SlabConsts slab_consts_scaled(uint32_t rec, uint32_t zero_off, uint32_t zero_shift,
+                                                         uint32_t scale_off) {
+  SlabConsts c;
+  c.a = group_consts(lds16_at<0>(rec + scale_off), (lds8_at<0>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.b = group_consts(lds16_at<16>(rec + scale_off), (lds8_at<4>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.sa = c.sb = 1.0f;
+  return c;
+}
+
+// One 64-wide K block BB of a lane's two rows: the 8-byte spans of rows R and R + 8 (words 2t, 2t + 1,
+// k = 16t .. 16t + 15 of the block) dequantized into the A fragments of 4 k16 steps, times the x
+// fragments of the block's tokens. Step p takes the pairs at k = 16t + 4p, +1 (the MMA's k-slot 2t, 2t + 1)
+// and 16t + 4p + 2, +3 (slot 2t + 8, 2t + 9) on both operands: the x pair of a step is then two
+// consecutive registers of one 16-byte load. SCALED: the constants of words 2t (c0) and 2t + 1 (c1)
+// carry the scale; else both are the block's group and the MMAs see the exact q - z.
+// The x operand of a lane: rows g and 8 + g of each block (the lane's tokens), present when < M.
+struct XLane {
+  uint32_t a, b;  // x of the lane's first row, chunks 2t and 2t + 1 (block 0 of the stage)
+  uint32_t blk;   // bytes per 64-wide block (M rows of 128 bytes)
+  bool v0, v1;    // token g, 8 + g < M
+};
+
+template <int NB8, int BB, bool SCALED>
+__device__ __forceinline__ void dec_block(uint32_t codes, const XLane &xl, const SlabConsts &c0,
+                                          const SlabConsts &c1, float (&acc)[NB8][4]) {
+  const uint2 wr = lds64_at<BB * kTileBytes>(codes);        // row R: words 2t, 2t + 1
+  const uint2 ws = lds64_at<BB * kTileBytes + 128>(codes);  // row R + 8
+  uint32_t r0[4], r1[4], s0[4], s1[4];
+  if (SCALED) {
+    dequant_word(wr.x, c0.a, r0);
+    dequant_word(wr.y, c1.a, r1);
+    dequant_word(ws.x, c0.b, s0);
+    dequant_word(ws.y, c1.b, s1);
+  } else {
+    dequant_word_int(wr.x, c0.a, r0);
+    dequant_word_int(wr.y, c0.a, r1);
+    dequant_word_int(ws.x, c0.b, s0);
+    dequant_word_int(ws.y, c0.b, s1);
+  }
+#pragma unroll
+  for (int nb = 0; nb < NB8; ++nb) {
+    // token g + 8 nb: x chunks 2t and 2t + 1 of the block (k 16t .. 16t + 15)
+    uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+    if (nb == 0 ? xl.v0 : xl.v1) {
+      x0 = nb == 0 ? lds128_at<0>(xl.a + BB * xl.blk) : lds128_at<1024>(xl.a + BB * xl.blk);
+      x1 = nb == 0 ? lds128_at<0>(xl.b + BB * xl.blk) : lds128_at<1024>(xl.b + BB * xl.blk);
+    }
+    {
+      const uint32_t a[4] = {r0[0], s0[0], r0[1], s0[1]};
+      mma16816(acc[nb], a, x0.x, x0.y);
+    }
+    {
+      const uint32_t a[4] = {r0[2], s0[2], r0[3], s0[3]};
+      mma16816(acc[nb], a, x0.z, x0.w);
+    }
+    {
+      const uint32_t a[4] = {r1[0], s1[0], r1[1], s1[1]};
+      mma16816(acc[nb], a, x1.x, x1.y);
+    }
+    {
+      const uint32_t a[4] = {r1[2], s1[2], r1[3], s1[3]};
+      mma16816(acc[nb], a, x1.z, x1.w);
+    }
+  }
+}
+
+template <int NB8>
+__device__ __forceinline__ void zero_acc(float (&acc)[NB8][4]) {
+#pragma unroll
+  for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[nb][c] = 0.0f;
+}
+
+// tot += s * acc per row (fragment elements 0, 1: row R; 2, 3: row R + 8).
+template <int NB8>
+__device__ __forceinline__ void flush_scaled(float (&tot)[NB8][4], const float (&acc)[NB8][4], const SlabConsts &c) {
+#pragma unroll
+  for (int nb = 0; nb < NB8; ++nb) {
+    tot[nb][0] = fmaf(c.sa, acc[nb][0], tot[nb][0]);
+    tot[nb][1] = fmaf(c.sa, acc[nb][1], tot[nb][1]);
+    tot[nb][2] = fmaf(c.sb, acc[nb][2], tot[nb][2]);
+    tot[nb][3] = fmaf(c.sb, acc[nb][3], tot[nb][3]);
+  }
+}
+
+// A lane's fixed offsets within a stage.
+struct LaneOffsets {
+  uint32_t code, x0, x1, xblk, zero, zero_shift, scale;
+  bool xv0, xv1;
+};
+
+template <int BB>
+__device__ __forceinline__ bool has_block(bool full, int nbk) {
+  return full || BB < nbk;
+}
+
+// One stage (up to four K blocks from k0) of a lane's two rows, accumulated into tot. FULL: all four
+// blocks present (the compiler then sees straight-line code); else nbk of them.
+template <int NB8, int MODE, int CODEBYTES, bool FULL>
+__device__ __forceinline__ void dec_stage(const DecParams &p, uint32_t stage, uint32_t xstage, const LaneOffsets &o,
+                                          int k0, int nbk, int t, float (&tot)[NB8][4]) {
+  const uint32_t codes = stage + o.code;
+  XLane xb;
+  xb.a = xstage + o.x0;
+  xb.b = xstage + o.x1;
+  xb.blk = o.xblk;
+  xb.v0 = o.xv0;
+  xb.v1 = o.xv1;
+  const uint32_t recs = stage + CODEBYTES;
+  if (MODE == kDecG256) {  // g % 256 == 0: the whole stage lies in one group
+    const SlabConsts c = slab_consts_int(recs, o.zero, o.zero_shift, o.scale);
+    float acc[NB8][4];
+    zero_acc<NB8>(acc);
+    dec_block<NB8, 0, false>(codes, xb, c, c, acc);
+    if (has_block<1>(FULL, nbk)) dec_block<NB8, 1, false>(codes, xb, c, c, acc);
+    if (has_block<2>(FULL, nbk)) dec_block<NB8, 2, false>(codes, xb, c, c, acc);
+    if (has_block<3>(FULL, nbk)) dec_block<NB8, 3, false>(codes, xb, c, c, acc);
+    flush_scaled<NB8>(tot, acc, c);
+  } else if (MODE == kDecG128) {  // g == 128: blocks 0, 1 in the stage's first group, 2, 3 in the next
+    const SlabConsts c0 = slab_consts_int(recs, o.zero, o.zero_shift, o.scale);
+    float acc[NB8][4];
+    zero_acc<NB8>(acc);
+    dec_block<NB8, 0, false>(codes, xb, c0, c0, acc);
+    if (has_block<1>(FULL, nbk)) dec_block<NB8, 1, false>(codes, xb, c0, c0, acc);
+    flush_scaled<NB8>(tot, acc, c0);
+    if (has_block<2>(FULL, nbk)) {
+      const SlabConsts c1 = slab_consts_int(recs + kRecBytes, o.zero, o.zero_shift, o.scale);
+      float acc1[NB8][4];
+      zero_acc<NB8>(acc1);
+      dec_block<NB8, 2, false>(codes, xb, c1, c1, acc1);
+      if (has_block<3>(FULL, nbk)) dec_block<NB8, 3, false>(codes, xb, c1, c1, acc1);
+      flush_scaled<NB8>(tot, acc1, c1);
+    }
+  } else if (MODE == kDecG64) {  // g % 64 == 0: each block lies in one group, looked up per block
+    const int jlo = p.gdiv.div(k0);
+#pragma unroll
+    for (int bb = 0; bb < kSB; ++bb) {
+      if (FULL || bb < nbk) {
+        const uint32_t rec = recs + (p.gdiv.div(k0 + bb * kTK) - jlo) * kRecBytes;
+        const SlabConsts c = slab_consts_int(rec, o.zero, o.zero_shift, o.scale);
+        float acc[NB8][4];
+        zero_acc<NB8>(acc);
+        if (bb == 0) dec_block<NB8, 0, false>(codes, xb, c, c, acc);
+        if (bb == 1) dec_block<NB8, 1, false>(codes, xb, c, c, acc);
+        if (bb == 2) dec_block<NB8, 2, false>(codes, xb, c, c, acc);
+        if (bb == 3) dec_block<NB8, 3, false>(codes, xb, c, c, acc);
+        flush_scaled<NB8>(tot, acc, c);
+      }
+    }
+  } else {  // any g (a multiple of 8): (q - z) * s per 8 codes; codes past K (zero, against zero x) take
+            // the last group's record, which the stage holds
+    const int jlo = p.gdiv.div(k0);
+#pragma unroll
+    for (int bb = 0; bb < kSB; ++bb) {
+      if (FULL || bb < nbk) {
+        const int kw = k0 + bb * kTK + 16 * t;
+        const uint32_t r0 = recs + (min(p.gdiv.div(kw), p.G - 1) - jlo) * kRecBytes;
+        const uint32_t r1 = recs + (min(p.gdiv.div(kw + 8), p.G - 1) - jlo) * kRecBytes;
+        const SlabConsts c0 = slab_consts_scaled(r0, o.zero, o.zero_shift, o.scale);
+        const SlabConsts c1 = slab_consts_scaled(r1, o.zero, o.zero_shift, o.scale);
+        if (bb == 0) dec_block<NB8, 0, true>(codes, xb, c0, c1, tot);
+        if (bb == 1) dec_block<NB8, 1, true>(codes, xb, c0, c1, tot);
+        if (bb == 2) dec_block<NB8, 2, true>(codes, xb, c0, c1, tot);
+        if (bb == 3) dec_block<NB8, 3, true>(codes, xb, c0, c1, tot);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int dec_stage_blocks(const DecParams &p, int ks) {
+  return ks == p.KS - 1 ? p.KB - kSB * (p.KS - 1) : kSB;
+}
+
+// Waits with a caller-given limit; on timeout raises the CTA's abort flag and the error word.
+__device__ __forceinline__ bool dec_wait(uint32_t bar, uint32_t parity, bool cluster_scope, const DecParams &p,
+                                         volatile uint32_t *abort_flag) {
+  const uint64_t t0 = clock_cycles();
+  for (;;) {
+    const bool done = cluster_scope ? mbar_try_wait_cluster(bar, parity, kSuspendNs)
+                                    : mbar_try_wait_sleep(bar, parity, kSuspendNs);
+    if (done) return true;
+    if (*abort_flag) return false;
+    if (clock_cycles() - t0 > p.wait_limit) {
+      *abort_flag = 1u;
+      atomicOr(p.err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool dec_warp_wait(uint32_t bar, uint32_t parity, bool cluster_scope, const DecParams &p,
+                                              volatile uint32_t *abort_flag) {
+  const bool ok = dec_wait(bar, parity, cluster_scope, p, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// The CTA's K range of x, stage by stage (four 64-wide K blocks of BN token rows each, 128-byte swizzle:
+// 16-byte chunk c of row n of a block at n * 128 + (c ^ (n % 8)) * 16), loaded once by the 512 consumer
+// threads with zero-filling asynchronous copies (rows >= M and k >= K read nothing and land as zeros):
+// thread `tid` copies chunk tid (and tid + 512) of each stage, then arrives on that stage's barrier once
+// its copies so far have landed.
+__device__ __forceinline__ void load_x_slice(const DecParams &p, uint32_t xbase, int kb, int nstages, int tid,
+                                             uint64_t *x_ready) {
+  const int m = p.M;  // rows per block; 32 m <= 512 chunks per stage
+  const int b = tid / (8 * m);
+  const int n = (tid / 8) % m;
+  const int c = tid % 8;
+  const bool mine = tid < 32 * m;  // thread tid copies chunk tid of every stage
+  const uint32_t dst0 = xbase + b * m * 128 + n * 128 + ((c ^ (n & 7)) << 4);
+  for (int st = 0; st < nstages; ++st) {
+    const int k = (kb + st) * kStageK + b * kTK + 8 * c;
+    if (mine) {
+      const bool valid = k < p.K;
+      const __half *src = valid ? p.x + static_cast<int64_t>(n) * p.K + k : p.x;
+      cp_async16_zfill(dst0 + st * kSB * m * 128, src, valid ? 16u : 0u);
+    }
+    cp_async_mbar_arrive(smem_u32(&x_ready[st]));
+  }
+}
+
+template <int NB8, int MODE>
+__global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
+    w4a16_gemm_dec_kernel(const DecParams p) {
+  using Cfg = DecCfg<NB8, MODE>;
+  constexpr int SMAX = Cfg::kMaxStages;
+  const int S = p.S;  // ring stages (even)
+  constexpr int BN = Cfg::BN;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[SMAX];   // the stage's weights landed
+  __shared__ __align__(8) uint64_t x_ready[Cfg::kXSlice];  // x of the CTA's k-th stage of every tile landed
+  __shared__ __align__(8) uint64_t empty_bar[SMAX];  // the 8 warps of the stage's set are done with it
+  __shared__ __align__(8) uint64_t recv_bar;      // the 16 warps of the cluster whose rows this CTA sums stored them
+  __shared__ __align__(8) uint64_t free_bar;      // every CTA of the cluster summed its rows of this CTA's last partials
+  __shared__ uint32_t abort_sh;
+
+  const uint32_t x_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t smem_base = x_base + p.xslice * kSB * p.M * 128;
+  const uint32_t red_base = smem_base + S * Cfg::kStageBytes;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  volatile uint32_t *abort_flag = &abort_sh;
+
+  const int C = p.C;
+  const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int q = static_cast<int>(blockIdx.x) / C;
+  const int kb = rank * p.KS / C;  // this CTA's K stages of every tile: [kb, ke)
+  const int ke = (rank + 1) * p.KS / C;
+  const int per_tile = ke - kb;    // >= 1: the planner keeps C <= KS
+  const int rounds = q < p.NT ? (p.NT - 1 - q) / p.Q + 1 : 0;  // tiles q, q + Q, ...
+  const int nst = rounds * per_tile;
+  const int rows_per = kTN / C;  // rows of each tile this CTA sums
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < S; ++st) {
+      mbar_init(smem_u32(&full_bar[st]), 1);
+      mbar_init(smem_u32(&empty_bar[st]), Cfg::kSetWarps);
+    }
+    for (int st = 0; st < Cfg::kXSlice; ++st) mbar_init(smem_u32(&x_ready[st]), 32 * Cfg::kConsumers);
+    mbar_init(smem_u32(&recv_bar), 1);  // the reducer's arrival; the partial sums come as transaction bytes
+    mbar_init(smem_u32(&free_bar), C);   // one arrival from each CTA's reducer
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // every CTA's barriers are initialized before any CTA of the cluster arrives on them remotely
+  if (C > 1)
+    cluster_sync_all();
+  else
+    cta_sync_all();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp < Cfg::kProducers) {
+    // ---------------------------------------------------------------- producers
+    const int pw = warp;
+    const uint64_t pol = policy_evict_first();  // each weight byte is read once
+    int i = pw, r = 0, ks = kb + pw;
+    while (ks >= ke) {
+      ks -= per_tile;
+      ++r;
+    }
+    if (p.early) {
+      // the first stages' weights before the previous grid is waited for: the packed weights are
+      // read-only to every kernel of the stream (the caller states this)
+      int re = r, kse = ks;
+      for (int ie = pw; ie < nst && ie < S; ie += 2) {
+        if (lane == 0) {
+          const int t = q + re * p.Q;
+          const int nb = dec_stage_blocks(p, kse);
+          const int k0 = kse * kStageK;
+          const int jlo = p.gdiv.div(k0);
+          const int nrec = p.gdiv.div(min(k0 + nb * kTK, p.K) - 1) - jlo + 1;
+          const uint32_t stage = smem_base + (ie % S) * Cfg::kStageBytes;
+          const uint32_t bar = smem_u32(&full_bar[ie % S]);
+          mbar_expect_tx(bar, nb * kTileBytes + nrec * kRecBytes);
+          bulk_g2s(stage, p.codes + (static_cast<int64_t>(t) * p.KB + kse * kSB) * kTileBytes, nb * kTileBytes, bar,
+                   pol);
+          bulk_g2s(stage + Cfg::kCodeBytes, p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes,
+                   nrec * kRecBytes, bar, pol);
+        }
+        kse += 2;
+        while (kse >= ke) {
+          kse -= per_tile;
+          ++re;
+        }
+      }
+      __syncwarp();
+    } else if (pw == 0 && lane == 0 && nst > 0) {
+      // ask L2 for the first tile's first stages while the previous grid finishes
+      const int t = q;
+      const int n0 = min(ke - kb, S);
+      const int blocks = min((kb + n0) * kSB, p.KB) - kb * kSB;
+      bulk_prefetch_l2(p.codes + (static_cast<int64_t>(t) * p.KB + kb * kSB) * kTileBytes, blocks * kTileBytes);
+      const int jlo = p.gdiv.div(kb * kStageK);
+      const int jhi = p.gdiv.div(min((kb + n0) * kStageK, p.K) - 1);
+      bulk_prefetch_l2(p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
+    }
+    griddep_wait();  // x may be the previous grid's output
+    int s = pw, ph = 0;  // slot i % S and the parity of its use i / S (S even: this warp's slots have its parity)
+    for (; i < nst; i += 2) {
+      if (i >= S && !dec_warp_wait(smem_u32(&empty_bar[s]), ph ^ 1, false, p, abort_flag)) break;
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&full_bar[s]);
+        if (p.early && i < S) {
+          mbar_arrive(bar);  // the weights are on their way since before the wait
+        } else {
+          const int t = q + r * p.Q;
+          const int nb = dec_stage_blocks(p, ks);
+          const int k0 = ks * kStageK;
+          const int jlo = p.gdiv.div(k0);
+          const int nrec = p.gdiv.div(min(k0 + nb * kTK, p.K) - 1) - jlo + 1;
+          const uint32_t stage = smem_base + s * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(bar, nb * kTileBytes + nrec * kRecBytes);
+          bulk_g2s(stage, p.codes + (static_cast<int64_t>(t) * p.KB + ks * kSB) * kTileBytes, nb * kTileBytes, bar,
+                   pol);
+          bulk_g2s(stage + Cfg::kCodeBytes, p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes,
+                   nrec * kRecBytes, bar, pol);
+        }
+      }
+      __syncwarp();
+      ks += 2;
+      while (ks >= ke) {
+        ks -= per_tile;
+        ++r;
+      }
+      s += 2;
+      if (s >= S) {
+        s -= S;
+        ph ^= 1;
+      }
+    }
+    if (*abort_flag && lane == 0) {
+      // let every weight copy this warp issued land before the CTA's shared memory goes away. Early
+      // weight copies of stages the loop never reached have no arrival yet: arrive, so that their phase
+      // completes once the bytes are in.
+      int last = i;
+      if (p.early) {
+        for (int j = i; j < min(nst, S); j += 2) mbar_arrive(smem_u32(&full_bar[j % S]));
+        const int n_early = min(nst, S);
+        if (n_early > pw) last = max(last, pw + (n_early - 1 - pw) / 2 * 2 + 2);
+      }
+      for (int j = last - 2; j >= 0 && j >= last - S; j -= 2) drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1);
+    }
+  } else if (warp < Cfg::kReducerWarp) {
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp - Cfg::kProducers;
+    const int qs = (cw >> 2) & 1;                // stage set: stages of parity qs (two warps per SMSP)
+    const int sl = (cw & 3) | ((cw >> 3) << 2);  // slab: rows 16 sl .. 16 sl + 15
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int R = 16 * sl + g;  // rows R and R + 8
+    LaneOffsets o;
+    o.code = (t >> 1) * 2048 + R * 16 + 8 * (t & 1);
+    // x of token g, 128-byte swizzle: chunk c of row n sits at n * 128 + (c ^ (n % 8)) * 16 (n % 8 == g)
+    o.x0 = 128 * g + (((2 * t) ^ g) << 4);
+    o.x1 = 128 * g + (((2 * t + 1) ^ g) << 4);
+    o.xblk = p.M * 128;
+    o.xv0 = g < p.M;
+    o.xv1 = 8 + g < p.M;
+    o.zero = 256 + R / 2;  // (+4 for row R + 8)
+    o.zero_shift = 4 * (R & 1);
+    o.scale = 2 * R;  // (+16 for row R + 8)
+    // this warp's rows are summed by cluster CTA j, into slot [rank][qs][token][row - j rows_per]
+    const int j = (16 * sl) / rows_per;
+    const uint32_t slot_local = red_base + ((rank * 2 + qs) * p.M * rows_per + (R - j * rows_per)) * 4;
+    const uint32_t slot = mapa_shared(slot_local, j);
+    const uint32_t recv_at_j = mapa_shared(smem_u32(&recv_bar), j);
+
+    // x of the CTA's K range, once: every tile of the launch uses the same range
+    griddep_wait();  // x may be the previous grid's output
+    if (rounds > 0) load_x_slice(p, x_base, kb, per_tile, cw * 32 + lane, x_ready);
+    float tot[NB8][4];
+    zero_acc<NB8>(tot);
+    bool ok = true;
+    int s = qs, ph = 0;  // slot and use parity of the set's next stage (its stages are i = qs, qs + 2, ...)
+    for (int r = 0; r < rounds && ok; ++r) {
+      // this set's stages of the round: local stage indices i = r per_tile + ... of parity qs
+      const int ibase = r * per_tile;
+      for (int i = ibase + ((qs - ibase) & 1); i < ibase + per_tile; i += 2) {
+        const int ks = kb + (i - ibase);
+        if (r == 0) {
+          ok = dec_warp_wait(smem_u32(&x_ready[ks - kb]), 0, false, p, abort_flag);
+          if (!ok) break;
+        }
+        ok = dec_warp_wait(smem_u32(&full_bar[s]), ph, false, p, abort_flag);
+        if (!ok) break;
+        const uint32_t stage = smem_base + s * Cfg::kStageBytes;
+        const uint32_t xstage = x_base + (ks - kb) * kSB * o.xblk;
+        const int nbk = dec_stage_blocks(p, ks);
+        if (nbk == kSB)
+          dec_stage<NB8, MODE, Cfg::kCodeBytes, true>(p, stage, xstage, o, ks * kStageK, nbk, t, tot);
+        else
+          dec_stage<NB8, MODE, Cfg::kCodeBytes, false>(p, stage, xstage, o, ks * kStageK, nbk, t, tot);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+        s += 2;
+        if (s >= S) {
+          s -= S;
+          ph ^= 1;
+        }
+      }
+      if (!ok) break;
+      // the tile's partial sums of rows R, R + 8 go to CTA j once it has summed the previous tile's
+      if (r > 0 && !dec_warp_wait(smem_u32(&free_bar), (r - 1) & 1, true, p, abort_flag)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int nb = 0; nb < NB8; ++nb) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int tok = 8 * nb + 2 * t + (c & 1);
+          if (tok < p.M) st_async_f32(slot + (tok * rows_per + 8 * (c >> 1)) * 4, tot[nb][c], recv_at_j);
+        }
+      }
+      zero_acc<NB8>(tot);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // (after an abort) no copy of this thread in flight
+  } else {
+    // ---------------------------------------------------------------- reducer
+    // sums this CTA's rows [rank rows_per, (rank + 1) rows_per) of each finished tile over the cluster's
+    // CTAs and both sets, in a fixed order, and writes y; then frees the slots of every sender
+    griddep_wait();  // y may still be in use by the previous grid
+    const uint32_t free_at_lane = C > 1 && lane < C ? mapa_shared(smem_u32(&free_bar), lane) : smem_u32(&free_bar);
+    // 8-byte stores of 4 consecutive outputs when they stay aligned (y itself need only be 2-byte aligned)
+    const bool vec_y = p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 7) == 0;
+    for (int r = 0; r < rounds; ++r) {
+      // this tile's partial sums for this CTA's rows: 2 sets x C CTAs x rows_per rows x M tokens x 4 bytes
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&recv_bar), 1024u * p.M);
+      if (!dec_warp_wait(smem_u32(&recv_bar), r & 1, true, p, abort_flag)) break;
+      const int n0 = (q + r * p.Q) * kTN + rank * rows_per;
+      // 4 consecutive rows per lane and step: one 16-byte load per partial, one 8-byte store of y
+      const int quads = p.M * (rows_per / 4);
+#pragma unroll 2
+      for (int e = lane; e < quads; e += 32) {
+        const int tok = e / (rows_per / 4);
+        const int lr = 4 * (e - tok * (rows_per / 4));
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 2 * C; ++k) {  // senders by rank, set 0 then set 1 of each: a fixed order
+          const float4 a = lds128f(red_base + ((k * p.M + tok) * rows_per + lr) * 4);
+          v.x += a.x;
+          v.y += a.y;
+          v.z += a.z;
+          v.w += a.w;
+        }
+        __half *dst = p.y + static_cast<int64_t>(tok) * p.N + n0 + lr;
+        if (vec_y && n0 + lr + 3 < p.N) {
+          const __half2 lo = __floats2half2_rn(v.x, v.y);
+          const __half2 hi = __floats2half2_rn(v.z, v.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+          *reinterpret_cast<uint2 *>(dst) = pk;
+        } else {
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (n0 + lr + c < p.N) dst[c] = __float2half_rn(vv[c]);
+        }
+      }
+      __syncwarp();
+      if (lane < C) {
+        if (C > 1)
+          mbar_arrive_cluster(free_at_lane);
+        else
+          mbar_arrive(free_at_lane);
+      }
+    }
+  }
+  // no CTA leaves while another CTA of the cluster may still store into its shared memory
+  __syncwarp();
+  if (C > 1)
+    cluster_sync_all();
+  else
+    cta_sync_all();
+}
+
+// Largest number of clusters of `c` CTAs of this kernel that can be resident at once on the current
+// device (cached per device).
+template <int NB8, int MODE>
+int max_clusters(int c, int dev) {
+  using Cfg = DecCfg<NB8, MODE>;
+  static int cache[64][4] = {};
+  static std::mutex mu;
+  const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev >= 0 && dev < 64 && cache[dev][ci] > 0) return cache[dev][ci];
+  auto kern = w4a16_gemm_dec_kernel<NB8, MODE>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c * 64));
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemMax;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  if (dev >= 0 && dev < 64 && n > 0) cache[dev][ci] = n;
+  return n;
+}
+
+template <int NB8, int MODE>
+cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t stream) {
+  using Cfg = DecCfg<NB8, MODE>;
+  auto kern = w4a16_gemm_dec_kernel<NB8, MODE>;
+  static uint64_t done_mask = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 64 || !(done_mask & (1ull << dev))) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemMax);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) done_mask |= 1ull << dev;
+    }
+  }
+  // choose the cluster size (CTAs splitting each tile along K) and the number of clusters: the fewest
+  // stages per CTA, then the smaller cluster
+  int C = cluster, Q = clusters;
+  if (C <= 0) {
+    int best = 0x7FFFFFFF;
+    for (int c : {1, 2, 4, 8}) {
+      if (c > p.KS) break;
+      if (!dec_x_fits(p.KS, c, p.M)) continue;  // the CTA's x range would not fit
+      const int mc = max_clusters<NB8, MODE>(c, dev);
+      if (mc < 1) continue;
+      const int qq = std::min(Q > 0 ? Q : mc, p.NT);
+      const int work = ((p.NT + qq - 1) / qq) * ((p.KS + c - 1) / c);
+      if (work < best) {
+        best = work;
+        C = c;
+      }
+    }
+    if (C <= 0) C = 1;
+  }
+  if (C > p.KS || !dec_x_fits(p.KS, C, p.M)) return cudaErrorInvalidValue;
+  if (Q <= 0) {
+    const int mc = max_clusters<NB8, MODE>(C, dev);
+    Q = mc > 0 ? mc : 1;
+  }
+  Q = std::min(Q, p.NT);
+  p.C = C;
+  p.Q = Q;
+  p.xslice = (p.KS + C - 1) / C;  // the longest K range of a CTA, in stages
+  p.S = Cfg::ring_stages(p.xslice, p.M);
+  if (p.S < 4) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(Q * C));
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(Cfg::smem_bytes(p.xslice, p.M, p.S));
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int NB8>
+cudaError_t launch_dec_nb(const DecParams &p, int clusters, int cluster, cudaStream_t stream) {
+  if (p.g % 256 == 0) return launch_dec_t<NB8, kDecG256>(p, clusters, cluster, stream);
+  if (p.g == 128) return launch_dec_t<NB8, kDecG128>(p, clusters, cluster, stream);
+  if (p.g % 64 == 0) return launch_dec_t<NB8, kDecG64>(p, clusters, cluster, stream);
+  return launch_dec_t<NB8, kDecGen>(p, clusters, cluster, stream);
+}
+
+}  // namespace
+
+namespace detail {
+
+cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int clusters, int cluster, cudaStream_t stream) {
+  if (nb8 == 1) return launch_dec_nb<1>(p, clusters, cluster, stream);
+  if (nb8 == 2) return launch_dec_nb<2>(p, clusters, cluster, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace detail
+}  // namespace w4

@@ -21,8 +21,38 @@ cudaError_t launch_pack(const void *W, int64_t N, int64_t K, int32_t g, uint32_t
 cudaError_t launch_repack(const uint32_t *qw, const void *scales, const uint32_t *zeros, int64_t N, int64_t K,
                           int32_t g, void *packed, cudaStream_t stream);
 
+// Which GEMM kernel runs: the register-operand decode kernel (M <= 16, gemm_dec.cu) or the
+// tensor-memory kernel (gemm.cu).
+constexpr int kKernelAuto = 0;
+constexpr int kKernelDecode = 1;
+constexpr int kKernelTmem = 2;
+
+// The decode kernel keeps each CTA's K range of x in shared memory: M rows of 512 bytes per 256-wide
+// K stage, at most kDecXRegionBytes and kDecXSliceMax stages.
+constexpr int kDecXRegionBytes = 96 * 1024;
+constexpr int kDecXSliceMax = 48;
+inline int64_t dec_x_stages_max(int64_t M) {
+  const int64_t s = kDecXRegionBytes / (512 * M);
+  return s < kDecXSliceMax ? s : kDecXSliceMax;
+}
+// Whether a split of KS stages among C CTAs leaves each CTA a K range of x that fits.
+inline bool dec_x_fits(int64_t KS, int64_t C, int64_t M) { return (KS + C - 1) / C <= dec_x_stages_max(M); }
+
+// Caller choices for one GEMM (zero = automatic); mirrors w4a16_options of the C ABI.
+struct GemmOptions {
+  int kernel = kKernelAuto;
+  int block_n = 0;
+  int ctas = 0;       // tensor-memory kernel: persistent CTAs; decode kernel: clusters
+  int schedule = 0;   // tensor-memory kernel: 1 stream-K, 2 whole tiles
+  int cluster = 0;    // decode kernel: CTAs per cluster (1, 2, 4, 8)
+  bool weights_static = false;
+  uint64_t wait_limit = 0;
+};
+
 struct GemmPlan {
-  int block_n;   // activation rows per tile: 8 (decode kernel), 16, 32, 64 or 128 (tensor-memory kernel)
+  int kernel;    // kKernelDecode or kKernelTmem
+  int cluster;   // decode kernel: forced cluster size (0: chosen at launch)
+  int block_n;   // activation rows per tile: 8 or 16 (decode kernel), 16, 32, 64 or 128 (tensor-memory kernel)
   int m_tiles;
   int n_tiles;
   int k_blocks;
@@ -38,14 +68,14 @@ struct GemmPlan {
   size_t workspace_bytes;
 };
 
-// schedule: 0 automatic, 1 stream-K, 2 whole tiles. ctas: 0 = one per SM.
-// Returns false if block_n / ctas / schedule are not valid values.
-bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, int block_n, int ctas, int schedule, int num_sms,
+// Returns false if the options are not valid values for this problem.
+bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOptions &opt, int num_sms,
                     GemmPlan *plan);
 
 // Launches the GEMM for a validated plan. Returns the CUDA error (cudaSuccess on success);
 // *encode_failed is set when the tensor map could not be built.
 cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y,
-                        void *workspace, const GemmPlan &plan, cudaStream_t stream, bool *encode_failed);
+                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, cudaStream_t stream,
+                        bool *encode_failed);
 
 }  // namespace w4
