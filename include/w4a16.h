@@ -180,12 +180,20 @@ W4_API size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t 
  *            packed weights (true once a model is loaded). The decode kernel
  *            then starts copying its first weight tiles before that kernel
  *            has finished; x is still read only after it.
+ *            W4_FLAG_TEST_TIMEOUT (tests only): one wait of the kernel expects
+ *            more than will ever come -- the decode kernel's reducer a few
+ *            bytes more, the tensor-memory kernel's owner of a cut tile one
+ *            piece more -- so that it runs out after wait_limit_cycles. The
+ *            kernel then stops early without a fault, y is undefined and
+ *            w4_last_device_error reports W4_ERR_TIMEOUT; zero the workspace
+ *            before its next use.
  * wait_limit_cycles  0: about 1.5 s. A pipeline wait inside the kernels gives
  *            up after this many SM clock cycles, sets the workspace error
  *            word (W4_ERR_TIMEOUT from w4_last_device_error) and the kernel
- *            returns early. For tests of that path.
+ *            returns early.
  */
 #define W4_FLAG_WEIGHTS_STATIC 1u
+#define W4_FLAG_TEST_TIMEOUT 2u
 typedef struct {
     int32_t kernel;
     int32_t block_n;

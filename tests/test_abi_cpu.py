@@ -120,7 +120,7 @@ def test_options_validation(lib):
     # the tensor-memory kernel takes no 8-token tiles; unknown flags and kernels are refused
     assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(2, 8, 0, 0, 0, 0, 0)) == 0
     assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(2, 16, 4, 1, 0, 0, 0)) == 256 + 256 + 4 * 2 * 128 * 16 * 4
-    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 2, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 4, 0)) == 0  # no flag 4
     assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(3, 0, 0, 0, 0, 0, 0)) == 0
     assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 1, 0)) == 256
 

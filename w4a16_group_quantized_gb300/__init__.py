@@ -25,12 +25,13 @@ __all__ = [
     "W4Error", "lib_path", "load", "w4_pack", "w4_repack", "w4_repacked_bytes", "w4a16_gemm",
     "w4a16_gemm_ex", "w4a16_gemm_opts", "w4a16_workspace_bytes", "w4a16_workspace_bytes_ex",
     "w4a16_workspace_bytes_opts", "w4a16_gemm_plan", "w4_last_device_error", "w4_status_string", "Workspace",
-    "Options", "STATUS", "KERNEL_DECODE", "KERNEL_TMEM", "FLAG_WEIGHTS_STATIC",
+    "Options", "STATUS", "KERNEL_DECODE", "KERNEL_TMEM", "FLAG_WEIGHTS_STATIC", "FLAG_TEST_TIMEOUT",
 ]
 
 KERNEL_DECODE = 1
 KERNEL_TMEM = 2
 FLAG_WEIGHTS_STATIC = 1
+FLAG_TEST_TIMEOUT = 2
 
 
 class Options(ctypes.Structure):

@@ -46,13 +46,14 @@ int check_gemm_args(const void *x, const void *packed, int64_t M, int64_t N, int
 bool to_options(const w4a16_options *o, w4::GemmOptions *out) {
   *out = w4::GemmOptions{};
   if (!o) return true;
-  if (o->flags & ~W4_FLAG_WEIGHTS_STATIC) return false;
+  if (o->flags & ~(W4_FLAG_WEIGHTS_STATIC | W4_FLAG_TEST_TIMEOUT)) return false;
   out->kernel = o->kernel;
   out->block_n = o->block_n;
   out->ctas = o->ctas;
   out->schedule = o->schedule;
   out->cluster = o->cluster;
   out->weights_static = (o->flags & W4_FLAG_WEIGHTS_STATIC) != 0;
+  out->test_timeout = (o->flags & W4_FLAG_TEST_TIMEOUT) != 0;
   out->wait_limit = o->wait_limit_cycles;
   return true;
 }

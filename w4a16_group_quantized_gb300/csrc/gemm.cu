@@ -167,7 +167,8 @@ __device__ __forceinline__ void produce_stages_pair(const CUtensorMap *x_map, co
     if (i >= S) {  // the consumers are done with the stage this slot held
       const uint32_t ph = ((i / S) - 1) & 1;
       bool ok = true;
-      for (int e = 0; e < nrel && ok; ++e) ok = warp_wait(smem_u32(&rel[e * rel_stride + s]), ph, abort_flag, p.err);
+      for (int e = 0; e < nrel && ok; ++e)
+        ok = warp_wait(smem_u32(&rel[e * rel_stride + s]), ph, abort_flag, p.err, p.wait_limit);
       if (!ok) break;
     }
     if (lane == 0) {
@@ -313,12 +314,13 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
         // wait for every earlier segment's release in order, so no parity wait skips a phase
         for (; ok && seg_freed <= seg - C::kDBufs; ++seg_freed)
           ok = warp_wait(smem_u32(&dempty_bar[seg_freed % C::kDBufs]), (seg_freed / C::kDBufs) & 1, abort_flag,
-                         p.err);
+                         p.err, p.wait_limit);
       }
       const uint32_t dcol = tmem + ((seg % C::kDBufs) * I + e) * C::kDStride;
       // the dequant groups stored their A operands; they saw the stage land before that, which
       // orders the x tile's arrival before these MMAs
-      if (ok) ok = warp_wait(smem_u32(&afull_bar[e][i % C::kASlots]), (i / C::kASlots) & 1, abort_flag, p.err);
+      if (ok)
+        ok = warp_wait(smem_u32(&afull_bar[e][i % C::kASlots]), (i / C::kASlots) & 1, abort_flag, p.err, p.wait_limit);
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
@@ -369,11 +371,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
     it.init(p, u0);
     for (int i = 0; i < nst; ++i, it.advance(p, 1)) {
       const int s = i % S;
-      if (!warp_wait(smem_u32(&full_bar[s]), (i / S) & 1, abort_flag, p.err)) break;
+      if (!warp_wait(smem_u32(&full_bar[s]), (i / S) & 1, abort_flag, p.err, p.wait_limit)) break;
       const bool have = b < stage_blocks<C::kSBK>(p, it.ks);
       // the A slot's previous stage (i - kASlots) must have gone through its MMAs
       if (i >= C::kASlots &&
-          !warp_wait(smem_u32(&mdone_bar[e][(i - C::kASlots) % S]), ((i - C::kASlots) / S) & 1, abort_flag, p.err))
+          !warp_wait(smem_u32(&mdone_bar[e][(i - C::kASlots) % S]), ((i - C::kASlots) / S) & 1, abort_flag, p.err,
+                     p.wait_limit))
         break;
       if (have) {
         const uint32_t stage = smem_base + s * C::kStageBytes;
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
         ok = wait_pieces(p, tile, np, abort_flag);
         npieces_sh = np;
       }
-      const bool landed = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err);
+      const bool landed = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err, p.wait_limit);
       if (!named_bar_and(1, 128, ok && landed)) break;  // (also publishes npieces_sh)
       tc_fence_after();
       // With four or more pieces the owner's own sums go to shared memory (the stage ring is idle:
@@ -807,6 +810,7 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
     p.early = opt.weights_static ? 1 : 0;
     p.gdiv = make_fastdiv(static_cast<uint32_t>(g));
     p.wait_limit = opt.wait_limit ? opt.wait_limit : kWaitLimitCycles;
+    p.test_extra_tx = opt.test_timeout ? 4u : 0u;
     return launch_gemm_dec(p, plan.block_n / 8, plan.ctas, plan.cluster, stream);
   }
   const int sbk = kSB / plan.tiles_per_unit;
@@ -848,6 +852,8 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.x3d = x3d ? 1 : 0;
   p.tstride = plan.interleave ? plan.ctas : 1;
   p.grains = plan.grains;
+  p.wait_limit = opt.wait_limit ? opt.wait_limit : kWaitLimitCycles;
+  p.test_extra_piece = opt.test_timeout ? 1 : 0;
   return launch_variant(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p, plan.ctas,
                         stream);
 }

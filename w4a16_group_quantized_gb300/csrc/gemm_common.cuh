@@ -58,6 +58,8 @@ struct Params {
   int tstride;           // tiles between a CTA's consecutive tiles: 1 (contiguous ranges) or P
   FastDiv gdiv;          // division by g
   int64_t grains;        // total units / gran
+  uint64_t wait_limit;   // cycles a wait may take before the kernel gives up
+  int test_extra_piece;  // test only: owners wait for this many pieces more than will come
 };
 
 __device__ __forceinline__ int64_t range_begin(const Params &p, int c) {
@@ -175,8 +177,8 @@ __device__ __forceinline__ void dequant_word(uint32_t w, const GroupConsts &c, u
 // A wait whose outcome is the same for all 32 lanes: the warp then either executes the
 // following .sync.aligned tcgen05 instructions together or leaves the loop together.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          uint32_t *err) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err);
+                                          uint32_t *err, uint64_t limit) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, err, limit);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -206,11 +208,11 @@ __device__ __forceinline__ const float *piece_of(const Params &p, int c, int slo
 // The owner's wait for the other npieces - 1 pieces of its tile (one thread; the caller's barrier
 // after it orders the other threads' piece reads). Resets the counter. False on abort or timeout.
 __device__ __forceinline__ bool wait_pieces(const Params &p, int tile, int npieces, volatile uint32_t *abort_flag) {
-  const uint32_t target = static_cast<uint32_t>(npieces - 1);
+  const uint32_t target = static_cast<uint32_t>(npieces - 1 + p.test_extra_piece);
   const uint64_t t0 = clock_cycles();
   while (ld_acquire_gpu(&p.counters[tile]) < target) {
     if (*abort_flag) return false;
-    if (clock_cycles() - t0 > kWaitLimitCycles) {
+    if (clock_cycles() - t0 > p.wait_limit) {
       *abort_flag = 1u;
       atomicOr(p.err, kDevErrTimeout);
       return false;
@@ -264,7 +266,8 @@ __device__ __forceinline__ void produce_stages(const CUtensorMap *x_map, const P
     if (i >= S) {  // the consumers are done with the stage this slot held
       const uint32_t ph = ((i / S) - 1) & 1;
       bool ok = true;
-      for (int e = 0; e < nrel && ok; ++e) ok = warp_wait(smem_u32(&rel[e * rel_stride + s]), ph, abort_flag, p.err);
+      for (int e = 0; e < nrel && ok; ++e)
+        ok = warp_wait(smem_u32(&rel[e * rel_stride + s]), ph, abort_flag, p.err, p.wait_limit);
       if (!ok) break;
     }
     if (lane == 0) {
@@ -329,6 +332,7 @@ struct DecParams {
   int xslice;            // 256-wide K stages of x each CTA keeps in shared memory (its longest K range)
   int S;                 // stages in the weight ring (even)
   int early;             // issue the first stages' weight copies before waiting for the previous grid
+  uint32_t test_extra_tx;  // test only: the reducer expects this many bytes more than will come
   FastDiv gdiv;          // division by g
   uint64_t wait_limit;   // cycles a pipeline wait may take before the kernel gives up
 };

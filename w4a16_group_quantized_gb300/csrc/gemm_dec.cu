@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
     const bool vec_y = p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 7) == 0;
     for (int r = 0; r < rounds; ++r) {
       // this tile's partial sums for this CTA's rows: 2 sets x C CTAs x rows_per rows x M tokens x 4 bytes
-      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&recv_bar), 1024u * p.M);
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&recv_bar), 1024u * p.M + p.test_extra_tx);
       if (!dec_warp_wait(smem_u32(&recv_bar), r & 1, true, p, abort_flag)) break;
       const int n0 = (q + r * p.Q) * kTN + rank * rows_per;
       // 4 consecutive rows per lane and step: one 16-byte load per partial, one 8-byte store of y

@@ -46,6 +46,7 @@ struct GemmOptions {
   int schedule = 0;   // tensor-memory kernel: 1 stream-K, 2 whole tiles
   int cluster = 0;    // decode kernel: CTAs per cluster (1, 2, 4, 8)
   bool weights_static = false;
+  bool test_timeout = false;  // test only: one wait expects more than will come (runs out after wait_limit)
   uint64_t wait_limit = 0;
 };
 

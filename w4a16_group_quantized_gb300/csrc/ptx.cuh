@@ -12,8 +12,9 @@ namespace w4 {
 // Device error bits written into the workspace error word.
 constexpr uint32_t kDevErrTimeout = 1u;
 
-// A pipeline wait gives up after this many SM clock cycles (%clock64, local to
-// the SM and cheap to read: about 1.5 s at the top clock of 2.07 GHz).
+// By default a pipeline wait gives up after this many SM clock cycles (%clock64,
+// local to the SM and cheap to read: about 1.5 s at the top clock of 2.07 GHz);
+// the kernels take the limit as a parameter.
 constexpr uint64_t kWaitLimitCycles = 3ull * 1000ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ uint64_t clock_cycles() {
@@ -73,7 +74,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Waits for the phase of `bar` with the given parity to complete. Returns
 // false (and raises the CTA's abort flag and the device error word) when the
-// wait runs past kWaitLimitCycles, or once another thread of the CTA aborted.
+// wait runs past `limit` cycles, or once another thread of the CTA aborted.
 // A waiter that does not succeed at once is parked by the hardware
 // (try_wait with a suspend-time hint) until the phase completes or about
 // kSuspendNs pass: it takes no issue slots meanwhile and resumes as soon as
@@ -82,13 +83,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 constexpr uint32_t kSuspendNs = 20000;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          uint32_t *err_word) {
+                                          uint32_t *err_word, uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = clock_cycles();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
     if (*abort_flag) return false;
-    if (clock_cycles() - t0 > kWaitLimitCycles) {
+    if (clock_cycles() - t0 > limit) {
       *abort_flag = 1u;
       atomicOr(err_word, kDevErrTimeout);
       return false;
