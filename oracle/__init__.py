@@ -59,6 +59,16 @@ def _load():
         lib.orc_double_to_half.restype = ctypes.c_uint16
         lib.orc_quantize.argtypes = [P, I64, I64, I32, P, P, P]
         lib.orc_quantize.restype = ctypes.c_int
+        lib.orc_quantize_ex.argtypes = [P, I64, I64, I32, I32, I32, P, P, P]
+        lib.orc_quantize_ex.restype = ctypes.c_int
+        lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16_to_double.restype = ctypes.c_double
+        lib.orc_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.orc_double_to_bf16.restype = ctypes.c_uint16
+        lib.orc_dequant_ex.argtypes = [P, P, P, I64, I64, I32, I32, P]
+        lib.orc_dequant_ex.restype = None
+        lib.orc_gemm_rows_ex.argtypes = [P, I64, P, I64, P, P, P, I64, I64, I32, I32, P, ctypes.c_int]
+        lib.orc_gemm_rows_ex.restype = ctypes.c_int
         lib.orc_pack_nibbles.argtypes = [P, I64, I64, P]
         lib.orc_pack_nibbles.restype = None
         lib.orc_unpack_nibbles.argtypes = [P, I64, I64, P]
@@ -82,13 +92,26 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+DTYPES = {"f16": 0, "bf16": 1}
+
+
 def _bits(a) -> np.ndarray:
-    """fp16 array (or its uint16 bits) -> contiguous uint16 bits."""
+    """fp16 array (or uint16 bits of fp16 or bf16 values) -> contiguous uint16 bits."""
     a = np.asarray(a)
     if a.dtype == np.float16:
         a = a.view(np.uint16)
     assert a.dtype == np.uint16, a.dtype
     return np.ascontiguousarray(a)
+
+
+def _dt(dtype: str) -> int:
+    if dtype not in DTYPES:
+        raise ValueError(f"dtype must be one of {sorted(DTYPES)}")
+    return DTYPES[dtype]
+
+
+def _scales_out(s: np.ndarray, dtype: str) -> np.ndarray:
+    return s.view(np.float16) if dtype == "f16" else s
 
 
 def ngroups(k: int, g: int) -> int:
@@ -105,20 +128,29 @@ def double_to_half(v: float) -> int:
     return int(_load().orc_double_to_half(float(v)))
 
 
+def bf16_to_double(bits: int) -> float:
+    return _load().orc_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def double_to_bf16(v: float) -> int:
+    return int(_load().orc_double_to_bf16(float(v)))
+
+
 # ------------------------------------------------------------ quantize
 
-def quantize(W, g: int):
-    """W fp16 [N,K] -> (q uint8 [N,K], s fp16 [N,G], z uint8 [N,G])."""
+def quantize(W, g: int, dtype: str = "f16", symmetric: bool = False):
+    """W [N,K] (fp16, or uint16 bits of dtype) -> (q uint8 [N,K], s [N,G], z uint8 [N,G]).
+    s is fp16 for dtype 'f16' and uint16 bf16 bits for 'bf16'. symmetric: z = 8, range +-max|w|."""
     Wb = _bits(W)
     N, K = Wb.shape
     G = ngroups(K, g)
     q = np.zeros((N, K), np.uint8)
     s = np.zeros((N, G), np.uint16)
     z = np.zeros((N, G), np.uint8)
-    rc = _load().orc_quantize(_ptr(Wb), N, K, g, _ptr(q), _ptr(s), _ptr(z))
+    rc = _load().orc_quantize_ex(_ptr(Wb), N, K, g, _dt(dtype), int(bool(symmetric)), _ptr(q), _ptr(s), _ptr(z))
     if rc != 0:
         raise ValueError(f"orc_quantize failed ({rc}): {'non-finite weight' if rc == -2 else 'bad arguments'}")
-    return q, s.view(np.float16), z
+    return q, _scales_out(s, dtype), z
 
 
 def pack_nibbles(v: np.ndarray) -> np.ndarray:
@@ -138,9 +170,9 @@ def unpack_nibbles(words: np.ndarray, cols: int) -> np.ndarray:
     return out
 
 
-def pack(W, g: int):
-    """The canonical packed form: (qw uint32 [N,ceil(K/8)], scales fp16 [N,G], zeros uint32 [N,ceil(G/8)])."""
-    q, s, z = quantize(W, g)
+def pack(W, g: int, dtype: str = "f16", symmetric: bool = False):
+    """The canonical packed form: (qw uint32 [N,ceil(K/8)], scales [N,G], zeros uint32 [N,ceil(G/8)])."""
+    q, s, z = quantize(W, g, dtype, symmetric)
     return pack_nibbles(q), s, pack_nibbles(z)
 
 
@@ -172,18 +204,20 @@ def unrepack(buf, N: int, K: int, g: int):
 
 # ------------------------------------------------------ dequant / gemm
 
-def dequant(qw, scales, zeros, N: int, K: int, g: int) -> np.ndarray:
-    """w [N,K] fp64 = (q - z) * s, exact."""
+def dequant(qw, scales, zeros, N: int, K: int, g: int, dtype: str = "f16") -> np.ndarray:
+    """w [N,K] fp64 = (q - z) * s, exact (s fp16, or bf16 bits for dtype 'bf16')."""
     qw = np.ascontiguousarray(qw, dtype=np.uint32)
     sb = _bits(scales)
     zw = np.ascontiguousarray(zeros, dtype=np.uint32)
     w = np.zeros((N, K), np.float64)
-    _load().orc_dequant(_ptr(qw), _ptr(sb), _ptr(zw), N, K, g, _ptr(w))
+    _load().orc_dequant_ex(_ptr(qw), _ptr(sb), _ptr(zw), N, K, g, _dt(dtype), _ptr(w))
     return w
 
 
-def gemm(x, qw, scales, zeros, N: int, K: int, g: int, rows=None, nthreads: int | None = None) -> np.ndarray:
-    """y [R,N] fp64 = x[rows] . dequant(W)^T by the naive triple loop (rows=None: all M rows)."""
+def gemm(x, qw, scales, zeros, N: int, K: int, g: int, rows=None, nthreads: int | None = None,
+         dtype: str = "f16") -> np.ndarray:
+    """y [R,N] fp64 = x[rows] . dequant(W)^T by the naive triple loop (rows=None: all M rows).
+    x and the scales are fp16, or uint16 bf16 bits for dtype 'bf16'."""
     xb = _bits(x)
     M, Kx = xb.shape
     assert Kx == K
@@ -199,8 +233,8 @@ def gemm(x, qw, scales, zeros, N: int, K: int, g: int, rows=None, nthreads: int 
     y = np.zeros((R, N), np.float64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    rc = _load().orc_gemm_rows(_ptr(xb), M, rows_p, R, _ptr(qw), _ptr(sb), _ptr(zw), N, K, g,
-                               _ptr(y), int(nthreads))
+    rc = _load().orc_gemm_rows_ex(_ptr(xb), M, rows_p, R, _ptr(qw), _ptr(sb), _ptr(zw), N, K, g, _dt(dtype),
+                                  _ptr(y), int(nthreads))
     if rc != 0:
         raise MemoryError("orc_gemm_rows: allocation failed")
     return y

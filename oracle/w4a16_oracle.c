@@ -32,7 +32,12 @@
  *  - codes are packed 8 per uint32 along K, code k = 8c + i in bits
  *    4i..4i+3 of word c; zeros are packed the same way along groups;
  *    padding nibbles are 0;
- *  - non-finite weights are rejected.
+ *  - non-finite weights are rejected;
+ *  - bf16 weights, scales and activations (the 'bf16' precision torchchat
+ *    issue #1362 runs int4 quantization with) follow the same steps, with
+ *    every value of that type widened exactly and s rounded to bfloat16;
+ *  - the symmetric form fixes z at 8 and takes the range [-max|w|, max|w|]
+ *    (r = 2 max|w|); a group of zeros gets s = 1, z = 8, q = 8.
  *
  * Compile with -ffp-contract=off (no fused multiply-add) and no fast-math.
  */
@@ -110,18 +115,93 @@ uint16_t orc_double_to_half(double v)
 }
 
 /* ------------------------------------------------------------------ */
+/* bfloat16, from the format's definition: 1 sign bit, 8 exponent bits */
+/* (bias 127), 7 fraction bits.                                        */
+/* ------------------------------------------------------------------ */
+
+double orc_bf16_to_double(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133); /* subnormal: f * 2^-133 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134); /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* fp64 -> bfloat16, round to nearest, ties to even, in one step. */
+uint16_t orc_double_to_bf16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v))
+        return 0x7fc0;
+    /* halfway between the largest finite value (2 - 2^-7) * 2^127 and 2^128 rounds (to even) up */
+    if (a >= ldexp(2.0 - ldexp(1.0, -8), 127))
+        return sign | 0x7f80;
+    if (a == 0.0)
+        return sign;
+    int E;
+    frexp(a, &E); /* a = f * 2^E, f in [0.5, 1) */
+    int e = E - 1; /* a in [2^e, 2^(e+1)) */
+    if (e < -126) {
+        /* subnormal range: multiples of 2^-133 */
+        double n = round_half_even(ldexp(a, 133));
+        return sign | (uint16_t)n; /* n == 128 is the smallest normal, encoded alike */
+    }
+    double n = round_half_even(ldexp(a, 7 - e)); /* in [128, 256] */
+    if (n == 256.0) {
+        n = 128.0;
+        e += 1;
+    }
+    if (e > 127)
+        return sign | 0x7f80;
+    return sign | (uint16_t)(((e + 127) << 7) | ((int)n - 128));
+}
+
+/* The 16-bit value types of weights, scales and activations: 0 = fp16, 1 = bf16. */
+static double dt_to_double(uint16_t bits, int dtype)
+{
+    return dtype ? orc_bf16_to_double(bits) : orc_half_to_double(bits);
+}
+
+static uint16_t dt_from_double(double v, int dtype)
+{
+    return dtype ? orc_double_to_bf16(v) : orc_double_to_half(v);
+}
+
+static uint16_t dt_one(int dtype) { return dtype ? 0x3f80 : 0x3c00; }
+
+/* ------------------------------------------------------------------ */
 /* Quantization (encoding step).                                       */
 /* ------------------------------------------------------------------ */
 
+/* The least positive value of the type that is >= r / 15: round r / 15 to nearest (ties to even)
+ * straight from fp64, then one step up if 15 times that is still below r. */
+static uint16_t scale_at_least(double r, int dtype)
+{
+    uint16_t sb = dt_from_double(r / 15.0, dtype);
+    if (dt_to_double(sb, dtype) * 15.0 < r) /* exact product: at most 11 + 4 significant bits */
+        sb = (uint16_t)(sb + 1);            /* next value up (sb is positive, finite) */
+    return sb;
+}
+
 /*
- * W [N,K] fp16 bits -> codes q [N,K] (one byte each, 0..15),
- * scales s [N,G] fp16 bits, zeros z [N,G] (one byte each, 0..15).
+ * W [N,K] bits of type `dtype` -> codes q [N,K] (0..15), scales s [N,G] (bits of `dtype`),
+ * zeros z [N,G] (0..15). symmetric == 0: the range of each group includes zero,
+ * [min(0, min w), max(0, max w)], and z places zero on the code grid; symmetric == 1: the
+ * range is [-max|w|, max|w|] and z is 8 for every group.
  * Returns 0, or -1 for bad arguments, -2 for a non-finite weight.
  */
-int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int32_t g,
-                 uint8_t *q, uint16_t *s, uint8_t *z)
+int orc_quantize_ex(const uint16_t *W, int64_t N, int64_t K, int32_t g, int32_t dtype, int32_t symmetric,
+                    uint8_t *q, uint16_t *s, uint8_t *z)
 {
-    if (N < 1 || K < 1 || g < 1)
+    if (N < 1 || K < 1 || g < 1 || dtype < 0 || dtype > 1 || symmetric < 0 || symmetric > 1)
         return -1;
     int64_t G = (K + g - 1) / g;
     for (int64_t n = 0; n < N; ++n) {
@@ -130,7 +210,7 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int32_t g,
             int64_t k1 = k0 + g < K ? k0 + g : K; /* last group may be narrower */
             double lo = 0.0, hi = 0.0;
             for (int64_t k = k0; k < k1; ++k) {
-                double w = orc_half_to_double(W[n * K + k]);
+                double w = dt_to_double(W[n * K + k], dtype);
                 if (!isfinite(w))
                     return -2;
                 if (w < lo)
@@ -138,28 +218,33 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int32_t g,
                 if (w > hi)
                     hi = w;
             }
+            if (symmetric) {
+                double amax = hi > -lo ? hi : -lo;
+                lo = -amax;
+                hi = amax;
+            }
             double r = hi - lo;
             uint16_t sb;
             int zj;
             if (r == 0.0) {
-                sb = 0x3c00; /* 1.0 */
-                zj = 0;
+                sb = dt_one(dtype);
+                zj = symmetric ? 8 : 0;
             } else {
-                sb = orc_double_to_half(r / 15.0);
-                double sv = orc_half_to_double(sb);
-                if (sv * 15.0 < r) /* exact product: 11 + 4 significant bits */
-                    sb = (uint16_t)(sb + 1); /* next fp16 up (sb is positive, finite) */
-                sv = orc_half_to_double(sb);
-                double zz = rne_int(-lo / sv);
-                zj = zz < 0 ? 0 : (zz > 15 ? 15 : (int)zz);
+                sb = scale_at_least(r, dtype);
+                if (symmetric) {
+                    zj = 8;
+                } else {
+                    double zz = rne_int(-lo / dt_to_double(sb, dtype));
+                    zj = zz < 0 ? 0 : (zz > 15 ? 15 : (int)zz);
+                }
             }
             s[n * G + j] = sb;
             z[n * G + j] = (uint8_t)zj;
-            double sv = orc_half_to_double(sb);
+            double sv = dt_to_double(sb, dtype);
             for (int64_t k = k0; k < k1; ++k) {
-                int qk = 0;
+                int qk = zj; /* r == 0: every weight is 0 and encodes as z */
                 if (r != 0.0) {
-                    double w = orc_half_to_double(W[n * K + k]);
+                    double w = dt_to_double(W[n * K + k], dtype);
                     double t = rne_int(w / sv) + (double)zj;
                     qk = t < 0 ? 0 : (t > 15 ? 15 : (int)t);
                 }
@@ -168,6 +253,12 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int32_t g,
         }
     }
     return 0;
+}
+
+/* fp16 weights, range including zero (the default form). */
+int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int32_t g, uint8_t *q, uint16_t *s, uint8_t *z)
+{
+    return orc_quantize_ex(W, N, K, g, 0, 0, q, s, z);
 }
 
 /* ------------------------------------------------------------------ */
@@ -309,25 +400,31 @@ void orc_unrepack(const uint8_t *in, int64_t N, int64_t K, int32_t g,
 /* Dequantize and multiply.                                            */
 /* ------------------------------------------------------------------ */
 
-/* One row of weights: w[k] = (q - z) * s, exact in fp64. */
+/* One row of weights: w[k] = (q - z) * s, exact in fp64 (s of type `dtype`). */
 static void dequant_row(const uint32_t *qw, const uint16_t *scales, const uint32_t *zw,
-                        int64_t n, int64_t K, int32_t g, double *w)
+                        int64_t n, int64_t K, int32_t g, int dtype, double *w)
 {
     int64_t G = cdiv(K, g), Kw = cdiv(K, 8), Gw = cdiv(G, 8);
     for (int64_t k = 0; k < K; ++k) {
         int64_t j = k / g;
         int qk = (int)((qw[n * Kw + k / 8] >> (4 * (k % 8))) & 0xf);
         int zj = (int)((zw[n * Gw + j / 8] >> (4 * (j % 8))) & 0xf);
-        double s = orc_half_to_double(scales[n * G + j]);
+        double s = dt_to_double(scales[n * G + j], dtype);
         w[k] = (double)(qk - zj) * s;
     }
+}
+
+void orc_dequant_ex(const uint32_t *qw, const uint16_t *scales, const uint32_t *zw,
+                    int64_t N, int64_t K, int32_t g, int32_t dtype, double *w)
+{
+    for (int64_t n = 0; n < N; ++n)
+        dequant_row(qw, scales, zw, n, K, g, dtype, w + n * K);
 }
 
 void orc_dequant(const uint32_t *qw, const uint16_t *scales, const uint32_t *zw,
                  int64_t N, int64_t K, int32_t g, double *w)
 {
-    for (int64_t n = 0; n < N; ++n)
-        dequant_row(qw, scales, zw, n, K, g, w + n * K);
+    orc_dequant_ex(qw, scales, zw, N, K, g, 0, w);
 }
 
 struct gemm_job {
@@ -338,6 +435,7 @@ struct gemm_job {
     const uint32_t *zw;
     int64_t N, K;
     int32_t g;
+    int dtype;
     double *y; /* [R, N] */
     int64_t n_begin, n_end;
 };
@@ -349,7 +447,7 @@ static void *gemm_worker(void *arg)
     if (!w)
         return (void *)1;
     for (int64_t n = jb->n_begin; n < jb->n_end; ++n) {
-        dequant_row(jb->qw, jb->scales, jb->zw, n, jb->K, jb->g, w);
+        dequant_row(jb->qw, jb->scales, jb->zw, n, jb->K, jb->g, jb->dtype, w);
         for (int64_t m = 0; m < jb->R; ++m) {
             const double *xm = jb->x + m * jb->K;
             double acc = 0.0;
@@ -364,13 +462,13 @@ static void *gemm_worker(void *arg)
 
 /*
  * y[r, n] = sum_k x[rows[r], k] * w[n, k] for the listed activation rows
- * (rows == NULL: all M rows in order, R == M). x is fp16 bits [M, K];
- * y is fp64 [R, N], never rounded. Threads split the n range.
- * Returns 0, or -1 on allocation failure.
+ * (rows == NULL: all M rows in order, R == M). x is [M, K] bits of type `dtype`
+ * (0 fp16, 1 bf16; the scales are of the same type); y is fp64 [R, N], never
+ * rounded. Threads split the n range. Returns 0, or -1 on allocation failure.
  */
-int orc_gemm_rows(const uint16_t *x, int64_t M, const int64_t *rows, int64_t R,
-                  const uint32_t *qw, const uint16_t *scales, const uint32_t *zw,
-                  int64_t N, int64_t K, int32_t g, double *y, int nthreads)
+int orc_gemm_rows_ex(const uint16_t *x, int64_t M, const int64_t *rows, int64_t R,
+                     const uint32_t *qw, const uint16_t *scales, const uint32_t *zw,
+                     int64_t N, int64_t K, int32_t g, int32_t dtype, double *y, int nthreads)
 {
     (void)M;
     double *xd = (double *)malloc(sizeof(double) * (size_t)(R * K));
@@ -379,7 +477,7 @@ int orc_gemm_rows(const uint16_t *x, int64_t M, const int64_t *rows, int64_t R,
     for (int64_t r = 0; r < R; ++r) {
         int64_t src = rows ? rows[r] : r;
         for (int64_t k = 0; k < K; ++k)
-            xd[r * K + k] = orc_half_to_double(x[src * K + k]);
+            xd[r * K + k] = dt_to_double(x[src * K + k], dtype);
     }
     if (nthreads < 1)
         nthreads = 1;
@@ -395,7 +493,7 @@ int orc_gemm_rows(const uint16_t *x, int64_t M, const int64_t *rows, int64_t R,
         return -1;
     }
     for (int i = 0; i < nthreads; ++i) {
-        jobs[i] = (struct gemm_job){xd, R, qw, scales, zw, N, K, g, y,
+        jobs[i] = (struct gemm_job){xd, R, qw, scales, zw, N, K, g, dtype, y,
                                     N * i / nthreads, N * (i + 1) / nthreads};
         if (pthread_create(&th[i], NULL, gemm_worker, &jobs[i]) != 0) {
             gemm_worker(&jobs[i]);
@@ -413,4 +511,12 @@ int orc_gemm_rows(const uint16_t *x, int64_t M, const int64_t *rows, int64_t R,
     free(jobs);
     free(th);
     return rc;
+}
+
+/* fp16 activations and scales (the default form). */
+int orc_gemm_rows(const uint16_t *x, int64_t M, const int64_t *rows, int64_t R,
+                  const uint32_t *qw, const uint16_t *scales, const uint32_t *zw,
+                  int64_t N, int64_t K, int32_t g, double *y, int nthreads)
+{
+    return orc_gemm_rows_ex(x, M, rows, R, qw, scales, zw, N, K, g, 0, y, nthreads);
 }

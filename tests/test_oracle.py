@@ -1,9 +1,10 @@
 """Pins for the CPU oracle, checked against things other than the oracle itself.
 
 Each test ties an oracle function to an independent fact: numpy's IEEE
-binary16 conversion, exact rational arithmetic (``fractions.Fraction``), a
-closed form, an invariant proved from the definition, a library matmul, or a
-value derived by hand in ``tests/golden/``. None of them calls the CUDA path.
+binary16 and binary32 conversions (bfloat16 is the top half of a binary32),
+exact rational arithmetic (``fractions.Fraction``), a closed form, an invariant
+proved from the definition, a library matmul, or a value derived by hand in
+``tests/golden/``. None of them calls the CUDA path.
 """
 from __future__ import annotations
 
@@ -375,3 +376,201 @@ def test_gemm_is_linear_in_x():
     w = oracle.dequant(qw, s, zw, N, K, g)
     mag = (np.abs(x1.astype(np.float64)) + np.abs(x2.astype(np.float64))) @ np.abs(w).T
     assert (np.abs(ya - yb) <= 1e-13 * mag).all()
+
+
+# ------------------------------------------------------------------ bf16, symmetric
+
+
+def _bf16_val(b: int) -> float:
+    """bf16 bits -> value through numpy's IEEE float32 (bf16 is the top half of a float32)."""
+    return float(np.array([int(b) << 16], np.uint32).view(np.float32)[0])
+
+
+def _bf16_rne_exact(v: float) -> int:
+    """Exact round-to-nearest-even of a finite fp64 value to bfloat16 bits, by search over the grid
+    in rational arithmetic (an independent formulation)."""
+    if v == 0:
+        return 0x8000 if np.signbit(v) else 0
+    sign = 0x8000 if v < 0 else 0
+    a = Fraction(abs(v))
+    if a >= Fraction(2) ** 128 - Fraction(2) ** 119:  # the midpoint above the largest finite value
+        return sign | 0x7F80
+    # largest bf16 (bits, positive) whose value is <= a, by bisection over the ordered bit patterns
+    lo, hi = 0, 0x7F7F
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if Fraction(_bf16_val(mid)) <= a:
+            lo = mid
+        else:
+            hi = mid - 1
+    below = lo
+    if Fraction(_bf16_val(below)) == a:
+        return sign | below
+    above = below + 1
+    d_lo = a - Fraction(_bf16_val(below))
+    d_hi = (Fraction(2) ** 128 if above == 0x7F80 else Fraction(_bf16_val(above))) - a
+    pick = below if d_lo < d_hi else above if d_hi < d_lo else (below if below % 2 == 0 else above)
+    return sign | pick
+
+
+def test_bf16_decode_matches_float32_for_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (bits << 16).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+
+
+def test_bf16_encode_rounds_to_nearest_even():
+    rng = np.random.default_rng(321)
+    # values that are exact float32: the bf16 rounding of the float32 bit pattern (ties to even on
+    # the low 16 bits) is an independent statement of the same rounding
+    f32 = (np.exp2(rng.uniform(-140, 127, 3000)) * rng.choice([-1.0, 1.0], 3000)).astype(np.float32)
+    u = f32.view(np.uint32).astype(np.uint64)
+    ref = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    got = np.array([oracle.double_to_bf16(float(v)) for v in f32], dtype=np.uint16)
+    fin = np.isfinite(f32) & (np.abs(f32) < 3.3e38)
+    assert (got[fin] == ref[fin]).all()
+    # fp64 values between bf16 neighbours, exact ties, subnormals, overflow: exact rational rounding
+    vals = [1.0, 1.0 + 2.0**-8, 1.0 + 3 * 2.0**-8, -(1.0 + 2.0**-8 + 2.0**-40), 2.0**-133, 2.0**-134,
+            3 * 2.0**-135, 2.0**-126 - 2.0**-134, 3.3895313892515355e38, 3.39e38, -1e39, 0.333333333333]
+    vals += list(rng.standard_normal(500) * np.exp2(rng.uniform(-130, 120, 500)))
+    b = rng.integers(1, 0x7F7F, 300)
+    mids = [(_bf16_val(v) + _bf16_val(v + 1)) / 2 for v in b]  # exact in fp64
+    vals += mids + [np.nextafter(m, 0) for m in mids]
+    for v in vals:
+        assert oracle.double_to_bf16(v) == _bf16_rne_exact(v), v
+    # hand values: ties go to the even neighbour
+    assert oracle.double_to_bf16(1.0 + 2.0**-8) == 0x3F80
+    assert oracle.double_to_bf16(1.0 + 3 * 2.0**-8) == 0x3F82
+    assert oracle.double_to_bf16(2.0**-133) == 0x0001
+    assert oracle.double_to_bf16(3.4e38) == 0x7F80
+
+
+def _dtype_val(b: int, dtype: str) -> Fraction:
+    return Fraction(_bf16_val(b)) if dtype == "bf16" else _val_bits(b)
+
+
+def _smallest_at_least(r: Fraction, dtype: str) -> int:
+    """Exact: the least positive value of the type (bits) that is >= r."""
+    b = _bf16_rne_exact(float(r)) if dtype == "bf16" else int(np.float16(float(r)).view(np.uint16))
+    b &= 0x7FFF
+    while _dtype_val(b, dtype) < r:
+        b += 1
+    while b > 0 and _dtype_val(b - 1, dtype) >= r:
+        b -= 1
+    return b
+
+
+def _quantize_exact_ex(w, K: int, g: int, dtype: str, symmetric: bool):
+    """The definition in exact rational arithmetic for either type and either form."""
+    one = 0x3F80 if dtype == "bf16" else 0x3C00
+    G = -(-K // g)
+    q, s, z = [0] * K, [0] * G, [0] * G
+    for j in range(G):
+        grp = w[j * g:min((j + 1) * g, K)]
+        lo, hi = min([Fraction(0)] + grp), max([Fraction(0)] + grp)
+        if symmetric:
+            amax = max(hi, -lo)
+            lo, hi = -amax, amax
+        r = hi - lo
+        zj = 8 if symmetric else 0
+        if r == 0:
+            s[j], z[j] = one, zj
+            for i in range(len(grp)):
+                q[j * g + i] = zj
+            continue
+        sb = _smallest_at_least(r / 15, dtype)
+        sv = _dtype_val(sb, dtype)
+        if not symmetric:
+            zj = min(15, max(0, round(-lo / sv)))
+        s[j], z[j] = sb, zj
+        for i, wk in enumerate(grp):
+            q[j * g + i] = min(15, max(0, round(wk / sv) + zj))
+    return q, s, z
+
+
+@pytest.mark.parametrize("dtype,symmetric", [("f16", True), ("bf16", False), ("bf16", True)])
+@pytest.mark.parametrize("K,g,seed", [(40, 16, 1), (24, 8, 2), (100, 32, 3), (288, 256, 4), (7, 8, 6)])
+def test_quantize_variants_equal_exact_rational_definition(dtype, symmetric, K, g, seed):
+    rng = np.random.default_rng(seed + 100)
+    N = 5
+    Wf = (rng.standard_normal((N, K)) * rng.choice([0.02, 1.0, 300.0], (N, 1))).astype(np.float32)
+    Wf[0, : min(K, g)] = 0
+    Wf[1] = np.abs(Wf[1])
+    Wf[2] = -np.abs(Wf[2])
+    if dtype == "bf16":
+        W = workloads.f32_to_bf16_bits(Wf)
+        vals = [[Fraction(_bf16_val(b)) for b in row] for row in W]
+    else:
+        W = Wf.astype(np.float16)
+        vals = [[_fr(v) for v in row] for row in W]
+    q, s, z = oracle.quantize(W, g, dtype=dtype, symmetric=symmetric)
+    sbits = s.view(np.uint16) if dtype == "f16" else s
+    for n in range(N):
+        qe, se, ze = _quantize_exact_ex(vals[n], K, g, dtype, symmetric)
+        assert list(q[n]) == qe
+        assert list(sbits[n]) == se
+        assert list(z[n]) == ze
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_symmetric_invariants(dtype):
+    N, K, g = 64, 1000, 128
+    W = workloads.weights_bf16(N, K, seed=8) if dtype == "bf16" else workloads.weights_f16(N, K, seed=8)
+    q, s, z = oracle.quantize(W, g, dtype=dtype, symmetric=True)
+    assert (z == 8).all() and q.max() <= 15
+    sbits = s.view(np.uint16) if dtype == "f16" else s
+    dec = (lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)) if dtype == "bf16" else \
+        (lambda b: b.view(np.float16).astype(np.float64))
+    w = dec(W if dtype == "bf16" else W.view(np.uint16))
+    sv = dec(sbits)
+    idx = np.arange(K) // g
+    what = (q.astype(np.float64) - 8) * sv[:, idx]
+    assert (np.abs(w - what) <= sv[:, idx] / 2 * (1 + 2.0**-40)).all()
+    for j in range(oracle.ngroups(K, g)):
+        amax = np.abs(w[:, j * g:min((j + 1) * g, K)]).max(1)
+        assert (15 * sv[:, j] >= 2 * amax).all()
+        prev = dec((sbits[:, j] - 1).astype(np.uint16))
+        assert (15 * prev < 2 * amax).all()
+
+
+def test_quantize_variants_hand_derived():
+    for name, dtype, sym, ws, sbits, zz, codes in _read_golden("quantize_variants.txt"):
+        vals = np.array([float(v) for v in ws.split()], np.float32)
+        W = workloads.f32_to_bf16_bits(vals)[None, :] if dtype == "bf16" else vals.astype(np.float16)[None, :]
+        q, s, z = oracle.quantize(W, 8, dtype=dtype, symmetric=bool(int(sym)))
+        sb = s.view(np.uint16) if dtype == "f16" else s
+        assert int(sb[0, 0]) == int(sbits, 16), name
+        assert int(z[0, 0]) == int(zz), name
+        assert list(q[0]) == [int(c) for c in codes.split()], name
+
+
+@pytest.mark.parametrize("dtype,symmetric", [("bf16", False), ("bf16", True), ("f16", True)])
+def test_gemm_variants_one_hot_and_matmul(dtype, symmetric):
+    N, K, g, M = 70, 200, 64, 5
+    W = workloads.weights_bf16(N, K, seed=9) if dtype == "bf16" else workloads.weights_f16(N, K, seed=9)
+    qw, s, zw = oracle.pack(W, g, dtype=dtype, symmetric=symmetric)
+    wd = oracle.dequant(qw, s, zw, N, K, g, dtype=dtype)
+    # the dequantized weights are the exact products (q - z) s of the type's scale values
+    q = oracle.unpack_nibbles(qw, K).astype(np.float64)
+    z = oracle.unpack_nibbles(zw, oracle.ngroups(K, g)).astype(np.float64)
+    sv = ((s.astype(np.uint32) << 16).view(np.float32) if dtype == "bf16" else s).astype(np.float64)
+    idx = np.arange(K) // g
+    assert (wd == (q - z[:, idx]) * sv[:, idx]).all()
+    # one-hot activation rows return weight columns exactly
+    ks = [0, 63, 64, 199]
+    one = 0x3F80 if dtype == "bf16" else 0x3C00
+    x = np.zeros((len(ks), K), np.uint16)
+    for i, k in enumerate(ks):
+        x[i, k] = one
+    y = oracle.gemm(x if dtype == "bf16" else x.view(np.float16), qw, s, zw, N, K, g, dtype=dtype)
+    assert (y == wd[:, ks].T).all()
+    # random activations against numpy's fp64 matmul
+    xb = workloads.activations_bf16(M, K) if dtype == "bf16" else workloads.activations_f16(M, K)
+    xv = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64) if dtype == "bf16" else \
+        xb.astype(np.float64)
+    y = oracle.gemm(xb, qw, s, zw, N, K, g, dtype=dtype)
+    assert np.allclose(y, xv @ wd.T, rtol=1e-13, atol=1e-13)

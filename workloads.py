@@ -47,6 +47,32 @@ def activations_f16(m: int, k: int, seed: int = SEED_X, outliers: bool = False) 
     return x.astype(np.float16)
 
 
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 values -> uint16 bits of the nearest bfloat16 (ties to even; inputs finite). Input
+    generation only: bf16 weights and activations are drawn as float32 and then cast."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def weights_bf16(n: int, k: int, seed: int = SEED_W, std: float = 0.02) -> np.ndarray:
+    """bf16 source weights W [n, k] as uint16 bits (the same normal draw as weights_f16)."""
+    rng = np.random.default_rng(seed)
+    w = rng.standard_normal((n, k), dtype=np.float32)
+    w *= np.float32(std)
+    return f32_to_bf16_bits(w)
+
+
+def activations_bf16(m: int, k: int, seed: int = SEED_X, outliers: bool = False) -> np.ndarray:
+    """bf16 activations x [m, k] as uint16 bits; with ``outliers`` 1 % of channels are scaled by 20."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((m, k), dtype=np.float32)
+    if outliers:
+        n_out = int(math.ceil(0.01 * k))
+        cols = np.random.default_rng(SEED_OUTLIER).permutation(k)[:n_out]
+        x[:, cols] *= np.float32(20.0)
+    return f32_to_bf16_bits(x)
+
+
 @dataclass(frozen=True)
 class Layer:
     """One linear layer shape: y[M, N] = x[M, K] . W[N, K]^T, group size g."""
