@@ -83,6 +83,27 @@ W4_API const char *w4_status_string(int status);
 W4_API int w4_pack(const void *W_dev, int64_t N, int64_t K, int32_t g,
             uint32_t *qw_dev, void *scales_dev, uint32_t *zeros_dev, void *stream);
 
+/* Value types of weights, scales, activations and outputs. */
+#define W4_DTYPE_F16 0
+#define W4_DTYPE_BF16 1
+
+/*
+ * w4_pack_ex -- w4_pack for fp16 or bf16 weights, asymmetric or symmetric.
+ *
+ * dtype      W4_DTYPE_F16 or W4_DTYPE_BF16: the type of W and of the scales
+ *            written (bf16: the 'bf16' precision torchchat issue #1362 runs
+ *            'linear:int4' quantization with).
+ * symmetric  0: the zero-point form of w4_pack. 1: z = 8 for every group and
+ *            the range [-m, m], m = max|w| over the group: s is the least
+ *            value of the type with 15 s >= 2 m (s = 1 for an all-zero
+ *            group), q = clamp(rint(w / s) + 8, 0, 15); |w - (q - 8) s| <= s/2.
+ * Other arguments, layouts and guarantees as w4_pack (the zeros buffer holds
+ * 8 in every nibble for symmetric weights, so the GEMM takes them unchanged).
+ * Returns W4_ERR_INVALID_ARG for another dtype or symmetric value.
+ */
+W4_API int w4_pack_ex(const void *W_dev, int64_t N, int64_t K, int32_t g, int32_t dtype, int32_t symmetric,
+                      uint32_t *qw_dev, void *scales_dev, uint32_t *zeros_dev, void *stream);
+
 /*
  * Size in bytes of the GEMM's tile layout for an [N, K] weight with group size g:
  *   ceil(N/128) * ceil(K/64) * 4096 + ceil(N/128) * ceil(K/g) * 320.

@@ -61,6 +61,56 @@ def test_pack_wide_dynamic_range():
     assert (qw == oq).all() and (s.view(np.uint16) == os_.view(np.uint16)).all() and (zw == oz).all()
 
 
+def _pack_gpu_ex(Wbits, g, dtype, symmetric):
+    t = torch.from_numpy(Wbits.view(np.int16)).cuda().view(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    qw, s, zw = w4.w4_pack(t, g, symmetric=symmetric)
+    torch.cuda.synchronize()
+    assert s.dtype == t.dtype
+    return (qw.cpu().numpy().view(np.uint32), s.view(torch.int16).cpu().numpy().view(np.uint16),
+            zw.cpu().numpy().view(np.uint32))
+
+
+VARIANT_CASES = [(256, 512, 128), (288, 288, 256), (100, 1001, 8), (130, 200, 24), (4096, 4096, 128)]
+
+
+@pytest.mark.parametrize("dtype,symmetric", [("f16", True), ("bf16", False), ("bf16", True)])
+@pytest.mark.parametrize("N,K,g", VARIANT_CASES)
+def test_pack_variants_bit_exact(N, K, g, dtype, symmetric):
+    if dtype == "bf16":
+        W = workloads.weights_bf16(N, K, seed=N + K)
+    else:
+        W = workloads.weights_f16(N, K, seed=N + K).view(np.uint16)
+    W = W.copy()
+    W[0, :] = 0                                # all-zero groups: s = 1, every code = z
+    W[min(1, N - 1), :] &= np.uint16(0x7FFF)   # a non-negative row
+    W[min(2, N - 1), : K // 2] |= np.uint16(0x8000)  # a non-positive half row
+    qw, s, zw = _pack_gpu_ex(W, g, dtype, symmetric)
+    oq, os_, oz = oracle.pack(W if dtype == "bf16" else W.view(np.float16), g, dtype, symmetric)
+    assert (qw == oq).all()
+    assert (s == os_.view(np.uint16)).all()
+    assert (zw == oz).all()
+    if symmetric:
+        G = oracle.ngroups(K, g)
+        assert (oracle.unpack_nibbles(zw, G) == 8).all()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_pack_variants_wide_range(dtype):
+    # magnitudes across the type's range, subnormal-sized groups included
+    rng = np.random.default_rng(10)
+    N, K, g = 64, 256, 32
+    if dtype == "bf16":
+        mag = np.exp2(rng.uniform(-130, 120, (N, 1)))
+        W = workloads.f32_to_bf16_bits((rng.standard_normal((N, K)) * mag).astype(np.float32))
+    else:
+        mag = np.exp2(rng.uniform(-24, 15, (N, 1)))
+        W = (rng.standard_normal((N, K)) * mag).clip(-60000, 60000).astype(np.float16).view(np.uint16)
+    for symmetric in (False, True):
+        qw, s, zw = _pack_gpu_ex(W, g, dtype, symmetric)
+        oq, os_, oz = oracle.pack(W if dtype == "bf16" else W.view(np.float16), g, dtype, symmetric)
+        assert (qw == oq).all() and (s == os_.view(np.uint16)).all() and (zw == oz).all(), symmetric
+
+
 @pytest.mark.parametrize("N,K,g", PACK_CASES + [(1, 8, 8), (129, 72, 8)])
 def test_repack_bit_exact(N, K, g):
     # canonical input from the oracle, so repack is checked on its own

@@ -72,6 +72,7 @@ def load() -> ctypes.CDLL:
         sigs = {
             "w4_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "w4_pack": ([P, I64, I64, I32, P, P, P, P], ctypes.c_int),
+            "w4_pack_ex": ([P, I64, I64, I32, I32, I32, P, P, P, P], ctypes.c_int),
             "w4_repacked_bytes": ([I64, I64, I32], SZ),
             "w4_repack": ([P, P, P, I64, I64, I32, P, P], ctypes.c_int),
             "w4a16_workspace_bytes": ([I64, I64, I64, I32], SZ),
@@ -119,17 +120,21 @@ def _ngroups(K: int, g: int) -> int:
     return -(-K // g)
 
 
-def w4_pack(W: torch.Tensor, g: int, stream=None):
-    """fp16 W [N,K] (cuda) -> (qw int32 [N,ceil(K/8)], scales fp16 [N,G], zeros int32 [N,ceil(G/8)])."""
-    if W.dtype != torch.float16 or W.dim() != 2:
-        raise ValueError("W must be a 2-D fp16 tensor")
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+
+
+def w4_pack(W: torch.Tensor, g: int, stream=None, symmetric: bool = False):
+    """fp16 or bf16 W [N,K] (cuda) -> (qw int32 [N,ceil(K/8)], scales [N,G] of W's dtype,
+    zeros int32 [N,ceil(G/8)]). symmetric: z = 8 and the range +-max|w| (w4_pack_ex)."""
+    if W.dtype not in _DTYPES or W.dim() != 2:
+        raise ValueError("W must be a 2-D fp16 or bf16 tensor")
     N, K = W.shape
     G = _ngroups(K, g) if g > 0 else 1
     qw = torch.empty((N, -(-K // 8)), dtype=torch.int32, device=W.device)
-    scales = torch.empty((N, G), dtype=torch.float16, device=W.device)
+    scales = torch.empty((N, G), dtype=W.dtype, device=W.device)
     zeros = torch.empty((N, -(-G // 8)), dtype=torch.int32, device=W.device)
-    _check(load().w4_pack(_dev(W, "W"), N, K, g, _dev(qw, "qw"), _dev(scales, "scales"), _dev(zeros, "zeros"),
-                          _stream(stream)), "w4_pack")
+    _check(load().w4_pack_ex(_dev(W, "W"), N, K, g, _DTYPES[W.dtype], int(bool(symmetric)), _dev(qw, "qw"),
+                             _dev(scales, "scales"), _dev(zeros, "zeros"), _stream(stream)), "w4_pack")
     return qw, scales, zeros
 
 

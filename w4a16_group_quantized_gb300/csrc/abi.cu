@@ -112,16 +112,23 @@ const char *w4_status_string(int status) {
   }
 }
 
-int w4_pack(const void *W_dev, int64_t N, int64_t K, int32_t g, uint32_t *qw_dev, void *scales_dev,
-            uint32_t *zeros_dev, void *stream) {
+int w4_pack_ex(const void *W_dev, int64_t N, int64_t K, int32_t g, int32_t dtype, int32_t symmetric,
+               uint32_t *qw_dev, void *scales_dev, uint32_t *zeros_dev, void *stream) {
   if (!W_dev || !qw_dev || !scales_dev || !zeros_dev) return W4_ERR_INVALID_ARG;
   if (N < 1 || K < 1 || !valid_group(g)) return W4_ERR_INVALID_ARG;
+  if ((dtype != W4_DTYPE_F16 && dtype != W4_DTYPE_BF16) || (symmetric != 0 && symmetric != 1))
+    return W4_ERR_INVALID_ARG;
   if (N > kMaxDim || K > kMaxDim || N * K > (int64_t{1} << 40)) return W4_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(W_dev, 2) || !aligned(qw_dev, 4) || !aligned(scales_dev, 2) || !aligned(zeros_dev, 4))
     return W4_ERR_MISALIGNED;
-  const cudaError_t e =
-      w4::launch_pack(W_dev, N, K, g, qw_dev, scales_dev, zeros_dev, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = w4::launch_pack(W_dev, N, K, g, dtype, symmetric != 0, qw_dev, scales_dev, zeros_dev,
+                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+int w4_pack(const void *W_dev, int64_t N, int64_t K, int32_t g, uint32_t *qw_dev, void *scales_dev,
+            uint32_t *zeros_dev, void *stream) {
+  return w4_pack_ex(W_dev, N, K, g, W4_DTYPE_F16, 0, qw_dev, scales_dev, zeros_dev, stream);
 }
 
 size_t w4_repacked_bytes(int64_t N, int64_t K, int32_t g) {

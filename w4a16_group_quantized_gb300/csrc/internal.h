@@ -15,8 +15,12 @@ constexpr int kRecBytes = 320;   // 128 fp16 scales + 128 4-bit zeros
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-cudaError_t launch_pack(const void *W, int64_t N, int64_t K, int32_t g, uint32_t *qw, void *scales,
-                        uint32_t *zeros, cudaStream_t stream);
+// 16-bit value types of weights, scales, activations and outputs.
+constexpr int kDtypeF16 = 0;
+constexpr int kDtypeBf16 = 1;
+
+cudaError_t launch_pack(const void *W, int64_t N, int64_t K, int32_t g, int dtype, bool symmetric, uint32_t *qw,
+                        void *scales, uint32_t *zeros, cudaStream_t stream);
 
 cudaError_t launch_repack(const uint32_t *qw, const void *scales, const uint32_t *zeros, int64_t N, int64_t K,
                           int32_t g, void *packed, cudaStream_t stream);
