@@ -53,6 +53,11 @@ L2_FLUSH_BYTES = 512 << 20
 DOM_M = 8
 DOM_KERNEL = "w4a16_gemm_dec_kernel"
 DOM_SOURCES = ("gemm_dec.cu", "gemm_common.cuh", "ptx.cuh")
+# bf16 points (per M and decode layer) and the fused epilogues (fused qkv split by 128-wide heads; gate/up
+# rows read as interleaved gate, up for silu(gate) * up), timed beside the fp16 sweep
+BF16_MS = (1, 8, 16, 128)
+EPI_LAYERS = {"qkv_fused_12288x4096": "qkv", "gate_up_fused_22016x4096": "silu"}
+EPI_MS = (1, 8, 64)
 TRAFFIC_FILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "decode_kernel_traffic.json")
 
 
@@ -298,7 +303,8 @@ def run_gpu(args):
         for m, L in sweep():
             c = copies[L.name]
             if part is None or (m <= DOM_M) == (part == 0):
-                w4.w4a16_gemm(xs[m][L.k], c[use[L.name] % 3], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
+                w4.w4a16_gemm(xs[m][L.k], c[use[L.name] % 3], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws,
+                              weights_static=True)
             use[L.name] += 1
 
     # warm-up launches outside capture (per-device kernel attributes), then capture the step
@@ -366,7 +372,8 @@ def run_gpu(args):
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=stream):
             for i in range(R):
-                w4.w4a16_gemm(xs[m][L.k], c[i], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
+                w4.w4a16_gemm(xs[m][L.k], c[i], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws,
+                              weights_static=True)
         with torch.cuda.stream(stream):
             g2.replay()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -389,6 +396,82 @@ def run_gpu(args):
                     "roofline_frac": round(max(t_hbm, t_tc) / t_launch, 3),
                     "block_n": bn, "ctas": ctas, "schedule": "stream-K" if sched == 1 else "whole tiles"})
         del g2
+    assert w4.w4_last_device_error(ws) == 0
+
+    def time_graph(launches, reps=4):
+        """Seconds per launch of `launches` (callables, one GEMM each) captured back to back in one graph."""
+        g3 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g3, stream=stream):
+            for f in launches:
+                f()
+        with torch.cuda.stream(stream):
+            g3.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g3.replay()
+            b.record(stream)
+        stream.synchronize()
+        del g3
+        return a.elapsed_time(b) * 1e-3 / (reps * len(launches))
+
+    # ---- bf16 activations, scales and outputs on the same shapes (one point per M and layer)
+    bf16 = []
+    for L in layers:
+        Wb = torch.from_numpy(workloads.weights_bf16(L.n, L.k).view(np.int16)).to(dev).view(torch.bfloat16)
+        qw, sc, zw = w4.w4_pack(Wb, L.g)
+        pb = w4.w4_repack(qw, sc, zw, L.n, L.k, L.g)
+        del Wb, qw, sc, zw
+        cb = [pb] + [pb.clone() for _ in range(len(copies[L.name]) - 1)]
+        for m in BF16_MS:
+            xb = torch.from_numpy(workloads.activations_bf16(m, L.k).view(np.int16)).to(dev).view(torch.bfloat16)
+            yb = torch.empty((m, L.n), dtype=torch.bfloat16, device=dev)
+            t = time_graph([lambda c=c: w4.w4a16_gemm(xb, c, L.n, L.k, L.g, y=yb, workspace=ws) for c in cb])
+            f16 = next(p for p in per if p["M"] == m and p["layer"] == L.name)
+            b = alg_bytes(m, L.n, L.k, L.g)
+            f = gemm_flops(m, L.n, L.k)
+            t_roof = max(b / (peaks["hbm_gbs"] * 1e9), f / (peaks["bf16_tflops"] * 1e12))
+            bf16.append({"M": m, "layer": L.name, "us": round(t * 1e6, 3), "tflops": round(f / t / 1e12, 2),
+                         "roofline_frac": round(t_roof / t, 3), "f16_us": f16["us"]})
+        del cb, pb
+    assert w4.w4_last_device_error(ws) == 0
+
+    # ---- fused epilogues against the plain GEMM plus the PyTorch ops that would follow it (a y round trip)
+    epilogues = []
+    for L in layers:
+        if L.name not in EPI_LAYERS:
+            continue
+        kind = EPI_LAYERS[L.name]
+        c = copies[L.name]
+        for m in EPI_MS:
+            x = xs[m][L.k]
+            y = ys[(m, L.name)]
+            if kind == "qkv":
+                outs = [torch.empty((m, L.n // 3), dtype=torch.float16, device=dev) for _ in range(3)]
+                fused = [lambda cc=cc: w4.w4a16_gemm_grouped(
+                    [dict(x=x, packed=cc, N=L.n, K=L.k, qkv=(128, 1), out=outs)], L.g, workspace=ws,
+                    flags=w4.FLAG_WEIGHTS_STATIC) for cc in c]
+
+                def after(y=y, outs=outs, m=m):
+                    yv = y.view(m, L.n // 384, 3, 128)
+                    for j in range(3):
+                        outs[j].view(m, L.n // 384, 128).copy_(yv[:, :, j])
+            else:
+                h = torch.empty((m, L.n // 2), dtype=torch.float16, device=dev)
+                fused = [lambda cc=cc: w4.w4a16_gemm_grouped(
+                    [dict(x=x, packed=cc, N=L.n, K=L.k, y=h, silu_mul=True)], L.g, workspace=ws,
+                    flags=w4.FLAG_WEIGHTS_STATIC) for cc in c]
+
+                def after(y=y, h=h):
+                    torch.mul(torch.nn.functional.silu(y[:, 0::2]), y[:, 1::2], out=h)
+
+            unfused = [lambda cc=cc: (w4.w4a16_gemm(x, cc, L.n, L.k, L.g, y=y, workspace=ws, weights_static=True),
+                                      after()) for cc in c]
+            tf, tu = time_graph(fused), time_graph(unfused)
+            epilogues.append({"M": m, "layer": L.name, "epilogue": "qkv split (32 heads of 128)" if kind == "qkv"
+                              else "silu(gate) * up", "fused_us": round(tf * 1e6, 3),
+                              "gemm_then_torch_us": round(tu * 1e6, 3), "saved_us": round((tu - tf) * 1e6, 3),
+                              "y_round_trip_bytes": 2 * m * L.n * 2})
     assert w4.w4_last_device_error(ws) == 0
 
     # ---- end to end through the public API: every step copies its inputs (the 14 distinct x
@@ -417,7 +500,8 @@ def run_gpu(args):
     def step_e2e():
         dxbuf.copy_(hxbuf, non_blocking=True)
         for m, L in sweep():
-            w4.w4a16_gemm(dxv[(m, L.k)], copies[L.name][0], L.n, L.k, L.g, y=dyv[(m, L.name)], workspace=ws)
+            w4.w4a16_gemm(dxv[(m, L.k)], copies[L.name][0], L.n, L.k, L.g, y=dyv[(m, L.name)], workspace=ws,
+                          weights_static=True)
         hybuf.copy_(dybuf, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -496,6 +580,7 @@ def run_gpu(args):
                    "l2": "flushed between timed steps (512 MB write); 3 weight copies per layer rotate within a step",
                    "timing": "step captured as two CUDA graphs (the M <= 8 GEMMs, then the rest); CUDA events "
                              "around each per replay; max over ranks",
+                   "weights": "declared static (W4_FLAG_WEIGHTS_STATIC: no kernel writes the packed weights)",
                    "parallelism": f"replicas x{world}"},
         "weight_gbs": round(wbytes_step / (ms_per_step * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(dom_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -516,6 +601,8 @@ def run_gpu(args):
         "dense_fp16": dense,
         "offline": offline,
         "per_launch": per,
+        "bf16": bf16,
+        "epilogues": epilogues,
         "prefill": prefill,
     }
     if rank == 0:
@@ -644,14 +731,29 @@ def run_stack(args):
 
         def ours():
             for L, pk, y in zip(layers, packed, ys):
-                w4.w4a16_gemm(xs[L.k], pk, L.n, L.k, L.g, y=y, workspace=ws)
+                w4.w4a16_gemm(xs[L.k], pk, L.n, L.k, L.g, y=y, workspace=ws, weights_static=True)
+
+        # the same GEMMs grouped by what a decoder step could run together: q, k, v (one x), o, gate and
+        # up (one x), down, lm_head; one w4a16_gemm_grouped call each
+        per = len(workloads.STACK_LAYER)
+        groups = []
+        for li in range(workloads.STACK_LAYERS):
+            for part in ((0, 1, 2), (3,), (4, 5), (6,)):
+                groups.append([li * per + j for j in part])
+        groups.append([len(layers) - 1])
+        gprobs = [[dict(x=xs[layers[i].k], packed=packed[i], N=layers[i].n, K=layers[i].k, y=ys[i]) for i in grp]
+                  for grp in groups]
+
+        def ours_grouped():
+            for pr in gprobs:
+                w4.w4a16_gemm_grouped(pr, 128, flags=w4.FLAG_WEIGHTS_STATIC, workspace=ws)
 
         def theirs():
             for L, W, y in zip(layers, dense, ys):
                 torch.matmul(xs[L.k], W.t(), out=y)
 
         res = {}
-        for name, fn in (("w4a16", ours), ("dense_fp16", theirs)):
+        for name, fn in (("w4a16", ours), ("w4a16_grouped", ours_grouped), ("dense_fp16", theirs)):
             with torch.cuda.stream(stream):
                 fn()
             stream.synchronize()
@@ -672,6 +774,10 @@ def run_stack(args):
         assert w4.w4_last_device_error(ws) == 0
         rows.append({"M": m, "ms_per_step": round(res["w4a16"], 4), "tokens_per_s": round(m / (res["w4a16"] * 1e-3), 1),
                      "weight_gbs": round(wbytes / (res["w4a16"] * 1e-3) / 1e9, 1),
+                     "grouped_ms_per_step": round(res["w4a16_grouped"], 4),
+                     "grouped_tokens_per_s": round(m / (res["w4a16_grouped"] * 1e-3), 1),
+                     "grouped_launch_calls": len(groups),
+                     "weight_stream_ms_at_peak": round(wbytes / (load_peaks()["hbm_gbs"] * 1e9) * 1e3, 4),
                      "dense_ms_per_step": round(res["dense_fp16"], 4),
                      "dense_tokens_per_s": round(m / (res["dense_fp16"] * 1e-3), 1),
                      "speedup_vs_dense": round(res["dense_fp16"] / res["w4a16"], 3)})

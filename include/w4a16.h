@@ -212,6 +212,15 @@ W4_API size_t w4a16_workspace_bytes_ex(int64_t M, int64_t N, int64_t K, int32_t 
  *            up after this many SM clock cycles, sets the workspace error
  *            word (W4_ERR_TIMEOUT from w4_last_device_error) and the kernel
  *            returns early.
+ * dtype      W4_DTYPE_F16 (0) or W4_DTYPE_BF16: the type of x, of the packed
+ *            scales (w4_pack_ex / w4_repack of bf16 scales) and of y. bf16
+ *            runs the same kernels with bf16 operands (torchchat issue #1362
+ *            runs 'linear:int4' under the bf16 precision): (q - z) is exact in
+ *            bf16 too, products accumulate in fp32 and y is rounded once to
+ *            bf16. When g is not a multiple of 64, or on the tensor-memory
+ *            kernel, each weight is (q - z) * s rounded once to the type, so
+ *            the error bound doubles the unit roundoff of the type: 2^-7 for
+ *            bf16 against 2^-10 for fp16.
  */
 #define W4_FLAG_WEIGHTS_STATIC 1u
 #define W4_FLAG_TEST_TIMEOUT 2u
@@ -223,6 +232,8 @@ typedef struct {
     int32_t cluster;
     uint32_t flags;
     uint64_t wait_limit_cycles;
+    int32_t dtype;
+    int32_t reserved; /* 0 */
 } w4a16_options;
 
 /* w4a16_gemm with options (NULL = all automatic). The workspace must be at
@@ -234,6 +245,75 @@ W4_API int w4a16_gemm_opts(const void *x_dev, const void *packed_dev, int64_t M,
                            const w4a16_options *opts, void *stream);
 W4_API size_t w4a16_workspace_bytes_opts(int64_t M, int64_t N, int64_t K, int32_t g,
                                          const w4a16_options *opts);
+
+/*
+ * Output epilogues: where the fp32 sums of a GEMM go instead of y[m, n].
+ * AutoAWQ issue #31 lists fused qkv among the operations its tests must
+ * cover; these two write a fused layer's output in the form the next step
+ * reads, so that no separate pass over y follows.
+ *
+ * W4_EPI_NONE      y [M, N], as w4a16_gemm.
+ * W4_EPI_SILU_MUL  a fused gate/up projection whose weight rows alternate:
+ *                  row 2j is gate row j, row 2j + 1 is up row j (interleave
+ *                  the rows before packing). y [M, N / 2] receives
+ *                  silu(gate) * up, silu(v) = v / (1 + e^-v), evaluated in
+ *                  fp32 from the two unrounded sums and rounded once. N even.
+ * W4_EPI_QKV_SPLIT a fused q/k/v projection whose weight rows come in head
+ *                  groups: for each of the N / ((r + 2) d) groups, r query
+ *                  heads, then one key head, then one value head, d rows
+ *                  each (d = head_dim, r = q_per_group; r = 1 for multi-head
+ *                  attention, r > 1 for grouped-query attention). y_dev
+ *                  receives q [M, groups * r * d], k_dev and v_dev receive
+ *                  k and v [M, groups * d], all row-major. head_dim a
+ *                  multiple of 4; N a multiple of (r + 2) d.
+ */
+#define W4_EPI_NONE 0
+#define W4_EPI_SILU_MUL 1
+#define W4_EPI_QKV_SPLIT 2
+typedef struct {
+    int32_t kind;
+    int32_t head_dim;     /* W4_EPI_QKV_SPLIT */
+    int32_t q_per_group;  /* W4_EPI_QKV_SPLIT */
+    int32_t reserved;     /* 0 */
+    void *k_dev;          /* W4_EPI_QKV_SPLIT: out, 2-byte aligned */
+    void *v_dev;          /* W4_EPI_QKV_SPLIT: out, 2-byte aligned */
+} w4a16_epilogue;
+
+/* One GEMM of a group: x [M, K], packed weights [N, K], output y with its
+ * epilogue (a zeroed epilogue is W4_EPI_NONE). */
+typedef struct {
+    const void *x_dev;
+    const void *packed_dev;
+    void *y_dev;
+    int64_t N;
+    int64_t K;
+    w4a16_epilogue epilogue;
+} w4a16_problem;
+
+/*
+ * w4a16_gemm_grouped -- `count` (1..4096) independent GEMMs of the same M, g
+ * and value type (opts->dtype), enqueued on `stream` by one call. Each
+ * problem is checked as w4a16_gemm checks its arguments; the call enqueues
+ * nothing unless all pass. A single GEMM with an epilogue is a group of one.
+ *
+ * Where every problem would run on the decode kernel alone (M <= 8 by
+ * default), each launch takes up to 16 problems and walks all their weight
+ * tiles in one persistent grid: the weight stream of one problem runs on
+ * into the next without a launch boundary, which removes the start-up and
+ * tail cost of a launch per GEMM (the bigcode-inference-benchmark roadmap,
+ * issue #11, names that cost for many small GEMMs). Problems that share x
+ * and K (q, k and v of one layer; gate and up) keep x in shared memory
+ * across problems. Otherwise the problems run one launch each, in order.
+ * Outputs must not overlap one another or any input. The workspace must be
+ * at least w4a16_grouped_workspace_bytes(...) bytes, 256-byte aligned and
+ * zeroed before first use, like w4a16_gemm's.
+ * Returns as w4a16_gemm; W4_ERR_INVALID_ARG also for a bad epilogue.
+ */
+W4_API int w4a16_gemm_grouped(const w4a16_problem *problems, int32_t count, int64_t M, int32_t g,
+                              void *workspace_dev, size_t workspace_bytes, const w4a16_options *opts,
+                              void *stream);
+W4_API size_t w4a16_grouped_workspace_bytes(const w4a16_problem *problems, int32_t count, int64_t M, int32_t g,
+                                            const w4a16_options *opts);
 
 /*
  * The schedule w4a16_gemm picks on the current device: writes block_n, the

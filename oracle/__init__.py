@@ -238,3 +238,38 @@ def gemm(x, qw, scales, zeros, N: int, K: int, g: int, rows=None, nthreads: int 
     if rc != 0:
         raise MemoryError("orc_gemm_rows: allocation failed")
     return y
+
+
+# ----------------------------------------------------------- epilogues
+# Plain fp64 restatements of the two output epilogues, applied to the oracle's unrounded GEMM output.
+
+def silu(v) -> np.ndarray:
+    """silu(v) = v * sigmoid(v) = v / (1 + e^-v) in fp64: the gated MLP activation (SiLU / swish)."""
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def silu_mul(y) -> np.ndarray:
+    """h [R, N/2] = silu(gate) * up for a fused gate/up output y [R, N] whose columns alternate gate
+    (even column 2j) and up (odd column 2j + 1)."""
+    y = np.asarray(y, dtype=np.float64)
+    assert y.ndim == 2 and y.shape[1] % 2 == 0
+    return silu(y[:, 0::2]) * y[:, 1::2]
+
+
+def qkv_split(y, head_dim: int, q_per_group: int):
+    """(q, k, v) from a fused q/k/v output y [R, N] whose columns come in head groups: per group,
+    q_per_group query heads, one key head and one value head of head_dim columns each. q is
+    [R, groups * q_per_group * head_dim] (the groups' query heads in order), k and v [R, groups * head_dim]."""
+    y = np.asarray(y)
+    R, N = y.shape
+    d, r = head_dim, q_per_group
+    span = (r + 2) * d
+    assert N % span == 0
+    groups = N // span
+    yg = y.reshape(R, groups, r + 2, d)
+    q = yg[:, :, :r, :].reshape(R, groups * r * d)
+    k = yg[:, :, r, :].reshape(R, groups * d)
+    v = yg[:, :, r + 1, :].reshape(R, groups * d)
+    return q, k, v

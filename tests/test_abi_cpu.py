@@ -123,6 +123,10 @@ def test_options_validation(lib):
     assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 4, 0)) == 0  # no flag 4
     assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(3, 0, 0, 0, 0, 0, 0)) == 0
     assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 1, 0)) == 256
+    # value types: fp16 (0) or bf16 (1), the reserved field zero
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 0, 0, 1, 0)) == 256
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 0, 0, 2, 0)) == 0
+    assert w4.w4a16_workspace_bytes_opts(4, 4096, 4096, 128, O(0, 0, 0, 0, 0, 0, 0, 0, 1)) == 0
 
 
 def _vp(v):
@@ -155,6 +159,11 @@ def test_host_side_argument_checks(lib):
     assert lib.w4_pack(None, 4, 8, 8, fake, fake, fake, None) == 1
     assert lib.w4_pack(fake, 4, 8, 7, fake, fake, fake, None) == 1
     assert lib.w4_pack(_vp(0x10001), 4, 8, 8, fake, fake, fake, None) == 3
+    # w4_pack_ex: dtype 0 or 1, symmetric 0 or 1
+    assert lib.w4_pack_ex(fake, 4, 8, 8, 2, 0, fake, fake, fake, None) == 1
+    assert lib.w4_pack_ex(fake, 4, 8, 8, 0, 2, fake, fake, fake, None) == 1
+    assert lib.w4_pack_ex(fake, 4, 8, 8, -1, 0, fake, fake, fake, None) == 1
+    assert lib.w4_pack_ex(_vp(0x10001), 4, 8, 8, 1, 1, fake, fake, fake, None) == 3
     assert lib.w4_repack(fake, fake, fake, 4, 8, 8, _vp(0x10008), None) == 3
     assert lib.w4_repack(fake, fake, fake, -1, 8, 8, fake, None) == 1
     assert lib.w4_last_device_error(None, None) == 1

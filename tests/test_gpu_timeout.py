@@ -54,3 +54,31 @@ def test_wait_runs_out_then_next_call_is_correct(opts):
     yref = oracle.gemm(x, qw, s, zw, N, K, g)
     assert_within_tolerance(y.cpu().numpy(), yref, gemm_tolerance(x, row_norms_dequant(qw, s, zw, N, K, g)),
                             f"after timeout {opts}")
+
+
+def test_grouped_wait_runs_out_then_next_call_is_correct():
+    # two problems with different x: the decode kernel reloads x between them (the consumers' x_free wait)
+    g, M = 128, 4
+    specs = [(1000, 2048, 0), (700, 1024, 1)]
+    data = []
+    for N, K, seed in specs:
+        W = workloads.weights_f16(N, K, seed=seed)
+        qw, s, zw = oracle.pack(W, g)
+        packed = w4.w4_repack(torch.from_numpy(qw.view(np.int32)).cuda(), torch.from_numpy(s).cuda(),
+                              torch.from_numpy(zw.view(np.int32)).cuda(), N, K, g)
+        x = workloads.activations_f16(M, K, seed=seed + 5)
+        data.append((N, K, qw, s, zw, packed, x, torch.from_numpy(x).cuda()))
+    problems = [dict(x=xd, packed=packed, N=N, K=K) for N, K, _, _, _, packed, _, xd in data]
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    w4.w4a16_gemm_grouped(problems, g, kernel=1, block_n=8, flags=w4.FLAG_TEST_TIMEOUT,
+                          wait_limit_cycles=SHORT_LIMIT, workspace=ws)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_error(ws) == W4_ERR_TIMEOUT
+    ws.zero_()
+    outs = w4.w4a16_gemm_grouped(problems, g, kernel=1, block_n=8, workspace=ws)
+    torch.cuda.synchronize()
+    assert w4.w4_last_device_error(ws) == 0
+    for (N, K, qw, s, zw, _, x, _), y in zip(data, outs):
+        yref = oracle.gemm(x, qw, s, zw, N, K, g)
+        assert_within_tolerance(y.cpu().numpy(), yref, gemm_tolerance(x, row_norms_dequant(qw, s, zw, N, K, g)),
+                                "grouped, after timeout")

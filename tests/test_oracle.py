@@ -8,6 +8,7 @@ proved from the definition, a library matmul, or a value derived by hand in
 """
 from __future__ import annotations
 
+import math
 import os
 from fractions import Fraction
 
@@ -574,3 +575,56 @@ def test_gemm_variants_one_hot_and_matmul(dtype, symmetric):
         xb.astype(np.float64)
     y = oracle.gemm(xb, qw, s, zw, N, K, g, dtype=dtype)
     assert np.allclose(y, xv @ wd.T, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ epilogues
+
+def test_silu_closed_forms():
+    # sigmoid(ln 3) = 3/4, so silu(ln 3) = (3/4) ln 3; silu(0) = 0; silu(v) - silu(-v) = v for every v
+    # (v sigmoid(v) + v sigmoid(-v) = v); and the tanh form silu(v) = v/2 (1 + tanh(v/2))
+    assert oracle.silu(math.log(3.0)) == pytest.approx(0.75 * math.log(3.0), rel=1e-15)
+    assert oracle.silu(0.0) == 0.0
+    v = np.linspace(-40, 40, 1001)
+    assert np.allclose(oracle.silu(v) - oracle.silu(-v), v, rtol=1e-14, atol=1e-14)
+    # (the tanh form cancels for v << 0: an absolute bound of a few ulp of |v|)
+    assert np.allclose(oracle.silu(v), 0.5 * v * (1 + np.tanh(0.5 * v)), rtol=1e-13, atol=1e-13)
+    assert oracle.silu(-800.0) == 0.0 and oracle.silu(800.0) == 800.0  # saturates without overflow
+
+
+def test_silu_mul_hand_example():
+    # columns alternate gate, up: (ln 3, 2) -> (3/4) ln 3 * 2; (0, 5) -> 0; (-ln 3, 4) -> -(1/4) ln 3 * 4
+    y = np.array([[math.log(3.0), 2.0, 0.0, 5.0, -math.log(3.0), 4.0]])
+    h = oracle.silu_mul(y)
+    assert h.shape == (1, 3)
+    assert h[0] == pytest.approx([1.5 * math.log(3.0), 0.0, -math.log(3.0)], rel=1e-15)
+
+
+def test_qkv_split_hand_example():
+    # head_dim 2, two query heads per group, two groups: N = 2 * (2 + 2) * 2 = 16 columns
+    y = np.arange(16, dtype=np.float64)[None, :]
+    q, k, v = oracle.qkv_split(y, 2, 2)
+    assert q.tolist() == [[0, 1, 2, 3, 8, 9, 10, 11]]
+    assert k.tolist() == [[4, 5, 12, 13]]
+    assert v.tolist() == [[6, 7, 14, 15]]
+    # multi-head attention (one query head per group): q, k, v heads interleave per group
+    q, k, v = oracle.qkv_split(np.arange(12)[None, :], 2, 1)
+    assert q.tolist() == [[0, 1, 6, 7]] and k.tolist() == [[2, 3, 8, 9]] and v.tolist() == [[4, 5, 10, 11]]
+
+
+def test_weight_row_orders_match_the_epilogues():
+    # the binding's offline row orders, read back by the oracle's epilogue maps
+    import torch
+
+    import w4a16_group_quantized_gb300 as w4
+
+    d, r, groups, K = 4, 3, 2, 1
+    wq = torch.arange(groups * r * d, dtype=torch.float64)[:, None]
+    wk = 1000 + torch.arange(groups * d, dtype=torch.float64)[:, None]
+    wv = 2000 + torch.arange(groups * d, dtype=torch.float64)[:, None]
+    fused = w4.qkv_head_group_rows(wq, wk, wv, d)
+    q, k, v = oracle.qkv_split(fused.numpy().T, d, r)  # one token with x = 1: y = the weight column
+    assert (q[0] == wq[:, 0].numpy()).all() and (k[0] == wk[:, 0].numpy()).all() and (v[0] == wv[:, 0].numpy()).all()
+    gate = torch.arange(5, dtype=torch.float64)[:, None]
+    up = 100 + torch.arange(5, dtype=torch.float64)[:, None]
+    il = w4.interleave_gate_up(gate, up).numpy().T
+    assert (il[0, 0::2] == gate[:, 0].numpy()).all() and (il[0, 1::2] == up[:, 0].numpy()).all()

@@ -26,6 +26,9 @@ __all__ = [
     "w4a16_gemm_ex", "w4a16_gemm_opts", "w4a16_workspace_bytes", "w4a16_workspace_bytes_ex",
     "w4a16_workspace_bytes_opts", "w4a16_gemm_plan", "w4_last_device_error", "w4_status_string", "Workspace",
     "Options", "STATUS", "KERNEL_DECODE", "KERNEL_TMEM", "FLAG_WEIGHTS_STATIC", "FLAG_TEST_TIMEOUT",
+    "Epilogue", "Problem", "EPI_NONE", "EPI_SILU_MUL", "EPI_QKV_SPLIT", "w4a16_gemm_grouped",
+    "w4a16_grouped_workspace_bytes", "w4a16_gemm_silu_mul", "w4a16_gemm_qkv", "interleave_gate_up",
+    "qkv_head_group_rows",
 ]
 
 KERNEL_DECODE = 1
@@ -39,7 +42,24 @@ class Options(ctypes.Structure):
 
     _fields_ = [("kernel", ctypes.c_int32), ("block_n", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("schedule", ctypes.c_int32), ("cluster", ctypes.c_int32), ("flags", ctypes.c_uint32),
-                ("wait_limit_cycles", ctypes.c_uint64)]
+                ("wait_limit_cycles", ctypes.c_uint64), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+EPI_NONE, EPI_SILU_MUL, EPI_QKV_SPLIT = 0, 1, 2
+
+
+class Epilogue(ctypes.Structure):
+    """w4a16_epilogue of the C ABI."""
+
+    _fields_ = [("kind", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("q_per_group", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("k_dev", ctypes.c_void_p), ("v_dev", ctypes.c_void_p)]
+
+
+class Problem(ctypes.Structure):
+    """w4a16_problem of the C ABI."""
+
+    _fields_ = [("x_dev", ctypes.c_void_p), ("packed_dev", ctypes.c_void_p), ("y_dev", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("epilogue", Epilogue)]
+
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libw4a16.so")
@@ -84,6 +104,9 @@ def load() -> ctypes.CDLL:
             "w4_last_device_error": ([P, P], ctypes.c_int),
             "w4a16_gemm_opts": ([P, P, I64, I64, I64, I32, P, P, SZ, ctypes.POINTER(Options), P], ctypes.c_int),
             "w4a16_workspace_bytes_opts": ([I64, I64, I64, I32, ctypes.POINTER(Options)], SZ),
+            "w4a16_gemm_grouped": ([ctypes.POINTER(Problem), I32, I64, I32, P, SZ, ctypes.POINTER(Options), P],
+                                   ctypes.c_int),
+            "w4a16_grouped_workspace_bytes": ([ctypes.POINTER(Problem), I32, I64, I32, ctypes.POINTER(Options)], SZ),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -217,12 +240,13 @@ def _gemm_common(x, packed, N, K, g, y, workspace, block_n, ctas, schedule, stre
 
 def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: int, y: torch.Tensor | None = None,
                workspace=None, stream=None, weights_static: bool = False) -> torch.Tensor:
-    """y fp16 [M,N] = x fp16 [M,K] . dequant(packed)^T. ``workspace``: a Workspace or a zeroed uint8 tensor.
-    ``weights_static``: the kernel launched just before this call on the stream does not write ``packed``
-    (W4_FLAG_WEIGHTS_STATIC: the decode kernel may then fetch weights before that kernel ends)."""
-    if weights_static:
-        return w4a16_gemm_opts(x, packed, N, K, g, flags=FLAG_WEIGHTS_STATIC, y=y, workspace=workspace,
-                               stream=stream)
+    """y [M,N] = x [M,K] . dequant(packed)^T, fp16 or bf16 (x's dtype: the packed scales must be of the
+    same type). ``workspace``: a Workspace or a zeroed uint8 tensor. ``weights_static``: the kernel
+    launched just before this call on the stream does not write ``packed`` (W4_FLAG_WEIGHTS_STATIC: the
+    decode kernel may then fetch weights before that kernel ends)."""
+    if weights_static or x.dtype == torch.bfloat16:
+        return w4a16_gemm_opts(x, packed, N, K, g, flags=FLAG_WEIGHTS_STATIC if weights_static else 0, y=y,
+                               workspace=workspace, stream=stream)
     return _gemm_common(x, packed, N, K, g, y, workspace, 0, 0, 0, stream)
 
 
@@ -230,15 +254,15 @@ def w4a16_gemm_opts(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, g: in
                     block_n: int = 0, ctas: int = 0, schedule: int = 0, cluster: int = 0, flags: int = 0,
                     wait_limit_cycles: int = 0, y: torch.Tensor | None = None, workspace=None,
                     stream=None) -> torch.Tensor:
-    """w4a16_gemm with the options of w4a16_options (see include/w4a16.h)."""
-    if x.dtype != torch.float16 or x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be fp16 [M, K]")
+    """w4a16_gemm with the options of w4a16_options (see include/w4a16.h); the dtype option follows x."""
+    if x.dtype not in _DTYPES or x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be fp16 or bf16 [M, K]")
     M = x.shape[0]
     if y is None:
-        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
-    elif y.dtype != torch.float16 or tuple(y.shape) != (M, N):
-        raise ValueError("y must be fp16 [M, N]")
-    o = Options(kernel, block_n, ctas, schedule, cluster, flags, wait_limit_cycles)
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    elif y.dtype != x.dtype or tuple(y.shape) != (M, N):
+        raise ValueError("y must be [M, N] of x's dtype")
+    o = Options(kernel, block_n, ctas, schedule, cluster, flags, wait_limit_cycles, _DTYPES[x.dtype], 0)
     need = w4a16_workspace_bytes_opts(M, N, K, g, o)
     if need == 0:
         raise W4Error(1, "w4a16_workspace_bytes_opts")
@@ -265,3 +289,123 @@ def w4_last_device_error(workspace, stream=None) -> int:
     W4_ERR_TIMEOUT the workspace's tile counters are undefined too: zero it before reuse."""
     ws = workspace.buf if isinstance(workspace, Workspace) else workspace
     return int(load().w4_last_device_error(_dev(ws, "workspace"), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- groups and epilogues
+
+def _problem_array(problems, M, dtype, device):
+    """(ctypes array of Problem, outputs per problem, tensors to keep alive)."""
+    arr = (Problem * len(problems))()
+    outs, keep = [], []
+    for i, pr in enumerate(problems):
+        x, packed, N, K = pr["x"], pr["packed"], int(pr["N"]), int(pr["K"])
+        if x.dtype != dtype or x.dim() != 2 or tuple(x.shape) != (M, K):
+            raise ValueError(f"problem {i}: x must be [{M}, {K}] of the group's dtype")
+        epi = Epilogue()
+        if pr.get("silu_mul"):
+            epi.kind = EPI_SILU_MUL
+            y = pr.get("y")
+            if y is None:
+                y = torch.empty((M, N // 2), dtype=dtype, device=device)
+            elif y.dtype != dtype or tuple(y.shape) != (M, N // 2):
+                raise ValueError(f"problem {i}: y must be [{M}, {N // 2}]")
+            out = y
+        elif pr.get("qkv"):
+            head_dim, q_per_group = pr["qkv"]
+            span = (q_per_group + 2) * head_dim
+            if N % span:
+                raise ValueError(f"problem {i}: N must be a multiple of (q_per_group + 2) * head_dim")
+            groups = N // span
+            epi.kind, epi.head_dim, epi.q_per_group = EPI_QKV_SPLIT, head_dim, q_per_group
+            shapes = ((M, groups * q_per_group * head_dim), (M, groups * head_dim), (M, groups * head_dim))
+            if pr.get("out") is not None:
+                q, k, v = pr["out"]
+                if any(t.dtype != dtype or tuple(t.shape) != sh for t, sh in zip((q, k, v), shapes)):
+                    raise ValueError(f"problem {i}: out must be q, k, v of shapes {shapes}")
+            else:
+                q, k, v = (torch.empty(sh, dtype=dtype, device=device) for sh in shapes)
+            epi.k_dev, epi.v_dev = k.data_ptr(), v.data_ptr()
+            y, out = q, (q, k, v)
+            keep += [k, v]
+        else:
+            y = pr.get("y")
+            if y is None:
+                y = torch.empty((M, N), dtype=dtype, device=device)
+            elif y.dtype != dtype or tuple(y.shape) != (M, N):
+                raise ValueError(f"problem {i}: y must be [{M}, {N}]")
+            out = y
+        arr[i] = Problem(_dev(x, "x").value, _dev(packed, "packed").value, _dev(y, "y").value, N, K, epi)
+        outs.append(out)
+        keep += [x, packed, y]
+    return arr, outs, keep
+
+
+def w4a16_grouped_workspace_bytes(problems, g: int, **opts) -> int:
+    x0 = problems[0]["x"]
+    arr, _, _ = _problem_array(problems, x0.shape[0], x0.dtype, x0.device)
+    o = Options(opts.get("kernel", 0), opts.get("block_n", 0), opts.get("ctas", 0), opts.get("schedule", 0),
+                opts.get("cluster", 0), opts.get("flags", 0), opts.get("wait_limit_cycles", 0), _DTYPES[x0.dtype], 0)
+    return int(load().w4a16_grouped_workspace_bytes(arr, len(problems), x0.shape[0], g, ctypes.byref(o)))
+
+
+def w4a16_gemm_grouped(problems, g: int, *, kernel: int = 0, block_n: int = 0, ctas: int = 0, schedule: int = 0,
+                       cluster: int = 0, flags: int = 0, wait_limit_cycles: int = 0, workspace=None, stream=None):
+    """Independent GEMMs of one M, g and dtype in one call (w4a16_gemm_grouped). Each problem is a dict
+    with x [M, K], packed, N, K, and optionally y (the output), silu_mul=True (y [M, N/2] =
+    silu(gate) * up for weight rows alternating gate, up) or qkv=(head_dim, q_per_group) (weight rows in
+    head groups; the output is (q, k, v), given as out=(q, k, v) or allocated). Returns the outputs in
+    order."""
+    if not problems:
+        raise ValueError("empty group")
+    x0 = problems[0]["x"]
+    if x0.dtype not in _DTYPES:
+        raise ValueError("x must be fp16 or bf16")
+    M = x0.shape[0]
+    arr, outs, keep = _problem_array(problems, M, x0.dtype, x0.device)
+    o = Options(kernel, block_n, ctas, schedule, cluster, flags, wait_limit_cycles, _DTYPES[x0.dtype], 0)
+    need = int(load().w4a16_grouped_workspace_bytes(arr, len(problems), M, g, ctypes.byref(o)))
+    if need == 0:
+        raise W4Error(1, "w4a16_grouped_workspace_bytes")
+    if workspace is None:
+        workspace = Workspace(x0.device)
+    ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    nbytes = ws.numel() * ws.element_size()
+    rc = load().w4a16_gemm_grouped(arr, len(problems), M, g, _dev(ws, "workspace"), nbytes, ctypes.byref(o),
+                                   _stream(stream))
+    _check(rc, "w4a16_gemm_grouped")
+    del keep
+    return outs
+
+
+def w4a16_gemm_silu_mul(x, packed, N: int, K: int, g: int, y=None, workspace=None, stream=None, **opts):
+    """h [M, N/2] = silu(x . gate^T) * (x . up^T) for packed weight rows alternating gate, up."""
+    return w4a16_gemm_grouped([dict(x=x, packed=packed, N=N, K=K, y=y, silu_mul=True)], g, workspace=workspace,
+                              stream=stream, **opts)[0]
+
+
+def w4a16_gemm_qkv(x, packed, N: int, K: int, g: int, head_dim: int, q_per_group: int, workspace=None, stream=None,
+                   **opts):
+    """(q, k, v) of a fused projection whose weight rows come in head groups (see qkv_head_group_rows)."""
+    return w4a16_gemm_grouped([dict(x=x, packed=packed, N=N, K=K, qkv=(head_dim, q_per_group))], g,
+                              workspace=workspace, stream=stream, **opts)[0]
+
+
+def interleave_gate_up(gate: torch.Tensor, up: torch.Tensor) -> torch.Tensor:
+    """[2 I, K] weights with row 2j = gate row j and row 2j + 1 = up row j (offline weight preparation)."""
+    if gate.shape != up.shape or gate.dim() != 2:
+        raise ValueError("gate and up must be [I, K] each")
+    return torch.stack([gate, up], dim=1).reshape(2 * gate.shape[0], gate.shape[1])
+
+
+def qkv_head_group_rows(wq: torch.Tensor, wk: torch.Tensor, wv: torch.Tensor, head_dim: int) -> torch.Tensor:
+    """Fused q/k/v weights in head groups (r query heads, one key head, one value head per group), the row
+    order W4_EPI_QKV_SPLIT reads (offline weight preparation)."""
+    groups = wk.shape[0] // head_dim
+    if wk.shape != wv.shape or wk.shape[0] % head_dim or wq.shape[0] % (groups * head_dim):
+        raise ValueError("q, k, v rows must be whole heads, with as many key as value heads")
+    r = wq.shape[0] // (groups * head_dim)
+    K = wq.shape[1]
+    q = wq.reshape(groups, r * head_dim, K)
+    k = wk.reshape(groups, head_dim, K)
+    v = wv.reshape(groups, head_dim, K)
+    return torch.cat([q, k, v], dim=1).reshape(-1, K)

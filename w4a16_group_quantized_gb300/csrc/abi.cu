@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "w4a16.h"
@@ -18,6 +19,9 @@ bool valid_group(int32_t g) { return g > 0 && g % 8 == 0; }
 
 // 2^31 - 1 bounds every index the kernels form in 32-bit arithmetic.
 constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+// Problems per w4a16_gemm_grouped call (the host list is copied once per call).
+constexpr int32_t kMaxGroup = 4096;
 
 int num_sms_current_device() {
   static int cache[64] = {0};
@@ -47,6 +51,7 @@ bool to_options(const w4a16_options *o, w4::GemmOptions *out) {
   *out = w4::GemmOptions{};
   if (!o) return true;
   if (o->flags & ~(W4_FLAG_WEIGHTS_STATIC | W4_FLAG_TEST_TIMEOUT)) return false;
+  if ((o->dtype != W4_DTYPE_F16 && o->dtype != W4_DTYPE_BF16) || o->reserved != 0) return false;
   out->kernel = o->kernel;
   out->block_n = o->block_n;
   out->ctas = o->ctas;
@@ -55,6 +60,7 @@ bool to_options(const w4a16_options *o, w4::GemmOptions *out) {
   out->weights_static = (o->flags & W4_FLAG_WEIGHTS_STATIC) != 0;
   out->test_timeout = (o->flags & W4_FLAG_TEST_TIMEOUT) != 0;
   out->wait_limit = o->wait_limit_cycles;
+  out->dtype = o->dtype;
   return true;
 }
 
@@ -83,9 +89,31 @@ int gemm_impl(const void *x, const void *packed, int64_t M, int64_t N, int64_t K
   if (ws_bytes < plan.workspace_bytes) return W4_ERR_WORKSPACE_TOO_SMALL;
   bool encode_failed = false;
   const cudaError_t e =
-      w4::launch_gemm(x, packed, M, N, K, g, y, ws, plan, opt, static_cast<cudaStream_t>(stream), &encode_failed);
+      w4::launch_gemm(x, packed, M, N, K, g, y, ws, plan, opt, w4::EpiSpec{}, static_cast<cudaStream_t>(stream),
+                      &encode_failed);
   if (encode_failed) return W4_ERR_CUDA;
   return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+// The C problem list -> the library's, with every check of a single GEMM applied to each problem and
+// its epilogue (outputs 2-byte aligned). Returns W4_OK or the first failing status.
+int to_problems(const w4a16_problem *in, int32_t count, int64_t M, int32_t g, w4::GemmProblem *out) {
+  if (!in || count < 1 || count > kMaxGroup) return W4_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < count; ++i) {
+    const w4a16_problem &a = in[i];
+    const int rc = check_gemm_args(a.x_dev, a.packed_dev, M, a.N, a.K, g, a.y_dev, reinterpret_cast<void *>(256));
+    if (rc != W4_OK) return rc;
+    w4::EpiSpec e;
+    e.kind = a.epilogue.kind;
+    e.head_dim = a.epilogue.head_dim;
+    e.q_per_group = a.epilogue.q_per_group;
+    e.k = a.epilogue.k_dev;
+    e.v = a.epilogue.v_dev;
+    if (a.epilogue.reserved != 0 || !w4::epi_valid(e, a.N)) return W4_ERR_INVALID_ARG;
+    if ((e.k && !aligned(e.k, 2)) || (e.v && !aligned(e.v, 2))) return W4_ERR_MISALIGNED;
+    out[i] = w4::GemmProblem{a.x_dev, a.packed_dev, a.y_dev, a.N, a.K, e};
+  }
+  return W4_OK;
 }
 
 size_t workspace_impl(int64_t M, int64_t N, int64_t K, int32_t g, const w4::GemmOptions &opt) {
@@ -197,6 +225,37 @@ int w4a16_gemm_opts(const void *x_dev, const void *packed_dev, int64_t M, int64_
   return gemm_impl(x_dev, packed_dev, M, N, K, g, y_dev, workspace_dev, workspace_bytes, o, stream);
 }
 
+size_t w4a16_grouped_workspace_bytes(const w4a16_problem *problems, int32_t count, int64_t M, int32_t g,
+                                     const w4a16_options *opts) {
+  w4::GemmOptions o;
+  if (!to_options(opts, &o)) return 0;
+  std::vector<w4::GemmProblem> probs(count > 0 && count <= kMaxGroup ? count : 0);
+  if (to_problems(problems, count, M, g, probs.data()) != W4_OK) return 0;
+  w4::GroupPlan plan;
+  if (!w4::make_group_plan(probs.data(), count, M, g, o, num_sms_current_device(), &plan)) return 0;
+  return plan.workspace_bytes;
+}
+
+int w4a16_gemm_grouped(const w4a16_problem *problems, int32_t count, int64_t M, int32_t g, void *workspace_dev,
+                       size_t workspace_bytes, const w4a16_options *opts, void *stream) {
+  w4::GemmOptions o;
+  if (!to_options(opts, &o)) return W4_ERR_INVALID_ARG;
+  if (!workspace_dev) return W4_ERR_INVALID_ARG;
+  if (!aligned(workspace_dev, 256)) return W4_ERR_MISALIGNED;
+  std::vector<w4::GemmProblem> probs(count > 0 && count <= kMaxGroup ? count : 0);
+  const int rc = to_problems(problems, count, M, g, probs.data());
+  if (rc != W4_OK) return rc;
+  const int sms = num_sms_current_device();
+  w4::GroupPlan plan;
+  if (!w4::make_group_plan(probs.data(), count, M, g, o, sms, &plan)) return W4_ERR_INVALID_ARG;
+  if (workspace_bytes < plan.workspace_bytes) return W4_ERR_WORKSPACE_TOO_SMALL;
+  bool encode_failed = false;
+  const cudaError_t e = w4::launch_gemm_grouped(probs.data(), count, M, g, workspace_dev, plan, o, sms,
+                                                static_cast<cudaStream_t>(stream), &encode_failed);
+  if (encode_failed) return W4_ERR_CUDA;
+  return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
 int w4_last_device_error(void *workspace_dev, void *stream) {
   if (!workspace_dev) return W4_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -268,7 +327,7 @@ int w4a16_gemm_noalloc(const void *x_dev, const void *packed_dev, int64_t M, int
   if (cudaMemsetAsync(scratch, 0, plan.pieces_offset, st) != cudaSuccess) return W4_ERR_CUDA;
   bool encode_failed = false;
   const cudaError_t e =
-      w4::launch_gemm(x_dev, packed_dev, M, N, K, g, y_dev, scratch, plan, opt, st, &encode_failed);
+      w4::launch_gemm(x_dev, packed_dev, M, N, K, g, y_dev, scratch, plan, opt, w4::EpiSpec{}, st, &encode_failed);
   if (encode_failed) return W4_ERR_CUDA;
   return e == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }

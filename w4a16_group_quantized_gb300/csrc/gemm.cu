@@ -106,14 +106,28 @@ struct Cfg {
 // Writes 16 consecutive columns (activation rows m0 + c0 ..) of weight row n of a finished tile
 // segment: to y (fp16, rounded once) for a whole tile, else to the CTA's fp32 piece, which is laid
 // out column by column ([BN][128]) so that a warp's 32 rows make one 128-byte line per column.
-template <int BN>
+template <int BN, int DT>
 __device__ __forceinline__ void emit16(const Params &p, bool whole, int n, int m0, int m_end, int c0,
                                        const float (&v)[16], float *piece) {
   if (whole) {
-    if (n < p.N) {
+    if (p.epi.kind == kEpiSiluMul) {
+      // rows n (even lane: gate) and n + 1 (odd lane: up); the even lane writes silu(gate) * up
+      float u[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) u[e] = __shfl_xor_sync(0xffffffffu, v[e], 1);
+      if ((n & 1) == 0 && n < p.N) {
+        uint16_t *dst = p.y + n / 2;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (m0 + c0 + e < m_end)
+            dst[static_cast<int64_t>(m0 + c0 + e) * p.epi.ld] = out_bits<DT>(silu_mul(v[e], u[e]));
+      }
+    } else if (n < p.N) {
+      int ld;
+      uint16_t *dst = epi_row(p.epi, p.y, n, &ld);
 #pragma unroll
       for (int e = 0; e < 16; ++e)
-        if (m0 + c0 + e < m_end) p.y[static_cast<int64_t>(m0 + c0 + e) * p.N + n] = __float2half_rn(v[e]);
+        if (m0 + c0 + e < m_end) dst[static_cast<int64_t>(m0 + c0 + e) * ld] = out_bits<DT>(v[e]);
     }
   } else {
 #pragma unroll
@@ -195,7 +209,7 @@ __device__ __forceinline__ void produce_stages_pair(const CUtensorMap *x_map, co
   }
 }
 
-template <int BN, int MODE, int TP>
+template <int BN, int MODE, int TP, int DT>
 __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap code_map,
                       const __grid_constant__ CUtensorMap rec_map, const Params p) {
@@ -292,7 +306,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
     // stage's one tile, or (kTP = 2) all K blocks of the stage's weight tile e
     const int e = warp - C::kIssuerWarp0;
     const int b0 = C::kTP == 2 ? 0 : BPI * e;  // this warp's first K block (x sub-tile) in a stage
-    constexpr uint32_t idesc = idesc_f16_f32(128, BN);
+    constexpr uint32_t idesc = idesc_f16_f32(128, BN, DT == kDtypeBf16);
     StageIter it;
     it.init(p, u0);
     int seg = 0;          // segment (tile) index within the CTA's range
@@ -394,12 +408,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
               recs + (fixed_rec ? fixed_rec_off
                                 : (p.gdiv.div(kfirst) - p.gdiv.div(it.ks * kStageKHere)) * kRecBytes);
           const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
-          const GroupConsts gc = group_consts(lds16(rec + 2 * r), z);
+          const GroupConsts gc = group_consts<DT>(lds16(rec + 2 * r), z);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {  // two halves of 16 columns: fewer registers live at once
             uint32_t out[16];
 #pragma unroll
-            for (int ci = 0; ci < 4; ++ci) dequant_word(words[4 * h + ci], gc, &out[4 * ci]);
+            for (int ci = 0; ci < 4; ++ci) dequant_word<DT>(words[4 * h + ci], gc, &out[4 * ci]);
             tmem_st_32x32b_x16(acol + 16 * h, out);
           }
         } else {
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
               if (kc >= (j + 1) * p.g && j < p.G - 1) ++j;  // g >= 8: at most one group boundary per 8 codes
               const uint32_t rec = recs + (j - jlo) * kRecBytes;
               const uint32_t z = (lds8(rec + 256 + r / 2) >> (4 * (r & 1))) & 0xFu;
-              dequant_word(words[4 * h + ci], group_consts(lds16(rec + 2 * r), z), &out[4 * ci]);
+              dequant_word<DT>(words[4 * h + ci], group_consts<DT>(lds16(rec + 2 * r), z), &out[4 * ci]);
             }
             tmem_st_32x32b_x16(acol + 16 * h, out);
           }
@@ -501,7 +515,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
                 for (int q = 0; q < 16; ++q) f[q] += __ldcg(src + q * kTN);
               }
             }
-            emit16<BN>(p, whole || owner, n, m0, m_end, c0, f, piece);
+            emit16<BN, DT>(p, whole || owner, n, m0, m_end, c0, f, piece);
           }
         }
       }
@@ -534,17 +548,31 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       const int m0 = (tile % p.MT) * BN;
       const int ncols = min(p.M, m0 + BN) - m0;
       const int tid = static_cast<int>(threadIdx.x) - 32 * C::kDqWarp0;
+      // silu * up takes rows in (gate, up) pairs
+      const int step = p.epi.kind == kEpiSiluMul ? 2 : 1;
 #pragma unroll
       for (int te = 0; te < C::kTP; ++te) {
 #pragma unroll 2
-        for (int e = tid; e < ncols * kTN; e += kFixThreads) {
+        for (int e = tid * step; e < ncols * kTN; e += kFixThreads * step) {
           const int o = te * BN * kTN + e;
           float acc = own[o];
 #pragma unroll
           for (int pc = 1; pc < kMaxPieces; ++pc)
             if (pc < npieces) acc += __ldcg(piece_of<BN, C::kTP>(p, cta + pc, 0) + o);
           const int n = n0 + te * kTN + e % kTN;
-          if (n < p.N) p.y[static_cast<int64_t>(m0 + e / kTN) * p.N + n] = __float2half_rn(acc);
+          const int64_t m = m0 + e / kTN;
+          if (n >= p.N) continue;
+          if (step == 2) {
+            float up = own[o + 1];
+#pragma unroll
+            for (int pc = 1; pc < kMaxPieces; ++pc)
+              if (pc < npieces) up += __ldcg(piece_of<BN, C::kTP>(p, cta + pc, 0) + o + 1);
+            p.y[m * p.epi.ld + n / 2] = out_bits<DT>(silu_mul(acc, up));
+          } else {
+            int ld;
+            uint16_t *dst = epi_row(p.epi, p.y, n, &ld);
+            dst[m * ld] = out_bits<DT>(acc);
+          }
         }
       }
     }
@@ -585,9 +613,10 @@ EncodeTiledFn encode_tiled_fn() {
 //  3-D [K/64][M][64] (K a multiple of 64): one box {64, BN, sbk} is a whole stage, sbk BN x 64
 //      sub-tiles one after another, each laid out as the MMA reads it;
 //  2-D [M][K]: one box {64, BN} per K block.
-bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, int sbk, bool three_d) {
+bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, int sbk, bool three_d, int dtype) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
+  const CUtensorMapDataType dt = dtype == kDtypeBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (three_d) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kTK), static_cast<cuuint64_t>(M),
                                 static_cast<cuuint64_t>(K / kTK)};
@@ -595,7 +624,7 @@ bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, i
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(kTK), static_cast<cuuint32_t>(bn),
                                static_cast<cuuint32_t>(sbk)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(x), dims, strides, box, estr,
+    return enc(map, dt, 3, const_cast<void *>(x), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   }
@@ -603,7 +632,7 @@ bool make_x_map(CUtensorMap *map, const void *x, int64_t M, int64_t K, int bn, i
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTK), static_cast<cuuint32_t>(bn)};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+  return enc(map, dt, 2, const_cast<void *>(x), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -636,11 +665,11 @@ bool make_weight_maps(CUtensorMap *code_map, CUtensorMap *rec_map, const void *p
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, int TP>
+template <int BN, int MODE, int TP, int DT>
 cudaError_t launch_t(const CUtensorMap &map, const CUtensorMap &code_map, const CUtensorMap &rec_map, const Params &p,
                      int ctas, cudaStream_t stream) {
   using C = Cfg<BN, MODE, TP>;
-  auto kern = w4a16_gemm_kernel<BN, MODE, TP>;
+  auto kern = w4a16_gemm_kernel<BN, MODE, TP, DT>;
   // the dynamic shared-memory opt-in is a per-device function attribute
   static uint64_t done_mask = 0;
   static std::mutex mu;
@@ -661,20 +690,21 @@ cudaError_t launch_t(const CUtensorMap &map, const CUtensorMap &code_map, const 
 // One group per 64-wide K block (g % 64 == 0) lets the dequant take the block's group once.
 int gemm_mode(int32_t g) { return g % 64 == 0 ? kScaleIn : kGeneral; }
 
+template <int DT>
 cudaError_t launch_variant(int bn, int mode, int tp, const CUtensorMap &map, const CUtensorMap &code_map,
                            const CUtensorMap &rec_map, const Params &p, int ctas, cudaStream_t stream) {
   if (mode == kScaleIn) {
-    if (bn == 16) return launch_t<16, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 32) return launch_t<32, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 64) return launch_t<64, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 128 && tp == 1) return launch_t<128, kScaleIn, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 128 && tp == 2) return launch_t<128, kScaleIn, 2>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 16) return launch_t<16, kScaleIn, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 32) return launch_t<32, kScaleIn, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 64) return launch_t<64, kScaleIn, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 1) return launch_t<128, kScaleIn, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 2) return launch_t<128, kScaleIn, 2, DT>(map, code_map, rec_map, p, ctas, stream);
   } else {
-    if (bn == 16) return launch_t<16, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 32) return launch_t<32, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 64) return launch_t<64, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 128 && tp == 1) return launch_t<128, kGeneral, 1>(map, code_map, rec_map, p, ctas, stream);
-    if (bn == 128 && tp == 2) return launch_t<128, kGeneral, 2>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 16) return launch_t<16, kGeneral, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 32) return launch_t<32, kGeneral, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 64) return launch_t<64, kGeneral, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 1) return launch_t<128, kGeneral, 1, DT>(map, code_map, rec_map, p, ctas, stream);
+    if (bn == 128 && tp == 2) return launch_t<128, kGeneral, 2, DT>(map, code_map, rec_map, p, ctas, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -785,37 +815,84 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOption
   return true;
 }
 
+bool epi_valid(const EpiSpec &e, int64_t N) {
+  if (e.kind == kEpiNone) return true;
+  if (e.kind == kEpiSiluMul) return N % 2 == 0;
+  if (e.kind != kEpiQkv) return false;
+  if (e.head_dim < 4 || e.head_dim % 4 != 0 || e.q_per_group < 1 || !e.k || !e.v) return false;
+  const int64_t span = static_cast<int64_t>(e.q_per_group + 2) * e.head_dim;
+  return span <= N && N % span == 0;
+}
+
+namespace {
+
+Epi make_epi(const EpiSpec &e, int64_t N) {
+  Epi d{};
+  d.kind = e.kind;
+  d.ld = static_cast<int>(e.kind == kEpiSiluMul ? N / 2 : N);
+  if (e.kind == kEpiQkv) {
+    const int64_t groups = N / ((e.q_per_group + 2) * static_cast<int64_t>(e.head_dim));
+    d.d = e.head_dim;
+    d.r = e.q_per_group;
+    d.ld = static_cast<int>(groups * e.q_per_group * e.head_dim);
+    d.ldkv = static_cast<int>(groups * e.head_dim);
+    d.k = static_cast<uint16_t *>(e.k);
+    d.v = static_cast<uint16_t *>(e.v);
+  }
+  return d;
+}
+
+// One problem's entry of the decode kernel's table, its tiles from `tile_begin`.
+DecProblem dec_problem(const void *x, const void *packed, void *y, int64_t N, int64_t K, int32_t g,
+                       const EpiSpec &epi, int tile_begin) {
+  DecProblem d{};
+  const int64_t nt = cdiv(N, kTN), kb = cdiv(K, kTK);
+  d.x = static_cast<const uint16_t *>(x);
+  d.codes = static_cast<const uint8_t *>(packed);
+  d.meta = d.codes + nt * kb * kTileBytes;
+  d.y = static_cast<uint16_t *>(y);
+  d.epi = make_epi(epi, N);
+  d.N = static_cast<int>(N);
+  d.K = static_cast<int>(K);
+  d.G = static_cast<int>(cdiv(K, g));
+  d.NT = static_cast<int>(nt);
+  d.KB = static_cast<int>(kb);
+  d.KS = static_cast<int>(cdiv(kb, kSB));
+  d.tile_begin = tile_begin;
+  d.tile_end = tile_begin + d.NT;
+  return d;
+}
+
+DecParams dec_params(int64_t M, int32_t g, void *workspace, const GemmOptions &opt) {
+  DecParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.err = static_cast<uint32_t *>(workspace);
+  p.M = static_cast<int>(M);
+  p.g = g;
+  p.early = opt.weights_static ? 1 : 0;
+  p.gdiv = make_fastdiv(static_cast<uint32_t>(g));
+  p.wait_limit = opt.wait_limit ? opt.wait_limit : kWaitLimitCycles;
+  p.test_extra_tx = opt.test_timeout ? 4u : 0u;
+  return p;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y,
-                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, cudaStream_t stream,
-                        bool *encode_failed) {
+                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, const EpiSpec &epi,
+                        cudaStream_t stream, bool *encode_failed) {
   *encode_failed = false;
   CUtensorMap map;
   if (plan.kernel == kKernelDecode) {
-    DecParams p;
-    p.x = static_cast<const __half *>(x);
-    p.codes = static_cast<const uint8_t *>(packed);
-    p.meta = p.codes + static_cast<int64_t>(plan.n_tiles) * plan.k_blocks * kTileBytes;
-    p.y = static_cast<__half *>(y);
-    p.err = static_cast<uint32_t *>(workspace);
-    p.M = static_cast<int>(M);
-    p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.g = g;
-    p.G = static_cast<int>(cdiv(K, g));
-    p.NT = plan.n_tiles;
-    p.KB = plan.k_blocks;
-    p.KS = plan.k_stages;
-    p.C = 0;
-    p.Q = 0;
-    p.early = opt.weights_static ? 1 : 0;
-    p.gdiv = make_fastdiv(static_cast<uint32_t>(g));
-    p.wait_limit = opt.wait_limit ? opt.wait_limit : kWaitLimitCycles;
-    p.test_extra_tx = opt.test_timeout ? 4u : 0u;
-    return launch_gemm_dec(p, plan.block_n / 8, plan.ctas, plan.cluster, stream);
+    DecParams p = dec_params(M, g, workspace, opt);
+    p.prob[0] = dec_problem(x, packed, y, N, K, g, epi, 0);
+    p.nprob = 1;
+    p.tiles = p.prob[0].NT;
+    return launch_gemm_dec(p, plan.block_n / 8, opt.dtype, plan.ctas, plan.cluster, stream);
   }
   const int sbk = kSB / plan.tiles_per_unit;
-  bool x3d = K % kTK == 0 && make_x_map(&map, x, M, K, plan.block_n, sbk, true);
-  if (!x3d && !make_x_map(&map, x, M, K, plan.block_n, sbk, false)) {
+  bool x3d = K % kTK == 0 && make_x_map(&map, x, M, K, plan.block_n, sbk, true, opt.dtype);
+  if (!x3d && !make_x_map(&map, x, M, K, plan.block_n, sbk, false, opt.dtype)) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
@@ -833,7 +910,7 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   Params p;
   p.codes = static_cast<const uint8_t *>(packed);
   p.meta = p.codes + static_cast<int64_t>(plan.n_tiles) * plan.k_blocks * kTileBytes;
-  p.y = static_cast<__half *>(y);
+  p.y = static_cast<uint16_t *>(y);
   p.pieces = reinterpret_cast<float *>(ws + plan.pieces_offset);
   p.counters = reinterpret_cast<uint32_t *>(ws + plan.counters_offset);
   p.err = reinterpret_cast<uint32_t *>(ws);
@@ -854,8 +931,75 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.grains = plan.grains;
   p.wait_limit = opt.wait_limit ? opt.wait_limit : kWaitLimitCycles;
   p.test_extra_piece = opt.test_timeout ? 1 : 0;
-  return launch_variant(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p, plan.ctas,
-                        stream);
+  p.epi = make_epi(epi, N);
+  if (opt.dtype == kDtypeBf16)
+    return launch_variant<kDtypeBf16>(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p,
+                                      plan.ctas, stream);
+  return launch_variant<kDtypeF16>(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p,
+                                   plan.ctas, stream);
+}
+
+
+bool make_group_plan(const GemmProblem *probs, int count, int64_t M, int32_t g, const GemmOptions &opt, int num_sms,
+                     GroupPlan *plan) {
+  if (count < 1) return false;
+  *plan = GroupPlan{};
+  // the decode kernel runs the whole group when it would run each problem alone; the planner's checks
+  // of the options (cluster sizes, tokens per tile) apply to every problem
+  bool all_dec = true;
+  for (int i = 0; i < count; ++i) {
+    GemmPlan pl;
+    if (!make_gemm_plan(M, probs[i].N, probs[i].K, g, opt, num_sms, &pl)) return false;
+    if (pl.kernel != kKernelDecode) all_dec = false;
+    if (i == 0) plan->block_n = pl.block_n;
+    plan->workspace_bytes = std::max(plan->workspace_bytes, pl.workspace_bytes);
+  }
+  // one cluster size must suit every problem of a launch (at most each one's K stages, and short
+  // enough K ranges for x to fit); otherwise the problems run one launch each
+  bool common = false;
+  for (int c : {1, 2, 4, 8}) {
+    if (opt.cluster > 0 && c != opt.cluster) continue;
+    bool ok = true;
+    for (int i = 0; i < count && ok; ++i) {
+      const int64_t ks = cdiv(cdiv(probs[i].K, kTK), kSB);
+      ok = c <= ks && dec_x_fits(ks, c, M);
+    }
+    common = common || ok;
+  }
+  plan->decode = all_dec && common;
+  return true;
+}
+
+cudaError_t launch_gemm_grouped(const GemmProblem *probs, int count, int64_t M, int32_t g, void *workspace,
+                                const GroupPlan &plan, const GemmOptions &opt, int num_sms, cudaStream_t stream,
+                                bool *encode_failed) {
+  *encode_failed = false;
+  if (plan.decode) {
+    for (int i0 = 0; i0 < count; i0 += kGroupMax) {
+      const int n = std::min(count - i0, kGroupMax);
+      DecParams p = dec_params(M, g, workspace, opt);
+      int tiles = 0;
+      for (int i = 0; i < n; ++i) {
+        const GemmProblem &pr = probs[i0 + i];
+        p.prob[i] = dec_problem(pr.x, pr.packed, pr.y, pr.N, pr.K, g, pr.epi, tiles);
+        tiles = p.prob[i].tile_end;
+      }
+      p.nprob = n;
+      p.tiles = tiles;
+      const cudaError_t e = launch_gemm_dec(p, plan.block_n / 8, opt.dtype, opt.ctas, opt.cluster, stream);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  for (int i = 0; i < count; ++i) {
+    const GemmProblem &pr = probs[i];
+    GemmPlan pl;
+    if (!make_gemm_plan(M, pr.N, pr.K, g, opt, num_sms, &pl)) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_gemm(pr.x, pr.packed, M, pr.N, pr.K, g, pr.y, workspace, pl, opt, pr.epi, stream,
+                                      encode_failed);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace w4

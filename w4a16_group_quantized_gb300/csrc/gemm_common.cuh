@@ -1,9 +1,10 @@
 // Pieces shared by the GEMM kernels: the schedule (persistent CTAs over (tile, K stage) units:
-// stream-K ranges or round-robin whole tiles), the one-tile weight-stream producer, the fp16
+// stream-K ranges or round-robin whole tiles), the one-tile weight-stream producer, the fp16 / bf16
 // dequant of 8 packed codes, bounded waits and the owner-reduces finish of tiles cut between CTAs.
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -38,6 +39,43 @@ inline FastDiv make_fastdiv(uint32_t d) {
   return f;
 }
 
+// Output epilogues. The fp32 sum of weight row n for token m goes to
+//   kEpiNone     y[m * ld + n];
+//   kEpiSiluMul  rows alternate gate, up (row 2j: gate j, row 2j + 1: up j): h[m * ld + j] =
+//                silu(gate) * up, silu(v) = v / (1 + e^-v), from the two fp32 sums, rounded once;
+//   kEpiQkv      rows in head groups of (r query heads, 1 key head, 1 value head) x d rows: row n of
+//                group n / ((r + 2) d), head hh = n % ((r + 2) d) / d goes to q (y) column
+//                (grp r + hh) d + n % d for hh < r, to k column grp d + n % d for hh == r, to v for
+//                hh == r + 1; q has ld columns per token, k and v ldkv.
+struct Epi {
+  int kind;
+  int d, r;        // kEpiQkv: head size, query heads per group
+  int ld, ldkv;    // output columns per token: y (or q, or h) and k / v
+  uint16_t *k, *v;
+};
+
+// Where row n of token 0 goes (kEpiNone, kEpiQkv; d a multiple of 4, so four rows from a multiple
+// of 4 stay in one head) and the output's columns per token.
+__device__ __forceinline__ uint16_t *epi_row(const Epi &e, uint16_t *y, int n, int *ld) {
+  if (e.kind != kEpiQkv) {
+    *ld = e.ld;
+    return y + n;
+  }
+  const int span = (e.r + 2) * e.d;
+  const int grp = n / span;
+  const int w = n - grp * span;
+  const int hh = w / e.d;
+  const int c = w - hh * e.d;
+  if (hh < e.r) {
+    *ld = e.ld;
+    return y + (grp * e.r + hh) * e.d + c;
+  }
+  *ld = e.ldkv;
+  return (hh == e.r ? e.k : e.v) + grp * e.d + c;
+}
+
+__device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + expf(-gate)) * up; }
+
 // Work decomposition. A unit is one K stage of one output tile (128 weight rows, or 256 for two-tile
 // units, x BN activation rows); units are numbered tile-major: u = tile * KS + ks, tile = t * MT + mt.
 // CTA c owns the contiguous units [begin(c), begin(c+1)), cut at multiples of `gran` units
@@ -47,7 +85,7 @@ inline FastDiv make_fastdiv(uint32_t d) {
 struct Params {
   const uint8_t *codes;  // tile region of the packed weights
   const uint8_t *meta;   // group-record region of the packed weights
-  __half *y;
+  uint16_t *y;           // fp16 or bf16 bits
   float *pieces;         // [P][2][BN][128] fp32 partial tiles (first and last segment of each CTA)
   uint32_t *counters;    // [tiles] arrivals per split tile
   uint32_t *err;
@@ -60,6 +98,7 @@ struct Params {
   int64_t grains;        // total units / gran
   uint64_t wait_limit;   // cycles a wait may take before the kernel gives up
   int test_extra_piece;  // test only: owners wait for this many pieces more than will come
+  Epi epi;               // where the sums go (y: q for kEpiQkv, h for kEpiSiluMul)
 };
 
 __device__ __forceinline__ int64_t range_begin(const Params &p, int c) {
@@ -143,35 +182,73 @@ __device__ __forceinline__ uint32_t lds8(uint32_t addr) {
 // Per-(row, group) dequant constants as fp16x2 pairs.
 struct GroupConsts {
   uint32_t s2;    // (s, s)
-  uint32_t zb2;   // (1024 + z, 1024 + z)
-  uint32_t nz2;   // (-(64 + z), -(64 + z))
+  uint32_t zb2;   // fp16: (1024 + z, 1024 + z); bf16: (128 + z, 128 + z)
+  uint32_t nz2;   // fp16: (-(64 + z), -(64 + z)); bf16: unused
 };
 
+template <int DT = kDtypeF16>
 __device__ __forceinline__ GroupConsts group_consts(uint32_t sbits, uint32_t z) {
   GroupConsts c;
   c.s2 = sbits * 0x00010001u;
-  c.zb2 = (0x6400u + z) * 0x00010001u;          // fp16 1024 + z: exponent of 1024, z in the fraction
-  c.nz2 = (0xD400u + 16u * z) * 0x00010001u;    // fp16 -(64 + z): step of 1/16 at 64
+  if (DT == kDtypeBf16) {
+    c.zb2 = (0x4300u + z) * 0x00010001u;        // bf16 128 + z: exponent of 128, z in the fraction
+    c.nz2 = 0u;
+  } else {
+    c.zb2 = (0x6400u + z) * 0x00010001u;        // fp16 1024 + z: exponent of 1024, z in the fraction
+    c.nz2 = (0xD400u + 16u * z) * 0x00010001u;  // fp16 -(64 + z): step of 1/16 at 64
+  }
   return c;
 }
 
-// 8 codes (tile nibble order) -> 4 registers of fp16 pairs (k, k+1) holding q - z exactly.
-// 0x6400 | q is the fp16 1024 + q and 0x6400 | (q << 4) is 1024 + 16 q, both exact; subtracting
+// 8 codes (tile nibble order: code e at nibble 4 (e % 2) + e / 2) -> 4 registers of 16-bit pairs
+// (k, k+1) holding q - z exactly.
+// fp16: 0x6400 | q is 1024 + q and 0x6400 | (q << 4) is 1024 + 16 q, both exact; subtracting
 // 1024 + z (or scaling by 1/16 and adding -(64 + z)) leaves the small integer q - z, exact.
+// bf16 (7 fraction bits): only the low nibble of each half fits under the exponent of 128, so the
+// word is shifted by 0, 4, 8 and 12 bits; 0x4300 | q is 128 + q, and subtracting 128 + z is exact.
+template <int DT = kDtypeF16>
 __device__ __forceinline__ void dequant_word_int(uint32_t w, const GroupConsts &c, uint32_t *o) {
-  constexpr uint32_t kInv16x2 = 0x2C002C00u;  // (1/16, 1/16)
-  const uint32_t w8 = w >> 8;
-  o[0] = hsub2_rn(lop3_and_or(w, 0x000F000Fu, 0x64006400u), c.zb2);
-  o[1] = hfma2_rn(lop3_and_or(w, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
-  o[2] = hsub2_rn(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), c.zb2);
-  o[3] = hfma2_rn(lop3_and_or(w8, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
+  if (DT == kDtypeBf16) {
+    o[0] = bsub2_rn(lop3_and_or(w, 0x000F000Fu, 0x43004300u), c.zb2);
+    o[1] = bsub2_rn(lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u), c.zb2);
+    o[2] = bsub2_rn(lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u), c.zb2);
+    o[3] = bsub2_rn(lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u), c.zb2);
+  } else {
+    constexpr uint32_t kInv16x2 = 0x2C002C00u;  // (1/16, 1/16)
+    const uint32_t w8 = w >> 8;
+    o[0] = hsub2_rn(lop3_and_or(w, 0x000F000Fu, 0x64006400u), c.zb2);
+    o[1] = hfma2_rn(lop3_and_or(w, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
+    o[2] = hsub2_rn(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), c.zb2);
+    o[3] = hfma2_rn(lop3_and_or(w8, 0x00F000F0u, 0x64006400u), kInv16x2, c.nz2);
+  }
 }
 
-// As dequant_word_int, then one multiply by s: each weight (q - z) * s rounded once to fp16.
+// As dequant_word_int, then one multiply by s: each weight (q - z) * s rounded once to the type.
+template <int DT = kDtypeF16>
 __device__ __forceinline__ void dequant_word(uint32_t w, const GroupConsts &c, uint32_t *o) {
-  dequant_word_int(w, c, o);
+  dequant_word_int<DT>(w, c, o);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = hmul2_rn(o[i], c.s2);
+  for (int i = 0; i < 4; ++i) o[i] = DT == kDtypeBf16 ? bmul2_rn(o[i], c.s2) : hmul2_rn(o[i], c.s2);
+}
+
+// A stored scale (fp16 or bf16 bits) as fp32, exactly.
+template <int DT>
+__device__ __forceinline__ float scale_f32(uint32_t bits) {
+  if (DT == kDtypeBf16) return __uint_as_float(bits << 16);
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+// An fp32 sum rounded once (to nearest even) to the output type, as bits.
+template <int DT>
+__device__ __forceinline__ uint16_t out_bits(float v) {
+  if (DT == kDtypeBf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+// Two of them as one 32-bit word (lo at the lower address).
+template <int DT>
+__device__ __forceinline__ uint32_t out_bits2(float lo, float hi) {
+  return static_cast<uint32_t>(out_bits<DT>(lo)) | (static_cast<uint32_t>(out_bits<DT>(hi)) << 16);
 }
 
 // A wait whose outcome is the same for all 32 lanes: the warp then either executes the
@@ -319,16 +396,28 @@ cudaError_t launch_programmatic(Kernel kern, int ctas, int threads, int smem_byt
   return cudaGetLastError();
 }
 
-// Parameters of the cluster decode kernel (gemm_dec.cu): M <= 8 * nb8 tokens, one token tile.
-struct DecParams {
-  const __half *x;       // [M, K] activations
+// Parameters of the cluster decode kernel (gemm_dec.cu): M <= 8 * nb8 tokens, one token tile, and one
+// or more independent problems (same M, g and type) whose weight tiles the launch walks in order.
+constexpr int kDecMaxProblems = kGroupMax;
+
+struct DecProblem {
+  const uint16_t *x;     // [M, K] activations (fp16 or bf16 bits)
   const uint8_t *codes;  // tile region of the packed weights
   const uint8_t *meta;   // group-record region of the packed weights
-  __half *y;
+  uint16_t *y;           // output (q for kEpiQkv, h for kEpiSiluMul)
+  Epi epi;
+  int N, K, G, NT, KB, KS;
+  int tile_begin, tile_end;  // the problem's tiles in the launch's tile sequence
+};
+
+struct DecParams {
+  DecProblem prob[kDecMaxProblems];
+  int nprob;
+  int tiles;             // all problems' weight tiles
   uint32_t *err;
-  int M, N, K, g, G, NT, KB, KS;
+  int M, g;
   int C;                 // CTAs per cluster; each takes a contiguous K range of every tile of the cluster
-  int Q;                 // clusters; cluster q takes the weight tiles q, q + Q, ...
+  int Q;                 // clusters; cluster q takes the tiles q, q + Q, ...
   int xslice;            // 256-wide K stages of x each CTA keeps in shared memory (its longest K range)
   int S;                 // stages in the weight ring (even)
   int early;             // issue the first stages' weight copies before waiting for the previous grid
@@ -337,8 +426,9 @@ struct DecParams {
   uint64_t wait_limit;   // cycles a pipeline wait may take before the kernel gives up
 };
 
-// Launches the decode kernel with `clusters` clusters of `cluster` CTAs (0: chosen for the layer).
-cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int clusters, int cluster, cudaStream_t stream);
+// Launches the decode kernel with `clusters` clusters of `cluster` CTAs (0: chosen for the layer), for
+// fp16 or bf16 (dtype) activations, scales and outputs.
+cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int dtype, int clusters, int cluster, cudaStream_t stream);
 
 }  // namespace detail
 }  // namespace w4

@@ -1,6 +1,7 @@
 // w4a16_gemm for decode batches (M <= 16 tokens): the dequantized weights go straight into the A
-// fragments of register-operand tensor-core MMAs (mma.sync m16n8k16, fp16 in, fp32 accumulate), so a
-// weight is read once as a 4-bit code, turned into fp16 in registers and consumed there.
+// fragments of register-operand tensor-core MMAs (mma.sync m16n8k16, fp16 or bf16 in, fp32
+// accumulate), so a weight is read once as a 4-bit code, turned into fp16 / bf16 in registers and
+// consumed there.
 //
 // Work split: the weight tiles (128 rows each) are dealt out to thread-block clusters round-robin
 // (cluster q: tiles q, q + Q, ...). The C CTAs of a cluster split every tile along K: CTA rank k
@@ -37,8 +38,11 @@
 // This is Marlin's register-level dequant into MMA fragments (Marlin post) carried to sm_103a, with
 // TMA/mbarrier staging, clusters and distributed shared memory for the split along K.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "gemm_common.cuh"
@@ -118,13 +122,21 @@ __device__ __forceinline__ uint4 lds128_at(uint32_t addr) {
   return v;
 }
 
-// D (+)= A . B, m16n8k16, A row-major fp16 (4 regs), B column-major fp16 (2 regs), fp32 D.
+// D (+)= A . B, m16n8k16, A row-major (4 regs), B column-major (2 regs), both fp16 or both bf16, fp32 D.
+template <int DT>
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  if (DT == kDtypeBf16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // The two rows a lane serves in a slab (rows R and R + 8): dequant constants and fp32 scales.
@@ -134,22 +146,24 @@ struct SlabConsts {
 };
 
 // Integer path: zero points of rows R, R + 8 from the record at `rec`, scales as fp32.
+template <int DT>
 __device__ __forceinline__ SlabConsts slab_consts_int(uint32_t rec, uint32_t zero_off, uint32_t zero_shift,
                                                       uint32_t scale_off) {
   SlabConsts c;
-  c.a = group_consts(0u, (lds8_at<0>(rec + zero_off) >> zero_shift) & 0xFu);
-  c.b = group_consts(0u, (lds8_at<4>(rec + zero_off) >> zero_shift) & 0xFu);
-  c.sa = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at<0>(rec + scale_off))));
-  c.sb = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at<16>(rec + scale_off))));
+  c.a = group_consts<DT>(0u, (lds8_at<0>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.b = group_consts<DT>(0u, (lds8_at<4>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.sa = scale_f32<DT>(lds16_at<0>(rec + scale_off));
+  c.sb = scale_f32<DT>(lds16_at<16>(rec + scale_off));
   return c;
 }
 
 // Scaled path: the full constants (scale applied in the dequant) of rows R, R + 8.
+template <int DT>
 __device__ __forceinline__ SlabConsts slab_consts_scaled(uint32_t rec, uint32_t zero_off, uint32_t zero_shift,
                                                          uint32_t scale_off) {
   SlabConsts c;
-  c.a = group_consts(lds16_at<0>(rec + scale_off), (lds8_at<0>(rec + zero_off) >> zero_shift) & 0xFu);
-  c.b = group_consts(lds16_at<16>(rec + scale_off), (lds8_at<4>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.a = group_consts<DT>(lds16_at<0>(rec + scale_off), (lds8_at<0>(rec + zero_off) >> zero_shift) & 0xFu);
+  c.b = group_consts<DT>(lds16_at<16>(rec + scale_off), (lds8_at<4>(rec + zero_off) >> zero_shift) & 0xFu);
   c.sa = c.sb = 1.0f;
   return c;
 }
@@ -167,22 +181,22 @@ struct XLane {
   bool v0, v1;    // token g, 8 + g < M
 };
 
-template <int NB8, int BB, bool SCALED>
+template <int NB8, int BB, bool SCALED, int DT>
 __device__ __forceinline__ void dec_block(uint32_t codes, const XLane &xl, const SlabConsts &c0,
                                           const SlabConsts &c1, float (&acc)[NB8][4]) {
   const uint2 wr = lds64_at<BB * kTileBytes>(codes);        // row R: words 2t, 2t + 1
   const uint2 ws = lds64_at<BB * kTileBytes + 128>(codes);  // row R + 8
   uint32_t r0[4], r1[4], s0[4], s1[4];
   if (SCALED) {
-    dequant_word(wr.x, c0.a, r0);
-    dequant_word(wr.y, c1.a, r1);
-    dequant_word(ws.x, c0.b, s0);
-    dequant_word(ws.y, c1.b, s1);
+    dequant_word<DT>(wr.x, c0.a, r0);
+    dequant_word<DT>(wr.y, c1.a, r1);
+    dequant_word<DT>(ws.x, c0.b, s0);
+    dequant_word<DT>(ws.y, c1.b, s1);
   } else {
-    dequant_word_int(wr.x, c0.a, r0);
-    dequant_word_int(wr.y, c0.a, r1);
-    dequant_word_int(ws.x, c0.b, s0);
-    dequant_word_int(ws.y, c0.b, s1);
+    dequant_word_int<DT>(wr.x, c0.a, r0);
+    dequant_word_int<DT>(wr.y, c0.a, r1);
+    dequant_word_int<DT>(ws.x, c0.b, s0);
+    dequant_word_int<DT>(ws.y, c0.b, s1);
   }
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) {
@@ -194,19 +208,19 @@ __device__ __forceinline__ void dec_block(uint32_t codes, const XLane &xl, const
     }
     {
       const uint32_t a[4] = {r0[0], s0[0], r0[1], s0[1]};
-      mma16816(acc[nb], a, x0.x, x0.y);
+      mma16816<DT>(acc[nb], a, x0.x, x0.y);
     }
     {
       const uint32_t a[4] = {r0[2], s0[2], r0[3], s0[3]};
-      mma16816(acc[nb], a, x0.z, x0.w);
+      mma16816<DT>(acc[nb], a, x0.z, x0.w);
     }
     {
       const uint32_t a[4] = {r1[0], s1[0], r1[1], s1[1]};
-      mma16816(acc[nb], a, x1.x, x1.y);
+      mma16816<DT>(acc[nb], a, x1.x, x1.y);
     }
     {
       const uint32_t a[4] = {r1[2], s1[2], r1[3], s1[3]};
-      mma16816(acc[nb], a, x1.z, x1.w);
+      mma16816<DT>(acc[nb], a, x1.z, x1.w);
     }
   }
 }
@@ -244,9 +258,9 @@ __device__ __forceinline__ bool has_block(bool full, int nbk) {
 
 // One stage (up to four K blocks from k0) of a lane's two rows, accumulated into tot. FULL: all four
 // blocks present (the compiler then sees straight-line code); else nbk of them.
-template <int NB8, int MODE, int CODEBYTES, bool FULL>
-__device__ __forceinline__ void dec_stage(const DecParams &p, uint32_t stage, uint32_t xstage, const LaneOffsets &o,
-                                          int k0, int nbk, int t, float (&tot)[NB8][4]) {
+template <int NB8, int MODE, int CODEBYTES, bool FULL, int DT>
+__device__ __forceinline__ void dec_stage(const DecParams &p, int G, uint32_t stage, uint32_t xstage,
+                                          const LaneOffsets &o, int k0, int nbk, int t, float (&tot)[NB8][4]) {
   const uint32_t codes = stage + o.code;
   XLane xb;
   xb.a = xstage + o.x0;
@@ -256,27 +270,27 @@ __device__ __forceinline__ void dec_stage(const DecParams &p, uint32_t stage, ui
   xb.v1 = o.xv1;
   const uint32_t recs = stage + CODEBYTES;
   if (MODE == kDecG256) {  // g % 256 == 0: the whole stage lies in one group
-    const SlabConsts c = slab_consts_int(recs, o.zero, o.zero_shift, o.scale);
+    const SlabConsts c = slab_consts_int<DT>(recs, o.zero, o.zero_shift, o.scale);
     float acc[NB8][4];
     zero_acc<NB8>(acc);
-    dec_block<NB8, 0, false>(codes, xb, c, c, acc);
-    if (has_block<1>(FULL, nbk)) dec_block<NB8, 1, false>(codes, xb, c, c, acc);
-    if (has_block<2>(FULL, nbk)) dec_block<NB8, 2, false>(codes, xb, c, c, acc);
-    if (has_block<3>(FULL, nbk)) dec_block<NB8, 3, false>(codes, xb, c, c, acc);
+    dec_block<NB8, 0, false, DT>(codes, xb, c, c, acc);
+    if (has_block<1>(FULL, nbk)) dec_block<NB8, 1, false, DT>(codes, xb, c, c, acc);
+    if (has_block<2>(FULL, nbk)) dec_block<NB8, 2, false, DT>(codes, xb, c, c, acc);
+    if (has_block<3>(FULL, nbk)) dec_block<NB8, 3, false, DT>(codes, xb, c, c, acc);
     flush_scaled<NB8>(tot, acc, c);
   } else if (MODE == kDecG128) {  // g == 128: blocks 0, 1 in the stage's first group, 2, 3 in the next
-    const SlabConsts c0 = slab_consts_int(recs, o.zero, o.zero_shift, o.scale);
+    const SlabConsts c0 = slab_consts_int<DT>(recs, o.zero, o.zero_shift, o.scale);
     float acc[NB8][4];
     zero_acc<NB8>(acc);
-    dec_block<NB8, 0, false>(codes, xb, c0, c0, acc);
-    if (has_block<1>(FULL, nbk)) dec_block<NB8, 1, false>(codes, xb, c0, c0, acc);
+    dec_block<NB8, 0, false, DT>(codes, xb, c0, c0, acc);
+    if (has_block<1>(FULL, nbk)) dec_block<NB8, 1, false, DT>(codes, xb, c0, c0, acc);
     flush_scaled<NB8>(tot, acc, c0);
     if (has_block<2>(FULL, nbk)) {
-      const SlabConsts c1 = slab_consts_int(recs + kRecBytes, o.zero, o.zero_shift, o.scale);
+      const SlabConsts c1 = slab_consts_int<DT>(recs + kRecBytes, o.zero, o.zero_shift, o.scale);
       float acc1[NB8][4];
       zero_acc<NB8>(acc1);
-      dec_block<NB8, 2, false>(codes, xb, c1, c1, acc1);
-      if (has_block<3>(FULL, nbk)) dec_block<NB8, 3, false>(codes, xb, c1, c1, acc1);
+      dec_block<NB8, 2, false, DT>(codes, xb, c1, c1, acc1);
+      if (has_block<3>(FULL, nbk)) dec_block<NB8, 3, false, DT>(codes, xb, c1, c1, acc1);
       flush_scaled<NB8>(tot, acc1, c1);
     }
   } else if (MODE == kDecG64) {  // g % 64 == 0: each block lies in one group, looked up per block
@@ -285,13 +299,13 @@ __device__ __forceinline__ void dec_stage(const DecParams &p, uint32_t stage, ui
     for (int bb = 0; bb < kSB; ++bb) {
       if (FULL || bb < nbk) {
         const uint32_t rec = recs + (p.gdiv.div(k0 + bb * kTK) - jlo) * kRecBytes;
-        const SlabConsts c = slab_consts_int(rec, o.zero, o.zero_shift, o.scale);
+        const SlabConsts c = slab_consts_int<DT>(rec, o.zero, o.zero_shift, o.scale);
         float acc[NB8][4];
         zero_acc<NB8>(acc);
-        if (bb == 0) dec_block<NB8, 0, false>(codes, xb, c, c, acc);
-        if (bb == 1) dec_block<NB8, 1, false>(codes, xb, c, c, acc);
-        if (bb == 2) dec_block<NB8, 2, false>(codes, xb, c, c, acc);
-        if (bb == 3) dec_block<NB8, 3, false>(codes, xb, c, c, acc);
+        if (bb == 0) dec_block<NB8, 0, false, DT>(codes, xb, c, c, acc);
+        if (bb == 1) dec_block<NB8, 1, false, DT>(codes, xb, c, c, acc);
+        if (bb == 2) dec_block<NB8, 2, false, DT>(codes, xb, c, c, acc);
+        if (bb == 3) dec_block<NB8, 3, false, DT>(codes, xb, c, c, acc);
         flush_scaled<NB8>(tot, acc, c);
       }
     }
@@ -302,21 +316,21 @@ __device__ __forceinline__ void dec_stage(const DecParams &p, uint32_t stage, ui
     for (int bb = 0; bb < kSB; ++bb) {
       if (FULL || bb < nbk) {
         const int kw = k0 + bb * kTK + 16 * t;
-        const uint32_t r0 = recs + (min(p.gdiv.div(kw), p.G - 1) - jlo) * kRecBytes;
-        const uint32_t r1 = recs + (min(p.gdiv.div(kw + 8), p.G - 1) - jlo) * kRecBytes;
-        const SlabConsts c0 = slab_consts_scaled(r0, o.zero, o.zero_shift, o.scale);
-        const SlabConsts c1 = slab_consts_scaled(r1, o.zero, o.zero_shift, o.scale);
-        if (bb == 0) dec_block<NB8, 0, true>(codes, xb, c0, c1, tot);
-        if (bb == 1) dec_block<NB8, 1, true>(codes, xb, c0, c1, tot);
-        if (bb == 2) dec_block<NB8, 2, true>(codes, xb, c0, c1, tot);
-        if (bb == 3) dec_block<NB8, 3, true>(codes, xb, c0, c1, tot);
+        const uint32_t r0 = recs + (min(p.gdiv.div(kw), G - 1) - jlo) * kRecBytes;
+        const uint32_t r1 = recs + (min(p.gdiv.div(kw + 8), G - 1) - jlo) * kRecBytes;
+        const SlabConsts c0 = slab_consts_scaled<DT>(r0, o.zero, o.zero_shift, o.scale);
+        const SlabConsts c1 = slab_consts_scaled<DT>(r1, o.zero, o.zero_shift, o.scale);
+        if (bb == 0) dec_block<NB8, 0, true, DT>(codes, xb, c0, c1, tot);
+        if (bb == 1) dec_block<NB8, 1, true, DT>(codes, xb, c0, c1, tot);
+        if (bb == 2) dec_block<NB8, 2, true, DT>(codes, xb, c0, c1, tot);
+        if (bb == 3) dec_block<NB8, 3, true, DT>(codes, xb, c0, c1, tot);
       }
     }
   }
 }
 
-__device__ __forceinline__ int dec_stage_blocks(const DecParams &p, int ks) {
-  return ks == p.KS - 1 ? p.KB - kSB * (p.KS - 1) : kSB;
+__device__ __forceinline__ int dec_stage_blocks(const DecProblem &pr, int ks) {
+  return ks == pr.KS - 1 ? pr.KB - kSB * (pr.KS - 1) : kSB;
 }
 
 // Waits with a caller-given limit; on timeout raises the CTA's abort flag and the error word.
@@ -342,40 +356,100 @@ __device__ __forceinline__ bool dec_warp_wait(uint32_t bar, uint32_t parity, boo
   return __all_sync(0xffffffffu, ok);
 }
 
-// The CTA's K range of x, stage by stage (four 64-wide K blocks of BN token rows each, 128-byte swizzle:
-// 16-byte chunk c of row n of a block at n * 128 + (c ^ (n % 8)) * 16), loaded once by the 512 consumer
-// threads with zero-filling asynchronous copies (rows >= M and k >= K read nothing and land as zeros):
-// thread `tid` copies chunk tid (and tid + 512) of each stage, then arrives on that stage's barrier once
-// its copies so far have landed.
-__device__ __forceinline__ void load_x_slice(const DecParams &p, uint32_t xbase, int kb, int nstages, int tid,
-                                             uint64_t *x_ready) {
+// A cluster's tiles in order (q, q + Q, ... over the problems' tiles one after another) and this
+// CTA's K stages [kb, ke) of each: rank k of C takes stages [k KS / C, (k + 1) KS / C) of its tile.
+struct TileWalk {
+  int T;       // global tile
+  int pi;      // its problem
+  int t;       // tile within the problem
+  int kb, ke;  // this CTA's K stages of the tile
+};
+
+__device__ __forceinline__ void walk_to(const DecParams &p, int rank, int T, TileWalk &w) {
+  w.T = T;
+  while (w.pi + 1 < p.nprob && T >= p.prob[w.pi].tile_end) ++w.pi;  // tiles only move forward
+  const DecProblem &pr = p.prob[w.pi];
+  w.t = T - pr.tile_begin;
+  w.kb = rank * pr.KS / p.C;
+  w.ke = (rank + 1) * pr.KS / p.C;
+}
+
+// The same walk, one K stage at a time (the producers' view of the CTA's stage sequence).
+struct StageWalk {
+  TileWalk w;
+  int ks;
+  __device__ __forceinline__ void init(const DecParams &p, int rank, int q) {
+    w.pi = 0;
+    walk_to(p, rank, q, w);
+    ks = w.kb;
+  }
+  __device__ __forceinline__ void advance(const DecParams &p, int rank, int n) {
+    for (int j = 0; j < n; ++j) {
+      if (++ks >= w.ke) {
+        if (w.T + p.Q >= p.tiles) {  // past the cluster's last tile: stay put (never used)
+          ks = w.ke;
+          continue;
+        }
+        walk_to(p, rank, w.T + p.Q, w);
+        ks = w.kb;
+      }
+    }
+  }
+};
+
+// The CTA's K range [kb, kb + nstages) of problem pr's x, stage by stage (four 64-wide K blocks of M
+// token rows each, 128-byte swizzle: 16-byte chunk c of row n of a block at n * 128 + (c ^ (n % 8)) * 16),
+// loaded by the 512 consumer threads with zero-filling asynchronous copies (rows >= M and k >= K read
+// nothing and land as zeros): thread `tid` copies chunk tid of each stage, then arrives on every stage
+// barrier of the slice (xslice of them) once its copies so far have landed, so that each load moves
+// every barrier by one phase.
+__device__ __forceinline__ void load_x_slice(const DecParams &p, const DecProblem &pr, uint32_t xbase, int kb,
+                                             int nstages, int tid, uint64_t *x_ready) {
   const int m = p.M;  // rows per block; 32 m <= 512 chunks per stage
   const int b = tid / (8 * m);
   const int n = (tid / 8) % m;
   const int c = tid % 8;
   const bool mine = tid < 32 * m;  // thread tid copies chunk tid of every stage
   const uint32_t dst0 = xbase + b * m * 128 + n * 128 + ((c ^ (n & 7)) << 4);
-  for (int st = 0; st < nstages; ++st) {
-    const int k = (kb + st) * kStageK + b * kTK + 8 * c;
-    if (mine) {
-      const bool valid = k < p.K;
-      const __half *src = valid ? p.x + static_cast<int64_t>(n) * p.K + k : p.x;
+  for (int st = 0; st < p.xslice; ++st) {
+    if (mine && st < nstages) {
+      const int k = (kb + st) * kStageK + b * kTK + 8 * c;
+      const bool valid = k < pr.K;
+      const uint16_t *src = valid ? pr.x + static_cast<int64_t>(n) * pr.K + k : pr.x;
       cp_async16_zfill(dst0 + st * kSB * m * 128, src, valid ? 16u : 0u);
     }
     cp_async_mbar_arrive(smem_u32(&x_ready[st]));
   }
 }
 
-template <int NB8, int MODE>
+// The stage's weight copies: its code blocks and the group records it touches.
+template <int kCodeBytes>
+__device__ __forceinline__ void issue_stage(const DecProblem &pr, const FastDiv &gdiv, int t, int ks, uint32_t stage,
+                                            uint32_t bar, uint64_t pol, bool arrive) {
+  const int nb = dec_stage_blocks(pr, ks);
+  const int k0 = ks * kStageK;
+  const int jlo = gdiv.div(k0);
+  const int nrec = gdiv.div(min(k0 + nb * kTK, pr.K) - 1) - jlo + 1;
+  const uint32_t bytes = nb * kTileBytes + nrec * kRecBytes;
+  if (arrive)
+    mbar_arrive_expect_tx(bar, bytes);
+  else
+    mbar_expect_tx(bar, bytes);
+  bulk_g2s(stage, pr.codes + (static_cast<int64_t>(t) * pr.KB + ks * kSB) * kTileBytes, nb * kTileBytes, bar, pol);
+  bulk_g2s(stage + kCodeBytes, pr.meta + (static_cast<int64_t>(t) * pr.G + jlo) * kRecBytes, nrec * kRecBytes, bar,
+           pol);
+}
+
+template <int NB8, int MODE, int DT>
 __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
-    w4a16_gemm_dec_kernel(const DecParams p) {
+    w4a16_gemm_dec_kernel(const __grid_constant__ DecParams p) {
   using Cfg = DecCfg<NB8, MODE>;
   constexpr int SMAX = Cfg::kMaxStages;
   const int S = p.S;  // ring stages (even)
-  constexpr int BN = Cfg::BN;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[SMAX];   // the stage's weights landed
-  __shared__ __align__(8) uint64_t x_ready[Cfg::kXSlice];  // x of the CTA's k-th stage of every tile landed
+  __shared__ __align__(8) uint64_t x_ready[Cfg::kXSlice];  // x of the CTA's k-th stage of the current problem landed
+  __shared__ __align__(8) uint64_t x_free;           // the 16 consumer warps are done with the loaded x
   __shared__ __align__(8) uint64_t empty_bar[SMAX];  // the 8 warps of the stage's set are done with it
   __shared__ __align__(8) uint64_t recv_bar;      // the 16 warps of the cluster whose rows this CTA sums stored them
   __shared__ __align__(8) uint64_t free_bar;      // every CTA of the cluster summed its rows of this CTA's last partials
@@ -391,12 +465,17 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
   const int C = p.C;
   const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int q = static_cast<int>(blockIdx.x) / C;
-  const int kb = rank * p.KS / C;  // this CTA's K stages of every tile: [kb, ke)
-  const int ke = (rank + 1) * p.KS / C;
-  const int per_tile = ke - kb;    // >= 1: the planner keeps C <= KS
-  const int rounds = q < p.NT ? (p.NT - 1 - q) / p.Q + 1 : 0;  // tiles q, q + Q, ...
-  const int nst = rounds * per_tile;
+  const int rounds = q < p.tiles ? (p.tiles - 1 - q) / p.Q + 1 : 0;  // tiles q, q + Q, ...
   const int rows_per = kTN / C;  // rows of each tile this CTA sums
+  int nst = 0;  // the CTA's stages over all its tiles
+  {
+    TileWalk w;
+    w.pi = 0;
+    for (int r = 0; r < rounds; ++r) {
+      walk_to(p, rank, q + r * p.Q, w);
+      nst += w.ke - w.kb;  // >= 1: the planner keeps C <= KS of every problem
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < S; ++st) {
@@ -404,6 +483,7 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
       mbar_init(smem_u32(&empty_bar[st]), Cfg::kSetWarps);
     }
     for (int st = 0; st < Cfg::kXSlice; ++st) mbar_init(smem_u32(&x_ready[st]), 32 * Cfg::kConsumers);
+    mbar_init(smem_u32(&x_free), Cfg::kConsumers);
     mbar_init(smem_u32(&recv_bar), 1);  // the reducer's arrival; the partial sums come as transaction bytes
     mbar_init(smem_u32(&free_bar), C);   // one arrival from each CTA's reducer
     abort_sh = 0;
@@ -421,46 +501,31 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
     // ---------------------------------------------------------------- producers
     const int pw = warp;
     const uint64_t pol = policy_evict_first();  // each weight byte is read once
-    int i = pw, r = 0, ks = kb + pw;
-    while (ks >= ke) {
-      ks -= per_tile;
-      ++r;
-    }
+    StageWalk sw;
+    sw.init(p, rank, q);
+    sw.advance(p, rank, pw);
+    int i = pw;
     if (p.early) {
       // the first stages' weights before the previous grid is waited for: the packed weights are
       // read-only to every kernel of the stream (the caller states this)
-      int re = r, kse = ks;
+      StageWalk se = sw;
       for (int ie = pw; ie < nst && ie < S; ie += 2) {
-        if (lane == 0) {
-          const int t = q + re * p.Q;
-          const int nb = dec_stage_blocks(p, kse);
-          const int k0 = kse * kStageK;
-          const int jlo = p.gdiv.div(k0);
-          const int nrec = p.gdiv.div(min(k0 + nb * kTK, p.K) - 1) - jlo + 1;
-          const uint32_t stage = smem_base + (ie % S) * Cfg::kStageBytes;
-          const uint32_t bar = smem_u32(&full_bar[ie % S]);
-          mbar_expect_tx(bar, nb * kTileBytes + nrec * kRecBytes);
-          bulk_g2s(stage, p.codes + (static_cast<int64_t>(t) * p.KB + kse * kSB) * kTileBytes, nb * kTileBytes, bar,
-                   pol);
-          bulk_g2s(stage + Cfg::kCodeBytes, p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes,
-                   nrec * kRecBytes, bar, pol);
-        }
-        kse += 2;
-        while (kse >= ke) {
-          kse -= per_tile;
-          ++re;
-        }
+        if (lane == 0)
+          issue_stage<Cfg::kCodeBytes>(p.prob[se.w.pi], p.gdiv, se.w.t, se.ks, smem_base + (ie % S) * Cfg::kStageBytes,
+                                       smem_u32(&full_bar[ie % S]), pol, false);
+        se.advance(p, rank, 2);
       }
       __syncwarp();
     } else if (pw == 0 && lane == 0 && nst > 0) {
       // ask L2 for the first tile's first stages while the previous grid finishes
-      const int t = q;
-      const int n0 = min(ke - kb, S);
-      const int blocks = min((kb + n0) * kSB, p.KB) - kb * kSB;
-      bulk_prefetch_l2(p.codes + (static_cast<int64_t>(t) * p.KB + kb * kSB) * kTileBytes, blocks * kTileBytes);
+      const DecProblem &pr = p.prob[sw.w.pi];
+      const int t = sw.w.t, kb = sw.w.kb;
+      const int n0 = min(sw.w.ke - kb, S);
+      const int blocks = min((kb + n0) * kSB, pr.KB) - kb * kSB;
+      bulk_prefetch_l2(pr.codes + (static_cast<int64_t>(t) * pr.KB + kb * kSB) * kTileBytes, blocks * kTileBytes);
       const int jlo = p.gdiv.div(kb * kStageK);
-      const int jhi = p.gdiv.div(min((kb + n0) * kStageK, p.K) - 1);
-      bulk_prefetch_l2(p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
+      const int jhi = p.gdiv.div(min((kb + n0) * kStageK, pr.K) - 1);
+      bulk_prefetch_l2(pr.meta + (static_cast<int64_t>(t) * pr.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
     }
     griddep_wait();  // x may be the previous grid's output
     int s = pw, ph = 0;  // slot i % S and the parity of its use i / S (S even: this warp's slots have its parity)
@@ -468,28 +533,14 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
       if (i >= S && !dec_warp_wait(smem_u32(&empty_bar[s]), ph ^ 1, false, p, abort_flag)) break;
       if (lane == 0) {
         const uint32_t bar = smem_u32(&full_bar[s]);
-        if (p.early && i < S) {
+        if (p.early && i < S)
           mbar_arrive(bar);  // the weights are on their way since before the wait
-        } else {
-          const int t = q + r * p.Q;
-          const int nb = dec_stage_blocks(p, ks);
-          const int k0 = ks * kStageK;
-          const int jlo = p.gdiv.div(k0);
-          const int nrec = p.gdiv.div(min(k0 + nb * kTK, p.K) - 1) - jlo + 1;
-          const uint32_t stage = smem_base + s * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(bar, nb * kTileBytes + nrec * kRecBytes);
-          bulk_g2s(stage, p.codes + (static_cast<int64_t>(t) * p.KB + ks * kSB) * kTileBytes, nb * kTileBytes, bar,
-                   pol);
-          bulk_g2s(stage + Cfg::kCodeBytes, p.meta + (static_cast<int64_t>(t) * p.G + jlo) * kRecBytes,
-                   nrec * kRecBytes, bar, pol);
-        }
+        else
+          issue_stage<Cfg::kCodeBytes>(p.prob[sw.w.pi], p.gdiv, sw.w.t, sw.ks, smem_base + s * Cfg::kStageBytes, bar,
+                                       pol, true);
       }
       __syncwarp();
-      ks += 2;
-      while (ks >= ke) {
-        ks -= per_tile;
-        ++r;
-      }
+      sw.advance(p, rank, 2);
       s += 2;
       if (s >= S) {
         s -= S;
@@ -533,31 +584,59 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
     const uint32_t slot = mapa_shared(slot_local, j);
     const uint32_t recv_at_j = mapa_shared(smem_u32(&recv_bar), j);
 
-    // x of the CTA's K range, once: every tile of the launch uses the same range
     griddep_wait();  // x may be the previous grid's output
-    if (rounds > 0) load_x_slice(p, x_base, kb, per_tile, cw * 32 + lane, x_ready);
     float tot[NB8][4];
     zero_acc<NB8>(tot);
     bool ok = true;
     int s = qs, ph = 0;  // slot and use parity of the set's next stage (its stages are i = qs, qs + 2, ...)
+    int ibase = 0;       // the CTA's stage index of the round's first stage
+    int xloads = 0;      // x slices loaded so far
+    uint64_t xwaited = 0;  // x stages of the current load this warp has waited for
+    const uint16_t *x_cur = nullptr;  // the loaded slice: problem x, its K and the first stage
+    int xk_cur = -1, xkb_cur = -1;
+    TileWalk w;
+    w.pi = 0;
     for (int r = 0; r < rounds && ok; ++r) {
-      // this set's stages of the round: local stage indices i = r per_tile + ... of parity qs
-      const int ibase = r * per_tile;
-      for (int i = ibase + ((qs - ibase) & 1); i < ibase + per_tile; i += 2) {
-        const int ks = kb + (i - ibase);
-        if (r == 0) {
-          ok = dec_warp_wait(smem_u32(&x_ready[ks - kb]), 0, false, p, abort_flag);
+      walk_to(p, rank, q + r * p.Q, w);
+      const DecProblem &pr = p.prob[w.pi];
+      const int per_tile = w.ke - w.kb;
+      // x of the CTA's K range of this tile, unless it is already loaded (tiles of one problem, or of
+      // problems that share x and K)
+      if (pr.x != x_cur || pr.K != xk_cur || w.kb != xkb_cur) {
+        if (xloads > 0) {
+          // every phase of the last load is complete before the next load arrives on any barrier, and
+          // every consumer warp is done with the loaded slice before it is overwritten
+          for (int st = 0; st < p.xslice && ok; ++st)
+            if (!((xwaited >> st) & 1u)) ok = dec_warp_wait(smem_u32(&x_ready[st]), (xloads - 1) & 1, false, p, abort_flag);
           if (!ok) break;
+          if (lane == 0) mbar_arrive(smem_u32(&x_free));
+          ok = dec_warp_wait(smem_u32(&x_free), (xloads - 1) & 1, false, p, abort_flag);
+          if (!ok) break;
+        }
+        load_x_slice(p, pr, x_base, w.kb, per_tile, cw * 32 + lane, x_ready);
+        ++xloads;
+        xwaited = 0;
+        x_cur = pr.x;
+        xk_cur = pr.K;
+        xkb_cur = w.kb;
+      }
+      // this set's stages of the round: local stage indices ibase .. ibase + per_tile - 1 of parity qs
+      for (int i = ibase + ((qs - ibase) & 1); i < ibase + per_tile; i += 2) {
+        const int ks = w.kb + (i - ibase);
+        if (!((xwaited >> (ks - w.kb)) & 1u)) {  // first use of this x stage by this warp since the load
+          ok = dec_warp_wait(smem_u32(&x_ready[ks - w.kb]), (xloads - 1) & 1, false, p, abort_flag);
+          if (!ok) break;
+          xwaited |= uint64_t{1} << (ks - w.kb);
         }
         ok = dec_warp_wait(smem_u32(&full_bar[s]), ph, false, p, abort_flag);
         if (!ok) break;
         const uint32_t stage = smem_base + s * Cfg::kStageBytes;
-        const uint32_t xstage = x_base + (ks - kb) * kSB * o.xblk;
-        const int nbk = dec_stage_blocks(p, ks);
+        const uint32_t xstage = x_base + (ks - w.kb) * kSB * o.xblk;
+        const int nbk = dec_stage_blocks(pr, ks);
         if (nbk == kSB)
-          dec_stage<NB8, MODE, Cfg::kCodeBytes, true>(p, stage, xstage, o, ks * kStageK, nbk, t, tot);
+          dec_stage<NB8, MODE, Cfg::kCodeBytes, true, DT>(p, pr.G, stage, xstage, o, ks * kStageK, nbk, t, tot);
         else
-          dec_stage<NB8, MODE, Cfg::kCodeBytes, false>(p, stage, xstage, o, ks * kStageK, nbk, t, tot);
+          dec_stage<NB8, MODE, Cfg::kCodeBytes, false, DT>(p, pr.G, stage, xstage, o, ks * kStageK, nbk, t, tot);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
         s += 2;
@@ -567,6 +646,7 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
         }
       }
       if (!ok) break;
+      ibase += per_tile;
       // the tile's partial sums of rows R, R + 8 go to CTA j once it has summed the previous tile's
       if (r > 0 && !dec_warp_wait(smem_u32(&free_bar), (r - 1) & 1, true, p, abort_flag)) {
         ok = false;
@@ -586,17 +666,22 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
   } else {
     // ---------------------------------------------------------------- reducer
     // sums this CTA's rows [rank rows_per, (rank + 1) rows_per) of each finished tile over the cluster's
-    // CTAs and both sets, in a fixed order, and writes y; then frees the slots of every sender
+    // CTAs and both sets, in a fixed order, and writes them through the problem's epilogue; then frees
+    // the slots of every sender
     griddep_wait();  // y may still be in use by the previous grid
     const uint32_t free_at_lane = C > 1 && lane < C ? mapa_shared(smem_u32(&free_bar), lane) : smem_u32(&free_bar);
-    // 8-byte stores of 4 consecutive outputs when they stay aligned (y itself need only be 2-byte aligned)
-    const bool vec_y = p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 7) == 0;
+    TileWalk w;
+    w.pi = 0;
     for (int r = 0; r < rounds; ++r) {
+      walk_to(p, rank, q + r * p.Q, w);
+      const DecProblem &pr = p.prob[w.pi];
+      const Epi epi = pr.epi;
       // this tile's partial sums for this CTA's rows: 2 sets x C CTAs x rows_per rows x M tokens x 4 bytes
       if (lane == 0) mbar_arrive_expect_tx(smem_u32(&recv_bar), 1024u * p.M + p.test_extra_tx);
       if (!dec_warp_wait(smem_u32(&recv_bar), r & 1, true, p, abort_flag)) break;
-      const int n0 = (q + r * p.Q) * kTN + rank * rows_per;
-      // 4 consecutive rows per lane and step: one 16-byte load per partial, one 8-byte store of y
+      const int n0 = w.t * kTN + rank * rows_per;
+      // 4 consecutive rows per lane and step: one 16-byte load per partial, one store of 4 outputs
+      // (2 for silu * up), vectorized when aligned
       const int quads = p.M * (rows_per / 4);
 #pragma unroll 2
       for (int e = lane; e < quads; e += 32) {
@@ -610,19 +695,28 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
           v.z += a.z;
           v.w += a.w;
         }
-        __half *dst = p.y + static_cast<int64_t>(tok) * p.N + n0 + lr;
-        if (vec_y && n0 + lr + 3 < p.N) {
-          const __half2 lo = __floats2half2_rn(v.x, v.y);
-          const __half2 hi = __floats2half2_rn(v.z, v.w);
-          uint2 pk;
-          pk.x = *reinterpret_cast<const uint32_t *>(&lo);
-          pk.y = *reinterpret_cast<const uint32_t *>(&hi);
-          *reinterpret_cast<uint2 *>(dst) = pk;
+        const int n = n0 + lr;
+        if (n >= pr.N) continue;
+        if (epi.kind == kEpiSiluMul) {  // rows n, n + 1: gate, up of output n / 2 (N even)
+          uint16_t *dst = pr.y + static_cast<int64_t>(tok) * epi.ld + n / 2;
+          const float h0 = silu_mul(v.x, v.y), h1 = silu_mul(v.z, v.w);
+          if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+            *reinterpret_cast<uint32_t *>(dst) = out_bits2<DT>(h0, h1);
+          } else {
+            dst[0] = out_bits<DT>(h0);
+            if (n + 3 < pr.N) dst[1] = out_bits<DT>(h1);
+          }
         } else {
-          const float vv[4] = {v.x, v.y, v.z, v.w};
+          int ld;
+          uint16_t *dst = epi_row(epi, pr.y, n, &ld) + static_cast<int64_t>(tok) * ld;
+          if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(out_bits2<DT>(v.x, v.y), out_bits2<DT>(v.z, v.w));
+          } else {
+            const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (n0 + lr + c < p.N) dst[c] = __float2half_rn(vv[c]);
+            for (int c = 0; c < 4; ++c)
+              if (n + c < pr.N) dst[c] = out_bits<DT>(vv[c]);
+          }
         }
       }
       __syncwarp();
@@ -644,7 +738,7 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
 
 // Largest number of clusters of `c` CTAs of this kernel that can be resident at once on the current
 // device (cached per device).
-template <int NB8, int MODE>
+template <int NB8, int MODE, int DT>
 int max_clusters(int c, int dev) {
   using Cfg = DecCfg<NB8, MODE>;
   static int cache[64][4] = {};
@@ -652,7 +746,7 @@ int max_clusters(int c, int dev) {
   const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lk(mu);
   if (dev >= 0 && dev < 64 && cache[dev][ci] > 0) return cache[dev][ci];
-  auto kern = w4a16_gemm_dec_kernel<NB8, MODE>;
+  auto kern = w4a16_gemm_dec_kernel<NB8, MODE, DT>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c * 64));
   cfg.blockDim = dim3(Cfg::kThreads);
@@ -673,10 +767,10 @@ int max_clusters(int c, int dev) {
   return n;
 }
 
-template <int NB8, int MODE>
+template <int NB8, int MODE, int DT>
 cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t stream) {
   using Cfg = DecCfg<NB8, MODE>;
-  auto kern = w4a16_gemm_dec_kernel<NB8, MODE>;
+  auto kern = w4a16_gemm_dec_kernel<NB8, MODE, DT>;
   static uint64_t done_mask = 0;
   static std::mutex mu;
   int dev = 0;
@@ -691,17 +785,24 @@ cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t st
     }
   }
   // choose the cluster size (CTAs splitting each tile along K) and the number of clusters: the fewest
-  // stages per CTA, then the smaller cluster
+  // stages for the busiest CTA (at most ceil(NT / Q) tiles of each problem per cluster), then the
+  // smaller cluster
+  auto fits = [&](int c) {
+    for (int i = 0; i < p.nprob; ++i)
+      if (c > p.prob[i].KS || !dec_x_fits(p.prob[i].KS, c, p.M)) return false;  // x range would not fit
+    return true;
+  };
   int C = cluster, Q = clusters;
   if (C <= 0) {
-    int best = 0x7FFFFFFF;
+    int64_t best = INT64_MAX;
     for (int c : {1, 2, 4, 8}) {
-      if (c > p.KS) break;
-      if (!dec_x_fits(p.KS, c, p.M)) continue;  // the CTA's x range would not fit
-      const int mc = max_clusters<NB8, MODE>(c, dev);
+      if (!fits(c)) continue;
+      const int mc = max_clusters<NB8, MODE, DT>(c, dev);
       if (mc < 1) continue;
-      const int qq = std::min(Q > 0 ? Q : mc, p.NT);
-      const int work = ((p.NT + qq - 1) / qq) * ((p.KS + c - 1) / c);
+      const int qq = std::min(Q > 0 ? Q : mc, p.tiles);
+      int64_t work = 0;
+      for (int i = 0; i < p.nprob; ++i)
+        work += static_cast<int64_t>((p.prob[i].NT + qq - 1) / qq) * ((p.prob[i].KS + c - 1) / c);
       if (work < best) {
         best = work;
         C = c;
@@ -709,15 +810,16 @@ cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t st
     }
     if (C <= 0) C = 1;
   }
-  if (C > p.KS || !dec_x_fits(p.KS, C, p.M)) return cudaErrorInvalidValue;
+  if (!fits(C)) return cudaErrorInvalidValue;
   if (Q <= 0) {
-    const int mc = max_clusters<NB8, MODE>(C, dev);
+    const int mc = max_clusters<NB8, MODE, DT>(C, dev);
     Q = mc > 0 ? mc : 1;
   }
-  Q = std::min(Q, p.NT);
+  Q = std::min(Q, p.tiles);
   p.C = C;
   p.Q = Q;
-  p.xslice = (p.KS + C - 1) / C;  // the longest K range of a CTA, in stages
+  p.xslice = 0;  // the longest K range of a CTA, in stages
+  for (int i = 0; i < p.nprob; ++i) p.xslice = std::max(p.xslice, (p.prob[i].KS + C - 1) / C);
   p.S = Cfg::ring_stages(p.xslice, p.M);
   if (p.S < 4) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -739,21 +841,26 @@ cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t st
   return cudaGetLastError();
 }
 
-template <int NB8>
+template <int NB8, int DT>
 cudaError_t launch_dec_nb(const DecParams &p, int clusters, int cluster, cudaStream_t stream) {
-  if (p.g % 256 == 0) return launch_dec_t<NB8, kDecG256>(p, clusters, cluster, stream);
-  if (p.g == 128) return launch_dec_t<NB8, kDecG128>(p, clusters, cluster, stream);
-  if (p.g % 64 == 0) return launch_dec_t<NB8, kDecG64>(p, clusters, cluster, stream);
-  return launch_dec_t<NB8, kDecGen>(p, clusters, cluster, stream);
+  if (p.g % 256 == 0) return launch_dec_t<NB8, kDecG256, DT>(p, clusters, cluster, stream);
+  if (p.g == 128) return launch_dec_t<NB8, kDecG128, DT>(p, clusters, cluster, stream);
+  if (p.g % 64 == 0) return launch_dec_t<NB8, kDecG64, DT>(p, clusters, cluster, stream);
+  return launch_dec_t<NB8, kDecGen, DT>(p, clusters, cluster, stream);
 }
 
 }  // namespace
 
 namespace detail {
 
-cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int clusters, int cluster, cudaStream_t stream) {
-  if (nb8 == 1) return launch_dec_nb<1>(p, clusters, cluster, stream);
-  if (nb8 == 2) return launch_dec_nb<2>(p, clusters, cluster, stream);
+cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int dtype, int clusters, int cluster, cudaStream_t stream) {
+  if (dtype == kDtypeBf16) {
+    if (nb8 == 1) return launch_dec_nb<1, kDtypeBf16>(p, clusters, cluster, stream);
+    if (nb8 == 2) return launch_dec_nb<2, kDtypeBf16>(p, clusters, cluster, stream);
+  } else {
+    if (nb8 == 1) return launch_dec_nb<1, kDtypeF16>(p, clusters, cluster, stream);
+    if (nb8 == 2) return launch_dec_nb<2, kDtypeF16>(p, clusters, cluster, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

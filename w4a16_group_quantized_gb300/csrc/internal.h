@@ -19,6 +19,11 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int kDtypeF16 = 0;
 constexpr int kDtypeBf16 = 1;
 
+// Output epilogues (W4_EPI_* of the C ABI).
+constexpr int kEpiNone = 0;
+constexpr int kEpiSiluMul = 1;
+constexpr int kEpiQkv = 2;
+
 cudaError_t launch_pack(const void *W, int64_t N, int64_t K, int32_t g, int dtype, bool symmetric, uint32_t *qw,
                         void *scales, uint32_t *zeros, cudaStream_t stream);
 
@@ -52,6 +57,7 @@ struct GemmOptions {
   bool weights_static = false;
   bool test_timeout = false;  // test only: one wait expects more than will come (runs out after wait_limit)
   uint64_t wait_limit = 0;
+  int dtype = kDtypeF16;      // x, scales and y
 };
 
 struct GemmPlan {
@@ -77,10 +83,47 @@ struct GemmPlan {
 bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOptions &opt, int num_sms,
                     GemmPlan *plan);
 
+// An output epilogue as the caller gives it (w4a16_epilogue of the C ABI).
+struct EpiSpec {
+  int kind = kEpiNone;
+  int head_dim = 0;     // kEpiQkv
+  int q_per_group = 0;  // kEpiQkv
+  void *k = nullptr;    // kEpiQkv
+  void *v = nullptr;
+};
+
+// Whether the epilogue is valid for a problem of N weight rows.
+bool epi_valid(const EpiSpec &e, int64_t N);
+
 // Launches the GEMM for a validated plan. Returns the CUDA error (cudaSuccess on success);
 // *encode_failed is set when the tensor map could not be built.
 cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y,
-                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, cudaStream_t stream,
-                        bool *encode_failed);
+                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, const EpiSpec &epi,
+                        cudaStream_t stream, bool *encode_failed);
+
+// Several independent GEMMs of the same M, g and type (w4a16_gemm_grouped).
+struct GemmProblem {
+  const void *x;
+  const void *packed;
+  void *y;
+  int64_t N, K;
+  EpiSpec epi;
+};
+
+// How a group runs: with the decode kernel, all problems in launches of up to kGroupMax problems
+// that walk their weight tiles in one persistent grid; otherwise one launch per problem.
+constexpr int kGroupMax = 16;
+struct GroupPlan {
+  bool decode;
+  int block_n;            // decode kernel: 8 or 16
+  size_t workspace_bytes;
+};
+
+bool make_group_plan(const GemmProblem *probs, int count, int64_t M, int32_t g, const GemmOptions &opt, int num_sms,
+                     GroupPlan *plan);
+
+cudaError_t launch_gemm_grouped(const GemmProblem *probs, int count, int64_t M, int32_t g, void *workspace,
+                                const GroupPlan &plan, const GemmOptions &opt, int num_sms, cudaStream_t stream,
+                                bool *encode_failed);
 
 }  // namespace w4

@@ -346,11 +346,12 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B, fp32 D,
+// Instruction descriptor of tcgen05.mma kind::f16: fp16 (or, with bf16, bf16) A and B, fp32 D,
 // both operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool bf16 = false) {
   return (1u << 4)                                  // D format: f32
-         | (0u << 7) | (0u << 10)                   // A, B format: f16
+         | ((bf16 ? 1u : 0u) << 7)                  // A format: f16 (0) or bf16 (1)
+         | ((bf16 ? 1u : 0u) << 10)                 // B format: the same
          | (0u << 15) | (0u << 16)                  // A, B K-major
          | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
@@ -379,6 +380,18 @@ __device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bsub2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bmul2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
