@@ -52,7 +52,7 @@ L2_FLUSH_BYTES = 512 << 20
 # GEMMs with M <= DOM_M (12 of the 28 launches); its roofline is reported, timed inside the step.
 DOM_M = 8
 DOM_KERNEL = "w4a16_gemm_dec_kernel"
-DOM_SOURCES = ("gemm_dec.cu", "gemm_common.cuh", "ptx.cuh")
+DOM_SOURCES = ("gemm_dec.cuh", "gemm_dec_f16.cu", "gemm_common.cuh", "ptx.cuh")
 # bf16 points (per M and decode layer) and the fused epilogues (fused qkv split by 128-wide heads; gate/up
 # rows read as interleaved gate, up for silu(gate) * up), timed beside the fp16 sweep
 BF16_MS = (1, 8, 16, 128)
@@ -798,30 +798,51 @@ def run_case(args):
 
     m_s, name = args.case.split(":", 1)
     m = int(m_s)
-    table = {L.name: L for L in workloads.DECODE_LAYERS + workloads.PREFILL_LAYERS + workloads.PARTIAL_LAYERS}
+    table = {L.name: L for L in workloads.DECODE_LAYERS + workloads.PREFILL_LAYERS + workloads.PARTIAL_LAYERS +
+             workloads.STACK_LAYER + (workloads.STACK_HEAD,)}
     L = table[name]
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    W = torch.from_numpy(workloads.weights_f16(L.n, L.k)).to(dev)
+    outl = L in workloads.PREFILL_LAYERS
+    if args.dtype == "bf16":
+        W = torch.from_numpy(workloads.weights_bf16(L.n, L.k).view(np.int16)).to(dev).view(torch.bfloat16)
+        x = torch.from_numpy(workloads.activations_bf16(m, L.k, outliers=outl).view(np.int16)).to(dev)
+        x = x.view(torch.bfloat16)
+    else:
+        W = torch.from_numpy(workloads.weights_f16(L.n, L.k)).to(dev)
+        x = torch.from_numpy(workloads.activations_f16(m, L.k, outliers=outl)).to(dev)
     qw, sc, zw = w4.w4_pack(W, L.g)
     packed = w4.w4_repack(qw, sc, zw, L.n, L.k, L.g)
     del W, qw, sc, zw
-    x = torch.from_numpy(workloads.activations_f16(m, L.k, outliers=L in workloads.PREFILL_LAYERS)).to(dev)
-    y = torch.empty((m, L.n), dtype=torch.float16, device=dev)
+    y = torch.empty((m, L.n), dtype=x.dtype, device=dev)
     ws = torch.zeros(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g), dtype=torch.uint8, device=dev)
+    if args.epilogue == "silu":
+        h = torch.empty((m, L.n // 2), dtype=x.dtype, device=dev)
+        prob = [dict(x=x, packed=packed, N=L.n, K=L.k, y=h, silu_mul=True)]
+    elif args.epilogue == "qkv":
+        outs = [torch.empty((m, L.n // 3), dtype=x.dtype, device=dev) for _ in range(3)]
+        prob = [dict(x=x, packed=packed, N=L.n, K=L.k, qkv=(128, 1), out=outs)]
+
+    def launch():
+        if args.epilogue == "none":
+            w4.w4a16_gemm(x, packed, L.n, L.k, L.g, y=y, workspace=ws)
+        else:
+            w4.w4a16_gemm_grouped(prob, L.g, workspace=ws)
+
     for _ in range(args.warmup):
-        w4.w4a16_gemm(x, packed, L.n, L.k, L.g, y=y, workspace=ws)
+        launch()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
-        w4.w4a16_gemm(x, packed, L.n, L.k, L.g, y=y, workspace=ws)
+        launch()
     e1.record()
     torch.cuda.synchronize()
     assert w4.w4_last_device_error(ws) == 0
     us = e0.elapsed_time(e1) * 1e3 / args.steps
     bn, ctas, sched = w4.w4a16_gemm_plan(m, L.n, L.k, L.g)
-    print(json.dumps({"case": args.case, "us_per_launch_eager": round(us, 3), "block_n": bn, "schedule": sched,
+    print(json.dumps({"case": args.case, "dtype": args.dtype, "epilogue": args.epilogue,
+                      "us_per_launch_eager": round(us, 3), "block_n": bn, "schedule": sched,
                       "ctas": ctas, "alg_bytes": alg_bytes(m, L.n, L.k, L.g), "flops": gemm_flops(m, L.n, L.k)}))
     return 0
 
@@ -835,6 +856,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense fp16 comparison")
     ap.add_argument("--case", default=None, help="M:layer_name - run only that GEMM (for profiling)")
+    ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16", help="--case: value type")
+    ap.add_argument("--epilogue", choices=["none", "silu", "qkv"], default="none",
+                    help="--case: output epilogue (silu(gate) * up; q/k/v split by 128-wide heads)")
     ap.add_argument("--prefill", action="store_true", help="time the prefill config instead of the decode step")
     ap.add_argument("--stack", action="store_true", help="time the 225-GEMM decode stack instead of the decode step")
     ap.add_argument("--no-prefill", action="store_true", help="leave the prefill block out of the default line")

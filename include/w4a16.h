@@ -3,23 +3,14 @@
  *
  *   y[M,N] = x[M,K] . dequant(Wq)[N,K]^T,   w[n,k] = (q[n,k] - z[n,j]) * s[n,j],  j = floor(k/g)
  *
- * x and y are fp16, row-major. Each weight is an unsigned 4-bit code q in
- * [0,15]; every (output row n, group j of g consecutive k) has an fp16 scale
- * s and a 4-bit zero z. When K is not a multiple of g the last group is
- * narrower than g and is handled as such: nothing is padded or skipped.
+ * x and y are fp16 (or bf16), row-major. Each weight is an unsigned 4-bit
+ * code q in [0,15]; every (output row n, group j of g consecutive k) has a
+ * scale s of the same 16-bit type and a 4-bit zero z. When K is not a
+ * multiple of g the last group is narrower than g and is handled as such:
+ * nothing is padded or skipped.
  *
- * Where this comes from:
- *  - fp16 activations times 4-bit weights, memory-bound at small batch and
- *    compute-bound at large batch: Marlin post ("FP16xINT4" kernel; ideal
- *    speed-up of 4x from weight bytes alone).
- *  - group-wise 4-bit weights with a group size: lmdeploy PR #202 "Blazing
- *    fast W4A16 inference" (AWQ weights, --group_size 128), torchchat issue
- *    #1362 ('linear:int4' with 'groupsize').
- *  - a last group narrower than g: torchchat issue #1362, option 2 ("groupwise
- *    GEMM with a last group that's not a full group").
- *  - converting canonical packed weights into the kernel's own layout once,
- *    offline: the converter step of lmdeploy PR #202 (deploy.py with
- *    --model_format awq).
+ * Each call's comment names the passage of the pages it follows ("Follows:");
+ * calls that are plumbing of this library (sizes, status, errors) name none.
  *
  * Conventions for every call:
  *  - Pointers named *_dev are device pointers; the caller allocates and owns
@@ -72,6 +63,12 @@ W4_API const char *w4_status_string(int status);
  * zeros_dev  out: uint32 [N, ceil(G/8)]; zero of group j = 8c + i in bits
  *            4i..4i+3 of word c of row n; padding nibbles are 0.
  *
+ * Follows: group-wise 4-bit weights with a group size -- lmdeploy PR #202
+ * "Blazing fast W4A16 inference" (AWQ weights, --group_size 128) and
+ * torchchat issue #1362 ('linear:int4' with 'groupsize'); a last group
+ * narrower than g -- torchchat issue #1362, option 2 ("groupwise GEMM with
+ * a last group that's not a full group").
+ *
  * Per (n, j), over k in [j*g, min((j+1)*g, K)), in fp64:
  *   lo = min(0, min w), hi = max(0, max w), r = hi - lo;
  *   r == 0: s = 1, z = 0, q = 0;
@@ -115,6 +112,11 @@ W4_API size_t w4_repacked_bytes(int64_t N, int64_t K, int32_t g);
  * w4_repack -- canonical packed form -> the GEMM's tile layout (a permutation
  * of codes, scales and zeros; bit-exact, deterministic).
  *
+ * Follows: converting canonical packed weights into the kernel's own layout
+ * once, offline -- the converter step of lmdeploy PR #202 (deploy.py with
+ * --model_format awq). Scales are moved as 16-bit values: fp16 and bf16
+ * scales repack alike.
+ *
  * Inputs as produced by w4_pack. `packed_dev` (out) has w4_repacked_bytes(N,K,g)
  * bytes, 16-byte aligned. Layout, with NT = ceil(N/128), KB = ceil(K/64):
  *  - code tiles: tile (t, b) of 4096 bytes at offset (t*KB + b)*4096 holds
@@ -122,7 +124,7 @@ W4_API size_t w4_repacked_bytes(int64_t N, int64_t K, int32_t g);
  *    uint32 at byte h*2048 + r*16 + 4*i (h < 2, i < 4) holds the 8 codes of
  *    row n at k = 64b + 32h + 8i + e (e < 8), code e at nibble 4*(e%2) + e/2;
  *  - group records after the tiles: record (t, j) of 320 bytes at offset
- *    NT*KB*4096 + (t*G + j)*320 holds the fp16 scale of row 128t + r at byte
+ *    NT*KB*4096 + (t*G + j)*320 holds the scale of row 128t + r at byte
  *    2r and its zero in byte 256 + r/2 (low nibble for even r);
  *  - everything at n >= N or k >= K is 0.
  */
@@ -150,11 +152,18 @@ W4_API size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t g);
  * must be a multiple of 16), g a positive multiple of 8; K % g may be
  * anything (the last group is partial).
  *
- * Numerics: each weight is dequantized once to fp16, rounded once:
- * fp16((q - z) * s) with q - z formed exactly; products are accumulated in
- * fp32 on the tensor cores (tcgen05, accumulator in tensor memory); pieces of
- * a tile cut along K are added in fp32 in K order; y is rounded to fp16
- * (nearest-even). Results are deterministic run to run on one device.
+ * Follows: fp16 activations times 4-bit weights on the tensor cores,
+ * memory-bound at small batch and compute-bound at large batch -- the Marlin
+ * post ("FP16xINT4" kernel; ideal speed-up of 4x from weight bytes alone).
+ *
+ * Numerics: q - z is formed exactly. The tensor-memory kernel (M >= 9 by
+ * default) rounds each weight once, fp16((q - z) * s), and accumulates in
+ * fp32 in tensor memory; the decode kernel (M <= 8) multiplies the exact
+ * integers q - z on the tensor cores and scales each group's fp32 partial
+ * sum by s when g is a multiple of 64 (else it rounds (q - z) * s once like
+ * the other kernel). Pieces of a tile cut along K are added in fp32 in a
+ * fixed order; y is rounded once to fp16 (nearest-even). Results are
+ * deterministic run to run on one device.
  */
 W4_API int w4a16_gemm(const void *x_dev, const void *packed_dev, int64_t M, int64_t N, int64_t K,
                int32_t g, void *y_dev, void *workspace_dev, size_t workspace_bytes, void *stream);

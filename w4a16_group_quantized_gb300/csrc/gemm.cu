@@ -1,5 +1,5 @@
 // w4a16_gemm: y[M,N] = x[M,K] . dequant(Wq)[N,K]^T on sm_103a tensor cores (M >= 9 by default; the
-// register-operand decode kernel, gemm_dec.cu, takes M <= 8).
+// register-operand decode kernel, gemm_dec.cuh, takes M <= 8).
 //
 // Output tiles are 128 (weight rows n) x BN (activation rows m) tiles of y^T
 // ("swap-AB": the weights sit on the MMA's M = 128 side, the tokens on its N
@@ -111,16 +111,28 @@ __device__ __forceinline__ void emit16(const Params &p, bool whole, int n, int m
                                        const float (&v)[16], float *piece) {
   if (whole) {
     if (p.epi.kind == kEpiSiluMul) {
-      // rows n (even lane: gate) and n + 1 (odd lane: up); the even lane writes silu(gate) * up
-      float u[16];
+      // rows n & ~1 (even lane: gate) and n | 1 (odd lane: up) of 16 tokens: the pair swaps values and
+      // splits the tokens, the even lane writes silu(gate) * up of tokens 0..7, the odd lane of 8..15
+      const bool odd = n & 1;
+      float gate[8], up[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) u[e] = __shfl_xor_sync(0xffffffffu, v[e], 1);
-      if ((n & 1) == 0 && n < p.N) {
+      for (int e = 0; e < 16; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[e], 1);
+        if (e < 8 && !odd) {
+          gate[e] = v[e];
+          up[e] = other;
+        } else if (e >= 8 && odd) {
+          gate[e - 8] = other;
+          up[e - 8] = v[e];
+        }
+      }
+      if (n < p.N) {
         uint16_t *dst = p.y + n / 2;
+        const int e0 = odd ? 8 : 0;
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (m0 + c0 + e < m_end)
-            dst[static_cast<int64_t>(m0 + c0 + e) * p.epi.ld] = out_bits<DT>(silu_mul(v[e], u[e]));
+        for (int e = 0; e < 8; ++e)
+          if (m0 + c0 + e0 + e < m_end)
+            dst[static_cast<int64_t>(m0 + c0 + e0 + e) * p.epi.ld] = out_bits<DT>(silu_mul(gate[e], up[e]));
       }
     } else if (n < p.N) {
       int ld;

@@ -74,7 +74,11 @@ __device__ __forceinline__ uint16_t *epi_row(const Epi &e, uint16_t *y, int n, i
   return (hh == e.r ? e.k : e.v) + grp * e.d + c;
 }
 
-__device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + expf(-gate)) * up; }
+// silu(gate) * up in fp32 with the fast exponential and division (relative error ~1e-6, far below the
+// output's rounding); a very negative gate gives 1 + e^-gate = inf and a (signed) zero.
+__device__ __forceinline__ float silu_mul(float gate, float up) {
+  return __fdividef(gate, 1.0f + __expf(-gate)) * up;
+}
 
 // Work decomposition. A unit is one K stage of one output tile (128 weight rows, or 256 for two-tile
 // units, x BN activation rows); units are numbered tile-major: u = tile * KS + ks, tile = t * MT + mt.
@@ -396,7 +400,7 @@ cudaError_t launch_programmatic(Kernel kern, int ctas, int threads, int smem_byt
   return cudaGetLastError();
 }
 
-// Parameters of the cluster decode kernel (gemm_dec.cu): M <= 8 * nb8 tokens, one token tile, and one
+// Parameters of the cluster decode kernel (gemm_dec.cuh): M <= 8 * nb8 tokens, one token tile, and one
 // or more independent problems (same M, g and type) whose weight tiles the launch walks in order.
 constexpr int kDecMaxProblems = kGroupMax;
 
@@ -409,6 +413,7 @@ struct DecProblem {
   int N, K, G, NT, KB, KS;
   int tile_begin, tile_end;  // the problem's tiles in the launch's tile sequence
 };
+static_assert(sizeof(DecProblem) % 4 == 0, "the kernel copies the table in 4-byte words");
 
 struct DecParams {
   DecProblem prob[kDecMaxProblems];
@@ -427,8 +432,14 @@ struct DecParams {
 };
 
 // Launches the decode kernel with `clusters` clusters of `cluster` CTAs (0: chosen for the layer), for
-// fp16 or bf16 (dtype) activations, scales and outputs.
-cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int dtype, int clusters, int cluster, cudaStream_t stream);
+// fp16 or bf16 (dtype) activations, scales and outputs (gemm_dec_f16.cu, gemm_dec_bf16.cu).
+cudaError_t launch_gemm_dec_f16(const DecParams &p, int nb8, int clusters, int cluster, cudaStream_t stream);
+cudaError_t launch_gemm_dec_bf16(const DecParams &p, int nb8, int clusters, int cluster, cudaStream_t stream);
+inline cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int dtype, int clusters, int cluster,
+                                   cudaStream_t stream) {
+  return dtype == kDtypeBf16 ? launch_gemm_dec_bf16(p, nb8, clusters, cluster, stream)
+                             : launch_gemm_dec_f16(p, nb8, clusters, cluster, stream);
+}
 
 }  // namespace detail
 }  // namespace w4

@@ -37,6 +37,8 @@
 //
 // This is Marlin's register-level dequant into MMA fragments (Marlin post) carried to sm_103a, with
 // TMA/mbarrier staging, clusters and distributed shared memory for the split along K.
+#pragma once
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -329,10 +331,6 @@ __device__ __forceinline__ void dec_stage(const DecParams &p, int G, uint32_t st
   }
 }
 
-__device__ __forceinline__ int dec_stage_blocks(const DecProblem &pr, int ks) {
-  return ks == pr.KS - 1 ? pr.KB - kSB * (pr.KS - 1) : kSB;
-}
-
 // Waits with a caller-given limit; on timeout raises the CTA's abort flag and the error word.
 __device__ __forceinline__ bool dec_wait(uint32_t bar, uint32_t parity, bool cluster_scope, const DecParams &p,
                                          volatile uint32_t *abort_flag) {
@@ -365,8 +363,30 @@ struct TileWalk {
   int kb, ke;  // this CTA's K stages of the tile
 };
 
+// Problem pi of the launch. A launch of one problem (MULTI false) reads entry 0 at a fixed place.
+template <bool MULTI>
+__device__ __forceinline__ const DecProblem &prob_at(const DecParams &p, int pi) {
+  return p.prob[MULTI ? pi : 0];
+}
+
+__device__ __forceinline__ TileWalk walk_start() {
+  TileWalk w;
+  w.T = w.t = w.pi = 0;
+  w.kb = w.ke = -1;
+  return w;
+}
+
+template <bool MULTI>
 __device__ __forceinline__ void walk_to(const DecParams &p, int rank, int T, TileWalk &w) {
   w.T = T;
+  if (!MULTI) {  // one problem: the K range is the same for every tile
+    w.t = T;
+    if (w.ke < 0) {
+      w.kb = rank * p.prob[0].KS / p.C;
+      w.ke = (rank + 1) * p.prob[0].KS / p.C;
+    }
+    return;
+  }
   while (w.pi + 1 < p.nprob && T >= p.prob[w.pi].tile_end) ++w.pi;  // tiles only move forward
   const DecProblem &pr = p.prob[w.pi];
   w.t = T - pr.tile_begin;
@@ -374,23 +394,53 @@ __device__ __forceinline__ void walk_to(const DecParams &p, int rank, int T, Til
   w.ke = (rank + 1) * pr.KS / p.C;
 }
 
+// Where a tile's weight stages come from, kept in registers while the producers walk the tile.
+struct StageSrc {
+  const uint8_t *codes;  // the tile's first code block
+  const uint8_t *meta;   // the tile's first group record
+  int K, KS, nb_last;    // the problem's K, K stages and blocks in its last stage
+};
+
 // The same walk, one K stage at a time (the producers' view of the CTA's stage sequence).
+template <bool MULTI>
 struct StageWalk {
   TileWalk w;
+  StageSrc src;
   int ks;
+  __device__ __forceinline__ void load_src(const DecParams &p) {
+    const DecProblem &pr = prob_at<MULTI>(p, w.pi);
+    src.codes = pr.codes + static_cast<int64_t>(w.t) * pr.KB * kTileBytes;
+    src.meta = pr.meta + static_cast<int64_t>(w.t) * pr.G * kRecBytes;
+    src.K = pr.K;
+    src.KS = pr.KS;
+    src.nb_last = pr.KB - kSB * (pr.KS - 1);
+  }
   __device__ __forceinline__ void init(const DecParams &p, int rank, int q) {
-    w.pi = 0;
-    walk_to(p, rank, q, w);
+    w = walk_start();
+    walk_to<MULTI>(p, rank, q, w);
+    load_src(p);
     ks = w.kb;
   }
   __device__ __forceinline__ void advance(const DecParams &p, int rank, int n) {
+    if (!MULTI) {  // the next tile of the one problem: Q tiles further on
+      ks += n;
+      while (ks >= w.ke) {
+        ks -= w.ke - w.kb;
+        w.T += p.Q;
+        w.t += p.Q;
+        src.codes += static_cast<int64_t>(p.Q) * p.prob[0].KB * kTileBytes;
+        src.meta += static_cast<int64_t>(p.Q) * p.prob[0].G * kRecBytes;
+      }
+      return;
+    }
     for (int j = 0; j < n; ++j) {
       if (++ks >= w.ke) {
         if (w.T + p.Q >= p.tiles) {  // past the cluster's last tile: stay put (never used)
           ks = w.ke;
           continue;
         }
-        walk_to(p, rank, w.T + p.Q, w);
+        walk_to<MULTI>(p, rank, w.T + p.Q, w);
+        load_src(p);
         ks = w.kb;
       }
     }
@@ -424,23 +474,22 @@ __device__ __forceinline__ void load_x_slice(const DecParams &p, const DecProble
 
 // The stage's weight copies: its code blocks and the group records it touches.
 template <int kCodeBytes>
-__device__ __forceinline__ void issue_stage(const DecProblem &pr, const FastDiv &gdiv, int t, int ks, uint32_t stage,
+__device__ __forceinline__ void issue_stage(const StageSrc &src, const FastDiv &gdiv, int ks, uint32_t stage,
                                             uint32_t bar, uint64_t pol, bool arrive) {
-  const int nb = dec_stage_blocks(pr, ks);
+  const int nb = ks == src.KS - 1 ? src.nb_last : kSB;
   const int k0 = ks * kStageK;
   const int jlo = gdiv.div(k0);
-  const int nrec = gdiv.div(min(k0 + nb * kTK, pr.K) - 1) - jlo + 1;
+  const int nrec = gdiv.div(min(k0 + nb * kTK, src.K) - 1) - jlo + 1;
   const uint32_t bytes = nb * kTileBytes + nrec * kRecBytes;
   if (arrive)
     mbar_arrive_expect_tx(bar, bytes);
   else
     mbar_expect_tx(bar, bytes);
-  bulk_g2s(stage, pr.codes + (static_cast<int64_t>(t) * pr.KB + ks * kSB) * kTileBytes, nb * kTileBytes, bar, pol);
-  bulk_g2s(stage + kCodeBytes, pr.meta + (static_cast<int64_t>(t) * pr.G + jlo) * kRecBytes, nrec * kRecBytes, bar,
-           pol);
+  bulk_g2s(stage, src.codes + static_cast<int64_t>(ks) * kSB * kTileBytes, nb * kTileBytes, bar, pol);
+  bulk_g2s(stage + kCodeBytes, src.meta + static_cast<int64_t>(jlo) * kRecBytes, nrec * kRecBytes, bar, pol);
 }
 
-template <int NB8, int MODE, int DT>
+template <int NB8, int MODE, int DT, bool MULTI>
 __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
     w4a16_gemm_dec_kernel(const __grid_constant__ DecParams p) {
   using Cfg = DecCfg<NB8, MODE>;
@@ -467,15 +516,6 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
   const int q = static_cast<int>(blockIdx.x) / C;
   const int rounds = q < p.tiles ? (p.tiles - 1 - q) / p.Q + 1 : 0;  // tiles q, q + Q, ...
   const int rows_per = kTN / C;  // rows of each tile this CTA sums
-  int nst = 0;  // the CTA's stages over all its tiles
-  {
-    TileWalk w;
-    w.pi = 0;
-    for (int r = 0; r < rounds; ++r) {
-      walk_to(p, rank, q + r * p.Q, w);
-      nst += w.ke - w.kb;  // >= 1: the planner keeps C <= KS of every problem
-    }
-  }
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < S; ++st) {
@@ -500,25 +540,33 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
   if (warp < Cfg::kProducers) {
     // ---------------------------------------------------------------- producers
     const int pw = warp;
+    int nst = 0;  // the CTA's stages over all its tiles
+    {
+      TileWalk w = walk_start();
+      for (int r = 0; r < rounds; ++r) {
+        walk_to<MULTI>(p, rank, q + r * p.Q, w);
+        nst += w.ke - w.kb;  // >= 1: the planner keeps C <= KS of every problem
+      }
+    }
     const uint64_t pol = policy_evict_first();  // each weight byte is read once
-    StageWalk sw;
+    StageWalk<MULTI> sw;
     sw.init(p, rank, q);
     sw.advance(p, rank, pw);
     int i = pw;
     if (p.early) {
       // the first stages' weights before the previous grid is waited for: the packed weights are
       // read-only to every kernel of the stream (the caller states this)
-      StageWalk se = sw;
+      StageWalk<MULTI> se = sw;
       for (int ie = pw; ie < nst && ie < S; ie += 2) {
         if (lane == 0)
-          issue_stage<Cfg::kCodeBytes>(p.prob[se.w.pi], p.gdiv, se.w.t, se.ks, smem_base + (ie % S) * Cfg::kStageBytes,
+          issue_stage<Cfg::kCodeBytes>(se.src, p.gdiv, se.ks, smem_base + (ie % S) * Cfg::kStageBytes,
                                        smem_u32(&full_bar[ie % S]), pol, false);
         se.advance(p, rank, 2);
       }
       __syncwarp();
     } else if (pw == 0 && lane == 0 && nst > 0) {
       // ask L2 for the first tile's first stages while the previous grid finishes
-      const DecProblem &pr = p.prob[sw.w.pi];
+      const DecProblem &pr = prob_at<MULTI>(p, sw.w.pi);
       const int t = sw.w.t, kb = sw.w.kb;
       const int n0 = min(sw.w.ke - kb, S);
       const int blocks = min((kb + n0) * kSB, pr.KB) - kb * kSB;
@@ -536,8 +584,7 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
         if (p.early && i < S)
           mbar_arrive(bar);  // the weights are on their way since before the wait
         else
-          issue_stage<Cfg::kCodeBytes>(p.prob[sw.w.pi], p.gdiv, sw.w.t, sw.ks, smem_base + s * Cfg::kStageBytes, bar,
-                                       pol, true);
+          issue_stage<Cfg::kCodeBytes>(sw.src, p.gdiv, sw.ks, smem_base + s * Cfg::kStageBytes, bar, pol, true);
       }
       __syncwarp();
       sw.advance(p, rank, 2);
@@ -591,23 +638,32 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
     int s = qs, ph = 0;  // slot and use parity of the set's next stage (its stages are i = qs, qs + 2, ...)
     int ibase = 0;       // the CTA's stage index of the round's first stage
     int xloads = 0;      // x slices loaded so far
-    uint64_t xwaited = 0;  // x stages of the current load this warp has waited for
+    int r_load = 0;      // the round of the last load
     const uint16_t *x_cur = nullptr;  // the loaded slice: problem x, its K and the first stage
     int xk_cur = -1, xkb_cur = -1;
-    TileWalk w;
-    w.pi = 0;
+    TileWalk w = walk_start();
+    if (!MULTI) {  // one problem: the same K range of x for every tile, loaded once
+      walk_to<MULTI>(p, rank, q, w);
+      if (rounds > 0) {
+        load_x_slice(p, p.prob[0], x_base, w.kb, w.ke - w.kb, cw * 32 + lane, x_ready);
+        xloads = 1;
+      }
+    }
     for (int r = 0; r < rounds && ok; ++r) {
-      walk_to(p, rank, q + r * p.Q, w);
-      const DecProblem &pr = p.prob[w.pi];
+      walk_to<MULTI>(p, rank, q + r * p.Q, w);
+      const DecProblem &pr = prob_at<MULTI>(p, w.pi);
       const int per_tile = w.ke - w.kb;
+      const int G = pr.G;
+      const int ks_short = pr.KB % kSB ? pr.KS - 1 : -1;  // the problem's short last stage, if any
+      const int nb_short = pr.KB - kSB * (pr.KS - 1);
       // x of the CTA's K range of this tile, unless it is already loaded (tiles of one problem, or of
       // problems that share x and K)
-      if (pr.x != x_cur || pr.K != xk_cur || w.kb != xkb_cur) {
+      if (MULTI && (pr.x != x_cur || pr.K != xk_cur || w.kb != xkb_cur)) {
         if (xloads > 0) {
           // every phase of the last load is complete before the next load arrives on any barrier, and
           // every consumer warp is done with the loaded slice before it is overwritten
           for (int st = 0; st < p.xslice && ok; ++st)
-            if (!((xwaited >> st) & 1u)) ok = dec_warp_wait(smem_u32(&x_ready[st]), (xloads - 1) & 1, false, p, abort_flag);
+            ok = dec_warp_wait(smem_u32(&x_ready[st]), (xloads - 1) & 1, false, p, abort_flag);
           if (!ok) break;
           if (lane == 0) mbar_arrive(smem_u32(&x_free));
           ok = dec_warp_wait(smem_u32(&x_free), (xloads - 1) & 1, false, p, abort_flag);
@@ -615,28 +671,31 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
         }
         load_x_slice(p, pr, x_base, w.kb, per_tile, cw * 32 + lane, x_ready);
         ++xloads;
-        xwaited = 0;
+        r_load = r;
         x_cur = pr.x;
         xk_cur = pr.K;
         xkb_cur = w.kb;
       }
+      // a warp meets each x stage of a load first in one of the two rounds after it (its set's stage
+      // parity flips between rounds when per_tile is odd and repeats after that)
+      const bool xchk = r - r_load < 2;
+      const uint32_t xpar = (xloads - 1) & 1;
       // this set's stages of the round: local stage indices ibase .. ibase + per_tile - 1 of parity qs
       for (int i = ibase + ((qs - ibase) & 1); i < ibase + per_tile; i += 2) {
-        const int ks = w.kb + (i - ibase);
-        if (!((xwaited >> (ks - w.kb)) & 1u)) {  // first use of this x stage by this warp since the load
-          ok = dec_warp_wait(smem_u32(&x_ready[ks - w.kb]), (xloads - 1) & 1, false, p, abort_flag);
+        const int st = i - ibase;  // the stage's place in the CTA's K range (its x slot)
+        if (xchk) {
+          ok = dec_warp_wait(smem_u32(&x_ready[st]), xpar, false, p, abort_flag);
           if (!ok) break;
-          xwaited |= uint64_t{1} << (ks - w.kb);
         }
         ok = dec_warp_wait(smem_u32(&full_bar[s]), ph, false, p, abort_flag);
         if (!ok) break;
         const uint32_t stage = smem_base + s * Cfg::kStageBytes;
-        const uint32_t xstage = x_base + (ks - w.kb) * kSB * o.xblk;
-        const int nbk = dec_stage_blocks(pr, ks);
-        if (nbk == kSB)
-          dec_stage<NB8, MODE, Cfg::kCodeBytes, true, DT>(p, pr.G, stage, xstage, o, ks * kStageK, nbk, t, tot);
+        const uint32_t xstage = x_base + st * kSB * o.xblk;
+        const int ks = w.kb + st;
+        if (ks != ks_short)
+          dec_stage<NB8, MODE, Cfg::kCodeBytes, true, DT>(p, G, stage, xstage, o, ks * kStageK, kSB, t, tot);
         else
-          dec_stage<NB8, MODE, Cfg::kCodeBytes, false, DT>(p, pr.G, stage, xstage, o, ks * kStageK, nbk, t, tot);
+          dec_stage<NB8, MODE, Cfg::kCodeBytes, false, DT>(p, G, stage, xstage, o, ks * kStageK, nb_short, t, tot);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
         s += 2;
@@ -670,11 +729,10 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
     // the slots of every sender
     griddep_wait();  // y may still be in use by the previous grid
     const uint32_t free_at_lane = C > 1 && lane < C ? mapa_shared(smem_u32(&free_bar), lane) : smem_u32(&free_bar);
-    TileWalk w;
-    w.pi = 0;
+    TileWalk w = walk_start();
     for (int r = 0; r < rounds; ++r) {
-      walk_to(p, rank, q + r * p.Q, w);
-      const DecProblem &pr = p.prob[w.pi];
+      walk_to<MULTI>(p, rank, q + r * p.Q, w);
+      const DecProblem &pr = prob_at<MULTI>(p, w.pi);
       const Epi epi = pr.epi;
       // this tile's partial sums for this CTA's rows: 2 sets x C CTAs x rows_per rows x M tokens x 4 bytes
       if (lane == 0) mbar_arrive_expect_tx(smem_u32(&recv_bar), 1024u * p.M + p.test_extra_tx);
@@ -683,39 +741,65 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
       // 4 consecutive rows per lane and step: one 16-byte load per partial, one store of 4 outputs
       // (2 for silu * up), vectorized when aligned
       const int quads = p.M * (rows_per / 4);
+      if (epi.kind == kEpiNone) {
+        const bool vec_y = pr.N % 4 == 0 && (reinterpret_cast<uintptr_t>(pr.y) & 7) == 0;
 #pragma unroll 2
-      for (int e = lane; e < quads; e += 32) {
-        const int tok = e / (rows_per / 4);
-        const int lr = 4 * (e - tok * (rows_per / 4));
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < 2 * C; ++k) {  // senders by rank, set 0 then set 1 of each: a fixed order
-          const float4 a = lds128f(red_base + ((k * p.M + tok) * rows_per + lr) * 4);
-          v.x += a.x;
-          v.y += a.y;
-          v.z += a.z;
-          v.w += a.w;
-        }
-        const int n = n0 + lr;
-        if (n >= pr.N) continue;
-        if (epi.kind == kEpiSiluMul) {  // rows n, n + 1: gate, up of output n / 2 (N even)
-          uint16_t *dst = pr.y + static_cast<int64_t>(tok) * epi.ld + n / 2;
-          const float h0 = silu_mul(v.x, v.y), h1 = silu_mul(v.z, v.w);
-          if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
-            *reinterpret_cast<uint32_t *>(dst) = out_bits2<DT>(h0, h1);
-          } else {
-            dst[0] = out_bits<DT>(h0);
-            if (n + 3 < pr.N) dst[1] = out_bits<DT>(h1);
+        for (int e = lane; e < quads; e += 32) {
+          const int tok = e / (rows_per / 4);
+          const int lr = 4 * (e - tok * (rows_per / 4));
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < 2 * C; ++k) {  // senders by rank, set 0 then set 1 of each: a fixed order
+            const float4 a = lds128f(red_base + ((k * p.M + tok) * rows_per + lr) * 4);
+            v.x += a.x;
+            v.y += a.y;
+            v.z += a.z;
+            v.w += a.w;
           }
-        } else {
-          int ld;
-          uint16_t *dst = epi_row(epi, pr.y, n, &ld) + static_cast<int64_t>(tok) * ld;
-          if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+          uint16_t *dst = pr.y + static_cast<int64_t>(tok) * pr.N + n0 + lr;
+          if (vec_y && n0 + lr + 3 < pr.N) {
             *reinterpret_cast<uint2 *>(dst) = make_uint2(out_bits2<DT>(v.x, v.y), out_bits2<DT>(v.z, v.w));
           } else {
             const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              if (n + c < pr.N) dst[c] = out_bits<DT>(vv[c]);
+              if (n0 + lr + c < pr.N) dst[c] = out_bits<DT>(vv[c]);
+          }
+        }
+      } else {
+#pragma unroll 2
+        for (int e = lane; e < quads; e += 32) {
+          const int tok = e / (rows_per / 4);
+          const int lr = 4 * (e - tok * (rows_per / 4));
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < 2 * C; ++k) {  // senders by rank, set 0 then set 1 of each: a fixed order
+            const float4 a = lds128f(red_base + ((k * p.M + tok) * rows_per + lr) * 4);
+            v.x += a.x;
+            v.y += a.y;
+            v.z += a.z;
+            v.w += a.w;
+          }
+          const int n = n0 + lr;
+          if (n >= pr.N) continue;
+          if (epi.kind == kEpiSiluMul) {  // rows n, n + 1: gate, up of output n / 2 (N even)
+            uint16_t *dst = pr.y + static_cast<int64_t>(tok) * epi.ld + n / 2;
+            const float h0 = silu_mul(v.x, v.y), h1 = silu_mul(v.z, v.w);
+            if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+              *reinterpret_cast<uint32_t *>(dst) = out_bits2<DT>(h0, h1);
+            } else {
+              dst[0] = out_bits<DT>(h0);
+              if (n + 3 < pr.N) dst[1] = out_bits<DT>(h1);
+            }
+          } else {
+            int ld;
+            uint16_t *dst = epi_row(epi, pr.y, n, &ld) + static_cast<int64_t>(tok) * ld;
+            if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+              *reinterpret_cast<uint2 *>(dst) = make_uint2(out_bits2<DT>(v.x, v.y), out_bits2<DT>(v.z, v.w));
+            } else {
+              const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                if (n + c < pr.N) dst[c] = out_bits<DT>(vv[c]);
+            }
           }
         }
       }
@@ -738,7 +822,7 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
 
 // Largest number of clusters of `c` CTAs of this kernel that can be resident at once on the current
 // device (cached per device).
-template <int NB8, int MODE, int DT>
+template <int NB8, int MODE, int DT, bool MULTI>
 int max_clusters(int c, int dev) {
   using Cfg = DecCfg<NB8, MODE>;
   static int cache[64][4] = {};
@@ -746,7 +830,7 @@ int max_clusters(int c, int dev) {
   const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lk(mu);
   if (dev >= 0 && dev < 64 && cache[dev][ci] > 0) return cache[dev][ci];
-  auto kern = w4a16_gemm_dec_kernel<NB8, MODE, DT>;
+  auto kern = w4a16_gemm_dec_kernel<NB8, MODE, DT, MULTI>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c * 64));
   cfg.blockDim = dim3(Cfg::kThreads);
@@ -767,10 +851,10 @@ int max_clusters(int c, int dev) {
   return n;
 }
 
-template <int NB8, int MODE, int DT>
+template <int NB8, int MODE, int DT, bool MULTI>
 cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t stream) {
   using Cfg = DecCfg<NB8, MODE>;
-  auto kern = w4a16_gemm_dec_kernel<NB8, MODE, DT>;
+  auto kern = w4a16_gemm_dec_kernel<NB8, MODE, DT, MULTI>;
   static uint64_t done_mask = 0;
   static std::mutex mu;
   int dev = 0;
@@ -797,7 +881,7 @@ cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t st
     int64_t best = INT64_MAX;
     for (int c : {1, 2, 4, 8}) {
       if (!fits(c)) continue;
-      const int mc = max_clusters<NB8, MODE, DT>(c, dev);
+      const int mc = max_clusters<NB8, MODE, DT, MULTI>(c, dev);
       if (mc < 1) continue;
       const int qq = std::min(Q > 0 ? Q : mc, p.tiles);
       int64_t work = 0;
@@ -812,7 +896,7 @@ cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t st
   }
   if (!fits(C)) return cudaErrorInvalidValue;
   if (Q <= 0) {
-    const int mc = max_clusters<NB8, MODE, DT>(C, dev);
+    const int mc = max_clusters<NB8, MODE, DT, MULTI>(C, dev);
     Q = mc > 0 ? mc : 1;
   }
   Q = std::min(Q, p.tiles);
@@ -841,28 +925,26 @@ cudaError_t launch_dec_t(DecParams p, int clusters, int cluster, cudaStream_t st
   return cudaGetLastError();
 }
 
-template <int NB8, int DT>
+template <int NB8, int DT, bool MULTI>
 cudaError_t launch_dec_nb(const DecParams &p, int clusters, int cluster, cudaStream_t stream) {
-  if (p.g % 256 == 0) return launch_dec_t<NB8, kDecG256, DT>(p, clusters, cluster, stream);
-  if (p.g == 128) return launch_dec_t<NB8, kDecG128, DT>(p, clusters, cluster, stream);
-  if (p.g % 64 == 0) return launch_dec_t<NB8, kDecG64, DT>(p, clusters, cluster, stream);
-  return launch_dec_t<NB8, kDecGen, DT>(p, clusters, cluster, stream);
+  if (p.g % 256 == 0) return launch_dec_t<NB8, kDecG256, DT, MULTI>(p, clusters, cluster, stream);
+  if (p.g == 128) return launch_dec_t<NB8, kDecG128, DT, MULTI>(p, clusters, cluster, stream);
+  if (p.g % 64 == 0) return launch_dec_t<NB8, kDecG64, DT, MULTI>(p, clusters, cluster, stream);
+  return launch_dec_t<NB8, kDecGen, DT, MULTI>(p, clusters, cluster, stream);
 }
 
-}  // namespace
-
-namespace detail {
-
-cudaError_t launch_gemm_dec(const DecParams &p, int nb8, int dtype, int clusters, int cluster, cudaStream_t stream) {
-  if (dtype == kDtypeBf16) {
-    if (nb8 == 1) return launch_dec_nb<1, kDtypeBf16>(p, clusters, cluster, stream);
-    if (nb8 == 2) return launch_dec_nb<2, kDtypeBf16>(p, clusters, cluster, stream);
-  } else {
-    if (nb8 == 1) return launch_dec_nb<1, kDtypeF16>(p, clusters, cluster, stream);
-    if (nb8 == 2) return launch_dec_nb<2, kDtypeF16>(p, clusters, cluster, stream);
-  }
+// The decode kernel for value type DT: tokens per tile (nb8 x 8) and one or several problems.
+template <int DT>
+cudaError_t launch_dec_dt(const DecParams &p, int nb8, int clusters, int cluster, cudaStream_t stream) {
+  const bool multi = p.nprob > 1;
+  if (nb8 == 1)
+    return multi ? launch_dec_nb<1, DT, true>(p, clusters, cluster, stream)
+                 : launch_dec_nb<1, DT, false>(p, clusters, cluster, stream);
+  if (nb8 == 2)
+    return multi ? launch_dec_nb<2, DT, true>(p, clusters, cluster, stream)
+                 : launch_dec_nb<2, DT, false>(p, clusters, cluster, stream);
   return cudaErrorInvalidValue;
 }
 
-}  // namespace detail
+}  // namespace
 }  // namespace w4

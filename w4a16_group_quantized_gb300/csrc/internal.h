@@ -30,7 +30,7 @@ cudaError_t launch_pack(const void *W, int64_t N, int64_t K, int32_t g, int dtyp
 cudaError_t launch_repack(const uint32_t *qw, const void *scales, const uint32_t *zeros, int64_t N, int64_t K,
                           int32_t g, void *packed, cudaStream_t stream);
 
-// Which GEMM kernel runs: the register-operand decode kernel (M <= 16, gemm_dec.cu) or the
+// Which GEMM kernel runs: the register-operand decode kernel (M <= 16, gemm_dec.cuh) or the
 // tensor-memory kernel (gemm.cu).
 constexpr int kKernelAuto = 0;
 constexpr int kKernelDecode = 1;
