@@ -303,8 +303,7 @@ def run_gpu(args):
         for m, L in sweep():
             c = copies[L.name]
             if part is None or (m <= DOM_M) == (part == 0):
-                w4.w4a16_gemm(xs[m][L.k], c[use[L.name] % 3], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws,
-                              weights_static=True)
+                w4.w4a16_gemm(xs[m][L.k], c[use[L.name] % 3], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
             use[L.name] += 1
 
     # warm-up launches outside capture (per-device kernel attributes), then capture the step
@@ -372,8 +371,7 @@ def run_gpu(args):
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=stream):
             for i in range(R):
-                w4.w4a16_gemm(xs[m][L.k], c[i], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws,
-                              weights_static=True)
+                w4.w4a16_gemm(xs[m][L.k], c[i], L.n, L.k, L.g, y=ys[(m, L.name)], workspace=ws)
         with torch.cuda.stream(stream):
             g2.replay()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -449,8 +447,7 @@ def run_gpu(args):
             if kind == "qkv":
                 outs = [torch.empty((m, L.n // 3), dtype=torch.float16, device=dev) for _ in range(3)]
                 fused = [lambda cc=cc: w4.w4a16_gemm_grouped(
-                    [dict(x=x, packed=cc, N=L.n, K=L.k, qkv=(128, 1), out=outs)], L.g, workspace=ws,
-                    flags=w4.FLAG_WEIGHTS_STATIC) for cc in c]
+                    [dict(x=x, packed=cc, N=L.n, K=L.k, qkv=(128, 1), out=outs)], L.g, workspace=ws) for cc in c]
 
                 def after(y=y, outs=outs, m=m):
                     yv = y.view(m, L.n // 384, 3, 128)
@@ -459,13 +456,12 @@ def run_gpu(args):
             else:
                 h = torch.empty((m, L.n // 2), dtype=torch.float16, device=dev)
                 fused = [lambda cc=cc: w4.w4a16_gemm_grouped(
-                    [dict(x=x, packed=cc, N=L.n, K=L.k, y=h, silu_mul=True)], L.g, workspace=ws,
-                    flags=w4.FLAG_WEIGHTS_STATIC) for cc in c]
+                    [dict(x=x, packed=cc, N=L.n, K=L.k, y=h, silu_mul=True)], L.g, workspace=ws) for cc in c]
 
                 def after(y=y, h=h):
                     torch.mul(torch.nn.functional.silu(y[:, 0::2]), y[:, 1::2], out=h)
 
-            unfused = [lambda cc=cc: (w4.w4a16_gemm(x, cc, L.n, L.k, L.g, y=y, workspace=ws, weights_static=True),
+            unfused = [lambda cc=cc: (w4.w4a16_gemm(x, cc, L.n, L.k, L.g, y=y, workspace=ws),
                                       after()) for cc in c]
             tf, tu = time_graph(fused), time_graph(unfused)
             epilogues.append({"M": m, "layer": L.name, "epilogue": "qkv split (32 heads of 128)" if kind == "qkv"
@@ -500,8 +496,7 @@ def run_gpu(args):
     def step_e2e():
         dxbuf.copy_(hxbuf, non_blocking=True)
         for m, L in sweep():
-            w4.w4a16_gemm(dxv[(m, L.k)], copies[L.name][0], L.n, L.k, L.g, y=dyv[(m, L.name)], workspace=ws,
-                          weights_static=True)
+            w4.w4a16_gemm(dxv[(m, L.k)], copies[L.name][0], L.n, L.k, L.g, y=dyv[(m, L.name)], workspace=ws)
         hybuf.copy_(dybuf, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -580,7 +575,6 @@ def run_gpu(args):
                    "l2": "flushed between timed steps (512 MB write); 3 weight copies per layer rotate within a step",
                    "timing": "step captured as two CUDA graphs (the M <= 8 GEMMs, then the rest); CUDA events "
                              "around each per replay; max over ranks",
-                   "weights": "declared static (W4_FLAG_WEIGHTS_STATIC: no kernel writes the packed weights)",
                    "parallelism": f"replicas x{world}"},
         "weight_gbs": round(wbytes_step / (ms_per_step * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(dom_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -731,7 +725,7 @@ def run_stack(args):
 
         def ours():
             for L, pk, y in zip(layers, packed, ys):
-                w4.w4a16_gemm(xs[L.k], pk, L.n, L.k, L.g, y=y, workspace=ws, weights_static=True)
+                w4.w4a16_gemm(xs[L.k], pk, L.n, L.k, L.g, y=y, workspace=ws)
 
         # the same GEMMs grouped by what a decoder step could run together: q, k, v (one x), o, gate and
         # up (one x), down, lm_head; one w4a16_gemm_grouped call each
@@ -746,7 +740,7 @@ def run_stack(args):
 
         def ours_grouped():
             for pr in gprobs:
-                w4.w4a16_gemm_grouped(pr, 128, flags=w4.FLAG_WEIGHTS_STATIC, workspace=ws)
+                w4.w4a16_gemm_grouped(pr, 128, workspace=ws)
 
         def theirs():
             for L, W, y in zip(layers, dense, ys):

@@ -517,17 +517,24 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
   const int rounds = q < p.tiles ? (p.tiles - 1 - q) / p.Q + 1 : 0;  // tiles q, q + Q, ...
   const int rows_per = kTN / C;  // rows of each tile this CTA sums
 
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < S; ++st) {
-      mbar_init(smem_u32(&full_bar[st]), 1);
-      mbar_init(smem_u32(&empty_bar[st]), Cfg::kSetWarps);
+  // the barriers, one per thread (one thread initializing them all took about a microsecond)
+  {
+    const int t = threadIdx.x;
+    bool did = true;
+    if (t < S) {
+      mbar_init(smem_u32(&full_bar[t]), 1);
+      mbar_init(smem_u32(&empty_bar[t]), Cfg::kSetWarps);
+    } else if (t >= 64 && t < 64 + p.xslice) {
+      mbar_init(smem_u32(&x_ready[t - 64]), 32 * Cfg::kConsumers);
+    } else if (t == 32) {
+      mbar_init(smem_u32(&x_free), Cfg::kConsumers);
+      mbar_init(smem_u32(&recv_bar), 1);  // the reducer's arrival; the partial sums come as transaction bytes
+      mbar_init(smem_u32(&free_bar), C);   // one arrival from each CTA's reducer
+      abort_sh = 0;
+    } else {
+      did = false;
     }
-    for (int st = 0; st < Cfg::kXSlice; ++st) mbar_init(smem_u32(&x_ready[st]), 32 * Cfg::kConsumers);
-    mbar_init(smem_u32(&x_free), Cfg::kConsumers);
-    mbar_init(smem_u32(&recv_bar), 1);  // the reducer's arrival; the partial sums come as transaction bytes
-    mbar_init(smem_u32(&free_bar), C);   // one arrival from each CTA's reducer
-    abort_sh = 0;
-    fence_mbar_init();
+    if (did) fence_mbar_init();
   }
   __syncwarp();
   // every CTA's barriers are initialized before any CTA of the cluster arrives on them remotely
