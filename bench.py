@@ -609,8 +609,8 @@ def run_gpu(args):
 def prefill_block(args, dev, gpu_id, peaks):
     """The prefill config: M in {256, 512, 1024, 4096} x the four Llama-2-70B-shaped layers (g = 128,
     1 % outlier channels x20 in the activations). Each GEMM is launched back to back over rotating
-    weight copies (more than 2.2x L2 of packed bytes, so weights come from HBM), CUDA events after
-    warm-up, beside a dense fp16 torch.matmul of the same shape; SM clocks and throttle reasons are
+    weight copies (more than 2.2x L2 of packed bytes, so weights come from HBM) inside a CUDA graph,
+    CUDA events after warm-up, beside a dense fp16 torch.matmul of the same shape; SM clocks and throttle reasons are
     sampled over the whole timed region. Weights are drawn on the device (seeded) and quantized by
     w4_pack / w4_repack. Returns the block for the JSON line."""
     import torch
@@ -623,17 +623,30 @@ def prefill_block(args, dev, gpu_id, peaks):
     gen = torch.Generator(device=dev)
     gen.manual_seed(workloads.SEED_W)
 
+    stream = torch.cuda.Stream(dev)
+
     def timed(fn, nrot):
-        for i in range(args.warmup):
-            fn(i % nrot)
-        torch.cuda.synchronize()
+        # one launch per weight copy captured back to back in a CUDA graph (the host's per-call cost
+        # would otherwise gap launches shorter than it), replayed after warm-ups
+        with torch.cuda.stream(stream):
+            for i in range(nrot):
+                fn(i)
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(nrot):
+                fn(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(reps):
-            fn(i % nrot)
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e-3 / reps
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                gr.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(stream)
+        stream.synchronize()
+        del gr
+        return e0.elapsed_time(e1) * 1e-3 / (reps * nrot)
 
     rows = []
     with ClockSampler(gpu_id) as clk:
@@ -668,8 +681,8 @@ def prefill_block(args, dev, gpu_id, peaks):
             "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst)",
             "min_tensor_frac_m_ge_512": min(r["tensor_frac"] for r in big),
             "clocks": clk.summary(),
-            "timing": f"{reps} back-to-back launches over rotating weight copies (> 2.2x L2) after "
-                      f"{args.warmup} warm-ups, CUDA events"}
+            "timing": f"one launch per weight copy (> 2.2x L2 of copies) captured back to back in a CUDA "
+                      f"graph, {reps} replays after {args.warmup} warm-up replays, CUDA events"}
 
 
 def gpu_uuid(dev):
@@ -856,7 +869,7 @@ def main():
     ap.add_argument("--prefill", action="store_true", help="time the prefill config instead of the decode step")
     ap.add_argument("--stack", action="store_true", help="time the 225-GEMM decode stack instead of the decode step")
     ap.add_argument("--no-prefill", action="store_true", help="leave the prefill block out of the default line")
-    ap.add_argument("--prefill-reps", type=int, default=6, help="timed launches per prefill GEMM")
+    ap.add_argument("--prefill-reps", type=int, default=4, help="timed graph replays per prefill GEMM")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

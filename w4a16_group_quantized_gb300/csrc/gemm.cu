@@ -791,16 +791,18 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOption
   const int64_t units = tiles * ks;
   if (tiles > 0x7FFFFFFF || units > (int64_t{1} << 40)) return false;
   int64_t P = ctas > 0 ? ctas : (num_sms > 0 ? num_sms : 148);
-  // Fewer output tiles than SMs (64- or 128-token tiles): cut each tile into about KS / 8 pieces,
-  // as many as the SMs allow, instead of spreading all stages over every SM; one piece is whole
-  // tiles. Measured on the 7B layers at M = 64..128: qkv (96 tiles) 18% faster as whole tiles,
-  // o_proj (16 stages per tile) 10-15% faster in 2 pieces, down_proj (43 stages) as fast or faster
-  // in 4 than in ~5.
+  // Fewer output tiles than SMs (64- or 128-token tiles): cut each tile into about KS / 8 pieces, as
+  // many as the SMs allow, instead of spreading all stages over every SM; one piece means whole tiles.
+  // Kept to whole tiles or tiles of at most 64 stages: long tiles gain from every SM. Measured on the
+  // 7B layers (M = 64..128: qkv 18% faster as whole tiles, o_proj 10-15% in 2 pieces, down_proj 5% in
+  // 2 pieces at M = 128) and the 70B layers (M = 256..512: o_proj 19-24% faster, down_proj 4%, qkv 4%).
   bool fewer = false;
   if (ctas == 0 && schedule == 0 && bn >= 64 && tiles < P) {
     const int64_t pieces = std::max<int64_t>(1, std::min<int64_t>((ks + 7) / 8, P / tiles));
-    P = tiles * pieces;
-    fewer = pieces == 1;
+    if (pieces == 1 || ks <= 64) {
+      P = tiles * pieces;
+      fewer = pieces == 1;
+    }
   }
   // whole-tile scheduling when every CTA gets many tiles (imbalance <= 1/8) or the tiles divide
   // evenly; otherwise stream-K over 256-wide K stages, which needs the partial-tile fixup
