@@ -472,6 +472,70 @@ __device__ __forceinline__ void load_x_slice(const DecParams &p, const DecProble
   }
 }
 
+// Reducer: quads a lane holds in registers between the sum and the store (up to 128 quads of 4 rows:
+// every cluster size at M <= 8, C >= 4 at M <= 16).
+constexpr int kRedQuads = 4;
+
+// Quad e (token e / (rows / 4), rows 4 (e % (rows / 4)) .. + 3 of the CTA's share) summed over the
+// partials of the 2 C senders (by rank, set 0 then set 1 of each: a fixed order).
+__device__ __forceinline__ float4 red_quad_sum(uint32_t red_base, int e, int M, int rows_per, int C) {
+  const int tok = e / (rows_per / 4);
+  const int lr = 4 * (e - tok * (rows_per / 4));
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < 2 * C; ++k) {
+    const float4 a = lds128f(red_base + ((k * M + tok) * rows_per + lr) * 4);
+    v.x += a.x;
+    v.y += a.y;
+    v.z += a.z;
+    v.w += a.w;
+  }
+  return v;
+}
+
+// Quad e of the tile's outputs (rows n0 + 4 (e % (rows / 4)) ..) through the problem's epilogue: one
+// store of 4 outputs (2 for silu * up), vectorized when aligned.
+template <int DT>
+__device__ __forceinline__ void red_quad_store(const DecProblem &pr, const Epi &epi, int n0, int e, int rows_per,
+                                               float4 v) {
+  const int tok = e / (rows_per / 4);
+  const int n = n0 + 4 * (e - tok * (rows_per / 4));
+  if (n >= pr.N) return;
+  if (epi.kind == kEpiSiluMul) {  // rows n, n + 1: gate, up of output n / 2 (N even)
+    uint16_t *dst = pr.y + static_cast<int64_t>(tok) * epi.ld + n / 2;
+    const float h0 = silu_mul(v.x, v.y), h1 = silu_mul(v.z, v.w);
+    if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+      *reinterpret_cast<uint32_t *>(dst) = out_bits2<DT>(h0, h1);
+    } else {
+      dst[0] = out_bits<DT>(h0);
+      if (n + 3 < pr.N) dst[1] = out_bits<DT>(h1);
+    }
+    return;
+  }
+  uint16_t *dst;
+  if (epi.kind == kEpiNone) {
+    dst = pr.y + static_cast<int64_t>(tok) * pr.N + n;
+  } else {
+    int ld;
+    dst = epi_row(epi, pr.y, n, &ld) + static_cast<int64_t>(tok) * ld;
+  }
+  if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(out_bits2<DT>(v.x, v.y), out_bits2<DT>(v.z, v.w));
+  } else {
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (n + c < pr.N) dst[c] = out_bits<DT>(vv[c]);
+  }
+}
+
+// The reducer frees the slots of the sender at `addr` (a release: the slots' reads come first).
+__device__ __forceinline__ void red_free(uint32_t addr, int C) {
+  if (C > 1)
+    mbar_arrive_cluster(addr);
+  else
+    mbar_arrive(addr);
+}
+
 // The stage's weight copies: its code blocks and the group records it touches.
 template <int kCodeBytes>
 __device__ __forceinline__ void issue_stage(const StageSrc &src, const FastDiv &gdiv, int ks, uint32_t stage,
@@ -748,20 +812,28 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
       // 4 consecutive rows per lane and step: one 16-byte load per partial, one store of 4 outputs
       // (2 for silu * up), vectorized when aligned
       const int quads = p.M * (rows_per / 4);
+      const bool more = r + 1 < rounds;
+      if (more && quads <= 32 * kRedQuads) {
+        // a later tile follows: every quad of the lane is summed into registers first, so that the
+        // release that frees the senders' slots orders only shared-memory reads, then the stores
+        float4 v[kRedQuads];
+#pragma unroll
+        for (int j = 0; j < kRedQuads; ++j)
+          if (lane + 32 * j < quads) v[j] = red_quad_sum(red_base, lane + 32 * j, p.M, rows_per, C);
+        __syncwarp();
+        if (lane < C) red_free(free_at_lane, C);
+#pragma unroll
+        for (int j = 0; j < kRedQuads; ++j)
+          if (lane + 32 * j < quads) red_quad_store<DT>(pr, epi, n0, lane + 32 * j, rows_per, v[j]);
+        continue;
+      }
       if (epi.kind == kEpiNone) {
         const bool vec_y = pr.N % 4 == 0 && (reinterpret_cast<uintptr_t>(pr.y) & 7) == 0;
 #pragma unroll 2
         for (int e = lane; e < quads; e += 32) {
           const int tok = e / (rows_per / 4);
           const int lr = 4 * (e - tok * (rows_per / 4));
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int k = 0; k < 2 * C; ++k) {  // senders by rank, set 0 then set 1 of each: a fixed order
-            const float4 a = lds128f(red_base + ((k * p.M + tok) * rows_per + lr) * 4);
-            v.x += a.x;
-            v.y += a.y;
-            v.z += a.z;
-            v.w += a.w;
-          }
+          const float4 v = red_quad_sum(red_base, e, p.M, rows_per, C);
           uint16_t *dst = pr.y + static_cast<int64_t>(tok) * pr.N + n0 + lr;
           if (vec_y && n0 + lr + 3 < pr.N) {
             *reinterpret_cast<uint2 *>(dst) = make_uint2(out_bits2<DT>(v.x, v.y), out_bits2<DT>(v.z, v.w));
@@ -774,57 +846,28 @@ __global__ void __launch_bounds__(DecCfg<NB8, MODE>::kThreads, 1)
         }
       } else {
 #pragma unroll 2
-        for (int e = lane; e < quads; e += 32) {
-          const int tok = e / (rows_per / 4);
-          const int lr = 4 * (e - tok * (rows_per / 4));
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int k = 0; k < 2 * C; ++k) {  // senders by rank, set 0 then set 1 of each: a fixed order
-            const float4 a = lds128f(red_base + ((k * p.M + tok) * rows_per + lr) * 4);
-            v.x += a.x;
-            v.y += a.y;
-            v.z += a.z;
-            v.w += a.w;
-          }
-          const int n = n0 + lr;
-          if (n >= pr.N) continue;
-          if (epi.kind == kEpiSiluMul) {  // rows n, n + 1: gate, up of output n / 2 (N even)
-            uint16_t *dst = pr.y + static_cast<int64_t>(tok) * epi.ld + n / 2;
-            const float h0 = silu_mul(v.x, v.y), h1 = silu_mul(v.z, v.w);
-            if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
-              *reinterpret_cast<uint32_t *>(dst) = out_bits2<DT>(h0, h1);
-            } else {
-              dst[0] = out_bits<DT>(h0);
-              if (n + 3 < pr.N) dst[1] = out_bits<DT>(h1);
-            }
-          } else {
-            int ld;
-            uint16_t *dst = epi_row(epi, pr.y, n, &ld) + static_cast<int64_t>(tok) * ld;
-            if (n + 3 < pr.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
-              *reinterpret_cast<uint2 *>(dst) = make_uint2(out_bits2<DT>(v.x, v.y), out_bits2<DT>(v.z, v.w));
-            } else {
-              const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                if (n + c < pr.N) dst[c] = out_bits<DT>(vv[c]);
-            }
-          }
-        }
+        for (int e = lane; e < quads; e += 32)
+          red_quad_store<DT>(pr, epi, n0, e, rows_per, red_quad_sum(red_base, e, p.M, rows_per, C));
       }
+      // the slots are freed for the next tile; after the last tile no CTA waits for that
       __syncwarp();
-      if (lane < C) {
-        if (C > 1)
-          mbar_arrive_cluster(free_at_lane);
-        else
-          mbar_arrive(free_at_lane);
-      }
+      if (lane < C && more) red_free(free_at_lane, C);
     }
   }
-  // no CTA leaves while another CTA of the cluster may still store into its shared memory
+  // no CTA leaves while another CTA of the cluster may still store into its shared memory. On the
+  // normal path every such access has completed by now: a CTA's partial sums are counted by the
+  // receiver's barrier before its reducer finishes, and every arrival on a CTA's free_bar was waited
+  // for by that CTA's consumers (the last tile's is not made), so the barrier needs no release
+  // ordering. After an abort, remote arrivals may not have been waited for: release them.
   __syncwarp();
-  if (C > 1)
-    cluster_sync_all();
-  else
+  if (C > 1) {
+    if (__shfl_sync(0xFFFFFFFFu, *abort_flag, 0))
+      cluster_sync_all();
+    else
+      cluster_sync_all_relaxed();
+  } else {
     cta_sync_all();
+  }
 }
 
 // Largest number of clusters of `c` CTAs of this kernel that can be resident at once on the current

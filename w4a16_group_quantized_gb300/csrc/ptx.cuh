@@ -176,6 +176,14 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The same barrier without release ordering on the arrival: for a barrier whose only job is to keep
+// every CTA resident until all CTAs of the cluster are done, when every access to another CTA's shared
+// memory is already known to be complete (a release arrival would first wait for this thread's
+// outstanding global stores).
+__device__ __forceinline__ void cluster_sync_all_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------- dependent launch
 
 // Programmatic dependent launch: wait until the grids this launch depends on have completed and
