@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
   __shared__ __align__(8) uint64_t dfull_bar[C::kDBufs];
   __shared__ __align__(8) uint64_t dempty_bar[C::kDBufs];
   __shared__ __align__(8) uint64_t drain_bar[I];
+  __shared__ __align__(8) uint64_t fix_bar;  // the owner's copies of the other pieces of its cut tile landed
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t abort_sh;
   __shared__ int npieces_sh;      // pieces of the cut tile the epilogue's segment owns
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       mbar_init(smem_u32(&dfull_bar[d]), I);
       mbar_init(smem_u32(&dempty_bar[d]), 4);
     }
+    mbar_init(smem_u32(&fix_bar), 1);
     abort_sh = 0;
     own_tile_sh = -1;
     fence_mbar_init();
@@ -488,6 +490,28 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       const bool landed = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err, p.wait_limit);
       if (!named_bar_and(1, 128, ok && landed)) break;  // (also publishes npieces_sh)
       tc_fence_after();
+      // Up to three pieces: the owner's segment is the CTA's last, so once its accumulators landed
+      // every stage of the CTA has gone through its MMAs and the stage ring is idle; the other pieces
+      // are copied into it at once (one round trip, instead of one per 16 columns when read from the
+      // epilogue's loop). Four or more go through the shared fixup below.
+      constexpr uint32_t kPieceBytes = C::kTP * BN * kTN * 4;
+      const int np = owner ? npieces_sh : 1;
+      const bool ring_fix = np > 1 && np < 4 && (np - 1) * kPieceBytes <= S * C::kStageBytes;
+      if (ring_fix) {
+        if (r == 0) {
+          fence_proxy_async_global();  // the pieces' stores, acquired by the counter wait, before the copies
+          mbar_arrive_expect_tx(smem_u32(&fix_bar), (np - 1) * kPieceBytes);
+          const uint64_t pol = policy_evict_first();
+          for (int pc = 1; pc < np; ++pc)
+            bulk_g2s(smem_base + (pc - 1) * kPieceBytes, piece_of<BN, C::kTP>(p, cta + pc, 0), kPieceBytes,
+                     smem_u32(&fix_bar), pol);
+        }
+        if (!warp_wait(smem_u32(&fix_bar), 0, abort_flag, p.err, p.wait_limit)) {
+          if (r == 0) drain_wait(smem_u32(&fix_bar), 0);  // no copy in flight when the CTA leaves
+          break;
+        }
+      }
+      const float *fixed = reinterpret_cast<const float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
       // With four or more pieces the owner's own sums go to shared memory (the stage ring is idle:
       // every MMA is done), where all dequant and epilogue warps add the other pieces below; with
       // fewer the epilogue adds them itself (measured on the 7B decode shapes: the extra barrier and
@@ -503,23 +527,42 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
         for (int c0 = 0; c0 < BN && m0 + c0 < m_end; c0 += 16) {
           uint32_t v[16];
           const uint32_t dbase = tmem + lane_addr + (db * I + te) * C::kDStride + c0;
+          // the MMA warps' partial sums, added in a fixed order; two loads per wait
+          uint32_t v2[16];
           tmem_ld_32x32b_x16(dbase, v);
+          if (nparts > 1) tmem_ld_32x32b_x16(dbase + C::kDStride, v2);
           tmem_wait_ld();
           float f[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q) f[q] = __uint_as_float(v[q]);
+          if (nparts > 1) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) f[q] += __uint_as_float(v2[q]);
+          }
 #pragma unroll 1
-          for (int e = 1; e < nparts; ++e) {  // the MMA warps' partial sums, in a fixed order
+          for (int e = 2; e < nparts; e += 2) {
             tmem_ld_32x32b_x16(dbase + e * C::kDStride, v);
+            if (e + 1 < nparts) tmem_ld_32x32b_x16(dbase + (e + 1) * C::kDStride, v2);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 16; ++q) f[q] += __uint_as_float(v[q]);
+            if (e + 1 < nparts) {
+#pragma unroll
+              for (int q = 0; q < 16; ++q) f[q] += __uint_as_float(v2[q]);
+            }
           }
           if (shared_fix) {
 #pragma unroll
             for (int q = 0; q < 16; ++q) own[(te * BN + c0 + q) * kTN + r] = f[q];
           } else {
-            if (owner) {  // the epilogue adds the later pieces in K order
+            if (ring_fix) {  // the later pieces in K order, from their copies in the ring
+#pragma unroll 1
+              for (int pc = 1; pc < np; ++pc) {
+                const float *src = fixed + (pc - 1) * (kPieceBytes / 4) + (te * BN + c0) * kTN + r;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) f[q] += src[q * kTN];
+              }
+            } else if (owner) {  // the epilogue adds the later pieces in K order
 #pragma unroll 1
               for (int pc = 1; pc < npieces_sh; ++pc) {
                 const float *src = piece_of<BN, C::kTP>(p, cta + pc, 0) + (te * BN + c0) * kTN + r;

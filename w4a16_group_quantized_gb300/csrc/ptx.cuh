@@ -269,6 +269,10 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   return p;
 }
 
+// Orders this thread's view of global memory (including writes of other threads it has acquired)
+// before its subsequent async-proxy (bulk copy) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
