@@ -73,8 +73,8 @@ def test_noalloc_matches_oracle(M, N, K, g):
 
 def test_noalloc_refuses_problems_larger_than_its_array():
     fn = _noalloc_fn()
-    # 128 tokens on a 4096 x 4096 layer: two token tiles of 64 and stream-K, whose fp32 partial
-    # tiles (two per CTA) need about 9.7 MB of scratch, more than the array holds
+    # 128 tokens on a 4096 x 4096 layer: two token tiles of 64, each tile cut between two CTAs, whose
+    # fp32 partial tiles (two per CTA, 128 CTAs) need a little over the 8 MiB the array holds
     N, K, g, M = 4096, 4096, 128, 128
     assert w4.w4a16_workspace_bytes(M, N, K, g) > SCRATCH_BYTES
     packed = torch.zeros(w4.w4_repacked_bytes(N, K, g), dtype=torch.uint8, device="cuda")

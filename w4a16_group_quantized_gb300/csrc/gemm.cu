@@ -490,13 +490,13 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       const bool landed = warp_wait(smem_u32(&dfull_bar[db]), (seg / C::kDBufs) & 1, abort_flag, p.err, p.wait_limit);
       if (!named_bar_and(1, 128, ok && landed)) break;  // (also publishes npieces_sh)
       tc_fence_after();
-      // Up to three pieces: the owner's segment is the CTA's last, so once its accumulators landed
-      // every stage of the CTA has gone through its MMAs and the stage ring is idle; the other pieces
-      // are copied into it at once (one round trip, instead of one per 16 columns when read from the
-      // epilogue's loop). Four or more go through the shared fixup below.
+      // The owner's segment is the CTA's last, so once its accumulators landed every stage of the CTA
+      // has gone through its MMAs and the stage ring is idle: the other pieces are copied into it at
+      // once when they fit (one round trip, instead of one per 16 columns when read from the
+      // epilogue's loop); else four or more go through the shared fixup below.
       constexpr uint32_t kPieceBytes = C::kTP * BN * kTN * 4;
       const int np = owner ? npieces_sh : 1;
-      const bool ring_fix = np > 1 && np < 4 && (np - 1) * kPieceBytes <= S * C::kStageBytes;
+      const bool ring_fix = np > 1 && (np - 1) * kPieceBytes <= S * C::kStageBytes;
       if (ring_fix) {
         if (r == 0) {
           fence_proxy_async_global();  // the pieces' stores, acquired by the counter wait, before the copies
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       // every MMA is done), where all dequant and epilogue warps add the other pieces below; with
       // fewer the epilogue adds them itself (measured on the 7B decode shapes: the extra barrier and
       // round trip through shared memory cost more than the wider reduction saves below four).
-      const bool shared_fix = kOwnInSmem && owner && npieces_sh >= 4;
+      const bool shared_fix = kOwnInSmem && owner && npieces_sh >= 4 && !ring_fix;
       float *own = reinterpret_cast<float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
 #pragma unroll 1
       for (int te = 0; te < C::kTP; ++te) {
@@ -745,6 +745,21 @@ cudaError_t launch_t(const CUtensorMap &map, const CUtensorMap &code_map, const 
 // One group per 64-wide K block (g % 64 == 0) lets the dequant take the block's group once.
 int gemm_mode(int32_t g) { return g % 64 == 0 ? kScaleIn : kGeneral; }
 
+// Pieces of a cut tile whose owner can take the others into its idle stage ring at once (the
+// epilogue's fast fixup): 1 + ring bytes / piece bytes.
+template <int BN, int MODE, int TP>
+constexpr int64_t ring_piece_cap_t() {
+  using C = Cfg<BN, MODE, TP>;
+  return 1 + static_cast<int64_t>(C::kStages) * C::kStageBytes / (static_cast<int64_t>(TP) * BN * kTN * 4);
+}
+int64_t ring_piece_cap(int bn, int tp, int mode) {
+  const bool s = mode == kScaleIn;
+  if (bn == 64) return s ? ring_piece_cap_t<64, kScaleIn, 1>() : ring_piece_cap_t<64, kGeneral, 1>();
+  if (bn == 128 && tp == 2) return s ? ring_piece_cap_t<128, kScaleIn, 2>() : ring_piece_cap_t<128, kGeneral, 2>();
+  if (bn == 128) return s ? ring_piece_cap_t<128, kScaleIn, 1>() : ring_piece_cap_t<128, kGeneral, 1>();
+  return 1;
+}
+
 template <int DT>
 cudaError_t launch_variant(int bn, int mode, int tp, const CUtensorMap &map, const CUtensorMap &code_map,
                            const CUtensorMap &rec_map, const Params &p, int ctas, cudaStream_t stream) {
@@ -834,18 +849,16 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOption
   const int64_t units = tiles * ks;
   if (tiles > 0x7FFFFFFF || units > (int64_t{1} << 40)) return false;
   int64_t P = ctas > 0 ? ctas : (num_sms > 0 ? num_sms : 148);
-  // Fewer output tiles than SMs (64- or 128-token tiles): cut each tile into about KS / 8 pieces, as
-  // many as the SMs allow, instead of spreading all stages over every SM; one piece means whole tiles.
-  // Kept to whole tiles or tiles of at most 64 stages: long tiles gain from every SM. Measured on the
-  // 7B layers (M = 64..128: qkv 18% faster as whole tiles, o_proj 10-15% in 2 pieces, down_proj 5% in
-  // 2 pieces at M = 128) and the 70B layers (M = 256..512: o_proj 19-24% faster, down_proj 4%, qkv 4%).
+  // Fewer output tiles than SMs (64- or 128-token tiles): cut each tile into equal pieces, as many as
+  // the SMs allow and the owner can take into its stage ring at once, instead of spreading all stages
+  // over every SM; one piece means whole tiles. Measured on the 7B layers (M = 64: o_proj 10% faster
+  // in 4 pieces, down_proj 16%; M = 64..128 qkv 18% faster as whole tiles) and the 70B layers
+  // (M = 256: down_proj 14% faster in 2 pieces, o_proj 30%; qkv 8% as whole tiles).
   bool fewer = false;
   if (ctas == 0 && schedule == 0 && bn >= 64 && tiles < P) {
-    const int64_t pieces = std::max<int64_t>(1, std::min<int64_t>((ks + 7) / 8, P / tiles));
-    if (pieces == 1 || ks <= 64) {
-      P = tiles * pieces;
-      fewer = pieces == 1;
-    }
+    const int64_t pieces = std::max<int64_t>(1, std::min<int64_t>(P / tiles, ring_piece_cap(bn, tp, gemm_mode(g))));
+    P = tiles * pieces;
+    fewer = pieces == 1;
   }
   // whole-tile scheduling when every CTA gets many tiles (imbalance <= 1/8) or the tiles divide
   // evenly; otherwise stream-K over 256-wide K stages, which needs the partial-tile fixup
