@@ -491,26 +491,18 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       if (!named_bar_and(1, 128, ok && landed)) break;  // (also publishes npieces_sh)
       tc_fence_after();
       // The owner's segment is the CTA's last, so once its accumulators landed every stage of the CTA
-      // has gone through its MMAs and the stage ring is idle: the other pieces are copied into it at
-      // once when they fit (one round trip, instead of one per 16 columns when read from the
-      // epilogue's loop); else four or more go through the shared fixup below.
-      constexpr uint32_t kPieceBytes = C::kTP * BN * kTN * 4;
+      // has gone through its MMAs and the stage ring is idle: the other pieces are copied into it (one
+      // round trip, instead of one per 16 columns when read from the epilogue's loop), all at once when
+      // they fit, else (two-tile units) one weight tile's part of every piece at a time; beyond that,
+      // four or more go through the shared fixup below.
+      constexpr uint32_t kPartBytes = BN * kTN * 4;  // one weight tile of a piece
+      constexpr uint32_t kPieceBytes = C::kTP * kPartBytes;
       const int np = owner ? npieces_sh : 1;
-      const bool ring_fix = np > 1 && (np - 1) * kPieceBytes <= S * C::kStageBytes;
-      if (ring_fix) {
-        if (r == 0) {
-          fence_proxy_async_global();  // the pieces' stores, acquired by the counter wait, before the copies
-          mbar_arrive_expect_tx(smem_u32(&fix_bar), (np - 1) * kPieceBytes);
-          const uint64_t pol = policy_evict_first();
-          for (int pc = 1; pc < np; ++pc)
-            bulk_g2s(smem_base + (pc - 1) * kPieceBytes, piece_of<BN, C::kTP>(p, cta + pc, 0), kPieceBytes,
-                     smem_u32(&fix_bar), pol);
-        }
-        if (!warp_wait(smem_u32(&fix_bar), 0, abort_flag, p.err, p.wait_limit)) {
-          if (r == 0) drain_wait(smem_u32(&fix_bar), 0);  // no copy in flight when the CTA leaves
-          break;
-        }
-      }
+      const bool ring_all = np > 1 && (np - 1) * kPieceBytes <= S * C::kStageBytes;
+      const bool ring_part = !ring_all && C::kTP == 2 && np > 1 && (np - 1) * kPartBytes <= S * C::kStageBytes;
+      const bool ring_fix = ring_all || ring_part;
+      const uint32_t ring_stride = ring_all ? kPieceBytes : kPartBytes;  // bytes between pieces in the ring
+      bool fix_ok = true;
       const float *fixed = reinterpret_cast<const float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
       // With four or more pieces the owner's own sums go to shared memory (the stage ring is idle:
       // every MMA is done), where all dequant and epilogue warps add the other pieces below; with
@@ -520,6 +512,28 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
       float *own = reinterpret_cast<float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
 #pragma unroll 1
       for (int te = 0; te < C::kTP; ++te) {
+        if (ring_fix && (te == 0 || ring_part)) {
+          // every warp takes part in each round (no warp leaves the loop early): the barrier orders the
+          // previous round's reads of the ring before its next copies
+          if (te > 0) fix_ok = named_bar_and(1, 128, fix_ok);
+          if (fix_ok) {
+            if (r == 0) {
+              // the pieces' stores (acquired by the counter wait) and the ring's earlier reads before the copies
+              fence_proxy_async_global();
+              fence_proxy_async_shared();
+              const uint32_t bytes = ring_all ? kPieceBytes : kPartBytes;
+              mbar_arrive_expect_tx(smem_u32(&fix_bar), (np - 1) * bytes);
+              const uint64_t pol = policy_evict_first();
+              for (int pc = 1; pc < np; ++pc)
+                bulk_g2s(smem_base + (pc - 1) * ring_stride,
+                         piece_of<BN, C::kTP>(p, cta + pc, 0) + (ring_all ? 0 : te * BN * kTN), bytes,
+                         smem_u32(&fix_bar), pol);
+            }
+            fix_ok = warp_wait(smem_u32(&fix_bar), te & 1, abort_flag, p.err, p.wait_limit);
+            if (!fix_ok && r == 0) drain_wait(smem_u32(&fix_bar), te & 1);  // no copy in flight when the CTA leaves
+          }
+        }
+        if (!fix_ok) continue;
         const int n = (t * C::kTP + te) * kTN + r;
         float *piece =
             p.pieces + ((static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * C::kTP + te) * BN * kTN + r;
@@ -558,7 +572,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
             if (ring_fix) {  // the later pieces in K order, from their copies in the ring
 #pragma unroll 1
               for (int pc = 1; pc < np; ++pc) {
-                const float *src = fixed + (pc - 1) * (kPieceBytes / 4) + (te * BN + c0) * kTN + r;
+                const float *src = fixed + (pc - 1) * (ring_stride / 4) + ((ring_all ? te * BN : 0) + c0) * kTN + r;
 #pragma unroll
                 for (int q = 0; q < 16; ++q) f[q] += src[q * kTN];
               }
@@ -854,11 +868,16 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOption
   // over every SM; one piece means whole tiles. Measured on the 7B layers (M = 64: o_proj 10% faster
   // in 4 pieces, down_proj 16%; M = 64..128 qkv 18% faster as whole tiles) and the 70B layers
   // (M = 256: down_proj 14% faster in 2 pieces, o_proj 30%; qkv 8% as whole tiles).
+  // Units of two weight tiles go stream-K over every SM instead, unless whole tiles keep at least 4/5 of
+  // the SMs busy (70B layers: qkv M = 256 20% faster than whole tiles, down_proj M = 256 6% faster than
+  // 2 pieces; o_proj M = 512 3% slower than whole tiles).
   bool fewer = false;
   if (ctas == 0 && schedule == 0 && bn >= 64 && tiles < P) {
     const int64_t pieces = std::max<int64_t>(1, std::min<int64_t>(P / tiles, ring_piece_cap(bn, tp, gemm_mode(g))));
-    P = tiles * pieces;
-    fewer = pieces == 1;
+    if (tp == 1 || tiles * 5 >= P * 4) {
+      P = tp == 1 ? tiles * pieces : tiles;
+      fewer = tp == 2 || pieces == 1;
+    }
   }
   // whole-tile scheduling when every CTA gets many tiles (imbalance <= 1/8) or the tiles divide
   // evenly; otherwise stream-K over 256-wide K stages, which needs the partial-tile fixup

@@ -272,6 +272,9 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
 // Orders this thread's view of global memory (including writes of other threads it has acquired)
 // before its subsequent async-proxy (bulk copy) reads of global memory.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Orders this thread's (and, after a barrier, the CTA's) generic accesses to shared memory before
+// subsequent async-proxy (bulk copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
