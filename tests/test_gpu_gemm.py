@@ -127,6 +127,26 @@ def test_two_tile_units(M, N, K, g, ctas, schedule):
 
 
 @pytest.mark.parametrize("M,N,K,g,block_n,ctas", [
+    (64, 256, 4096, 128, 64, 10),    # one-tile units, 5 pieces per tile: copied into the owner's ring at once
+    (64, 256, 4096, 128, 64, 14),    # 7 pieces: the ring's capacity for 32 KB pieces
+    (64, 256, 4096, 128, 64, 16),    # 8 pieces: more than the ring holds, the shared fixup
+    (200, 256, 4096, 128, 128, 8),   # block_n 128 (64 KB pieces), 2 pieces: ring
+    (200, 256, 4096, 128, 128, 12),  # 3 pieces: ring at capacity
+    (200, 256, 4096, 128, 128, 20),  # 5 pieces: shared fixup
+    (256, 512, 4096, 128, 128, 8),   # two-tile units (128 KB pieces), 2 pieces: ring
+    (256, 512, 4096, 128, 128, 12),  # 3 pieces: one weight tile's part of every piece at a time
+    (256, 512, 4096, 128, 128, 16),  # 4 pieces: one weight tile at a time, at capacity
+    (256, 512, 4096, 128, 128, 20),  # 5 pieces: shared fixup
+    (256, 512, 4000, 40, 128, 8),    # g = 40 (two-stage ring), 2 pieces: one weight tile at a time
+    (256, 512, 4000, 40, 128, 12),   # 3 pieces: read from L2 in the epilogue's loop
+])
+def test_cut_tile_fixups(M, N, K, g, block_n, ctas):
+    # stream-K forced over few CTAs, so that every tile is cut into the stated number of pieces and the
+    # owner takes each way of adding them; the sums must match the oracle like any other schedule
+    check(M, N, K, g, block_n=block_n, ctas=ctas, schedule=1, rows=_sample_rows(M, 16))
+
+
+@pytest.mark.parametrize("M,N,K,g,block_n,ctas", [
     (300, 1000, 1024, 128, 64, 7),  # 5 token tiles x 8 weight tiles over 7 CTAs: uneven tile counts
     (512, 700, 960, 128, 128, 5),   # two-tile units, a ragged pair, a one-block last stage
     (100, 300, 520, 40, 32, 3),     # per-word group lookup
