@@ -364,7 +364,8 @@ W4_API int w4_last_device_error(void *workspace_dev, void *stream);
  *    W4A16_NOALLOC_SCRATCH_BYTES. For example, on GB300 (152 SMs) a layer
  *    of N <= 10^6 rows fits for every M <= 32 (at most 4.8 MB of partial
  *    tiles plus 4 bytes per output tile), while M = 64 on a 4096 x 4096
- *    layer needs 9.5 MB and is refused.
+ *    layer (32 tiles, each cut between 4 of 128 CTAs) needs 8.4 MB and is
+ *    refused.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture begins.
