@@ -312,7 +312,11 @@ typedef struct {
  * tail cost of a launch per GEMM (the bigcode-inference-benchmark roadmap,
  * issue #11, names that cost for many small GEMMs). Problems that share x
  * and K (q, k and v of one layer; gate and up) keep x in shared memory
- * across problems. Otherwise the problems run one launch each, in order.
+ * across problems. Above the decode kernel's range, up to 8 problems that
+ * share x (the same pointer) and K run in one tensor-memory launch over all
+ * their weight tiles (scheduled as one GEMM of the tiles laid one after
+ * another, one-tile units; two-tile units from M = 256 do not group).
+ * Otherwise the problems run one launch each, in order.
  * Outputs must not overlap one another or any input. The workspace must be
  * at least w4a16_grouped_workspace_bytes(...) bytes, 256-byte aligned and
  * zeroed before first use, like w4a16_gemm's.

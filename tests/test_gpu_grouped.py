@@ -206,6 +206,36 @@ def test_group_above_decode_m_runs_one_launch_each():
     run_group(32, LAYER_7B[:3] + [(22016, 4096, 5, 2, "silu")])
 
 
+@pytest.mark.parametrize("M", [32, 64, 128, 200])
+def test_group_sharing_x_runs_one_tensor_memory_launch(M):
+    # q, k, v of one x above the decode kernel's range: one tensor-memory launch over their weight tiles
+    run_group(M, LAYER_7B[:3])
+
+
+@pytest.mark.parametrize("M", [24, 64])
+def test_tensor_memory_group_with_epilogues(M):
+    # a q/k/v split, a silu * up problem and a plain one on one x, each through its own epilogue
+    run_group(M, [(12288, 4096, 1, 0, "qkv"), (22016, 4096, 3, 0, "silu"), (4096, 4096, 2, 0, "y")])
+
+
+@pytest.mark.parametrize("opts", [dict(kernel=2, block_n=32, ctas=7, schedule=1),
+                                  dict(kernel=2, block_n=64, ctas=5, schedule=1),
+                                  dict(kernel=2, block_n=16, ctas=3, schedule=2),
+                                  dict(kernel=2, block_n=128, ctas=0, schedule=0)],
+                         ids=["bn32-streamk7", "bn64-streamk5", "bn16-whole3", "bn128-auto"])
+@pytest.mark.parametrize("K,g", [(1024, 128), (1032, 40)])
+def test_tensor_memory_group_ragged(opts, K, g):
+    # ragged problems (partial last weight tiles) whose tiles follow one another; stream-K ranges that
+    # cut tiles and cross from one problem into the next; g = 40 looks groups up per 8 codes, K = 1032
+    # has a short last stage
+    run_group(40, [(1000, K, 1, 0, "y"), (300, K, 2, 0, "y"), (130, K, 3, 0, "y"), (258, K, 4, 0, "silu")],
+              g=g, **opts)
+
+
+def test_tensor_memory_group_bf16():
+    run_group(64, LAYER_7B[:3] + [(11008, 4096, 5, 0, "y")], dtype="bf16")
+
+
 def test_group_rejects_bad_epilogues_on_host():
     _, _, _, packed, _ = layer(1000, 1024, 128)
     x = torch.zeros((2, 1024), dtype=torch.float16, device="cuda")

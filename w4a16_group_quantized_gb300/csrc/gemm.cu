@@ -107,10 +107,12 @@ struct Cfg {
 // segment: to y (fp16, rounded once) for a whole tile, else to the CTA's fp32 piece, which is laid
 // out column by column ([BN][128]) so that a warp's 32 rows make one 128-byte line per column.
 template <int BN, int DT>
-__device__ __forceinline__ void emit16(const Params &p, bool whole, int n, int m0, int m_end, int c0,
+__device__ __forceinline__ void emit16(const Params &p, int pi, bool whole, int n, int m0, int m_end, int c0,
                                        const float (&v)[16], float *piece) {
   if (whole) {
-    if (p.epi.kind == kEpiSiluMul) {
+    const Epi &epi = prob_epi(p, pi);
+    const int N = prob_n(p, pi);
+    if (epi.kind == kEpiSiluMul) {
       // rows n & ~1 (even lane: gate) and n | 1 (odd lane: up) of 16 tokens: the pair swaps values and
       // splits the tokens, the even lane writes silu(gate) * up of tokens 0..7, the odd lane of 8..15
       const bool odd = n & 1;
@@ -126,17 +128,17 @@ __device__ __forceinline__ void emit16(const Params &p, bool whole, int n, int m
           up[e - 8] = v[e];
         }
       }
-      if (n < p.N) {
-        uint16_t *dst = p.y + n / 2;
+      if (n < N) {
+        uint16_t *dst = prob_y(p, pi) + n / 2;
         const int e0 = odd ? 8 : 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e)
           if (m0 + c0 + e0 + e < m_end)
-            dst[static_cast<int64_t>(m0 + c0 + e0 + e) * p.epi.ld] = out_bits<DT>(silu_mul(gate[e], up[e]));
+            dst[static_cast<int64_t>(m0 + c0 + e0 + e) * epi.ld] = out_bits<DT>(silu_mul(gate[e], up[e]));
       }
-    } else if (n < p.N) {
+    } else if (n < N) {
       int ld;
-      uint16_t *dst = epi_row(p.epi, p.y, n, &ld);
+      uint16_t *dst = epi_row(epi, prob_y(p, pi), n, &ld);
 #pragma unroll
       for (int e = 0; e < 16; ++e)
         if (m0 + c0 + e < m_end) dst[static_cast<int64_t>(m0 + c0 + e) * ld] = out_bits<DT>(v[e]);
@@ -224,7 +226,7 @@ __device__ __forceinline__ void produce_stages_pair(const CUtensorMap *x_map, co
 template <int BN, int MODE, int TP, int DT>
 __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap code_map,
-                      const __grid_constant__ CUtensorMap rec_map, const Params p) {
+                      const __grid_constant__ CUtensorMap rec_map, const __grid_constant__ Params p) {
   using C = Cfg<BN, MODE, TP>;
   constexpr int S = C::kStages;
   // the owner of a cut tile parks its sums ([kTP][BN][128] fp32) in the idle stage ring
@@ -534,7 +536,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
           }
         }
         if (!fix_ok) continue;
-        const int n = (t * C::kTP + te) * kTN + r;
+        const TileOut out = tile_out(p, t * C::kTP + te);
+        const int n = out.row0 + r;  // the row within its problem
         float *piece =
             p.pieces + ((static_cast<int64_t>(cta) * 2 + (seg == 0 ? 0 : 1)) * C::kTP + te) * BN * kTN + r;
 #pragma unroll 1
@@ -584,7 +587,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
                 for (int q = 0; q < 16; ++q) f[q] += __ldcg(src + q * kTN);
               }
             }
-            emit16<BN, DT>(p, whole || owner, n, m0, m_end, c0, f, piece);
+            emit16<BN, DT>(p, out.pi, whole || owner, n, m0, m_end, c0, f, piece);
           }
         }
       }
@@ -613,14 +616,15 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
     if (tile >= 0) {
       const float *own = reinterpret_cast<const float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
       const int npieces = npieces_sh;
-      const int n0 = (tile / p.MT) * C::kTP * kTN;
       const int m0 = (tile % p.MT) * BN;
       const int ncols = min(p.M, m0 + BN) - m0;
       const int tid = static_cast<int>(threadIdx.x) - 32 * C::kDqWarp0;
-      // silu * up takes rows in (gate, up) pairs
-      const int step = p.epi.kind == kEpiSiluMul ? 2 : 1;
 #pragma unroll
       for (int te = 0; te < C::kTP; ++te) {
+        const TileOut out = tile_out(p, (tile / p.MT) * C::kTP + te);
+        const Epi &epi = prob_epi(p, out.pi);
+        // silu * up takes rows in (gate, up) pairs
+        const int step = epi.kind == kEpiSiluMul ? 2 : 1;
 #pragma unroll 2
         for (int e = tid * step; e < ncols * kTN; e += kFixThreads * step) {
           const int o = te * BN * kTN + e;
@@ -628,18 +632,18 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, TP>::kThreads, 1)
 #pragma unroll
           for (int pc = 1; pc < kMaxPieces; ++pc)
             if (pc < npieces) acc += __ldcg(piece_of<BN, C::kTP>(p, cta + pc, 0) + o);
-          const int n = n0 + te * kTN + e % kTN;
+          const int n = out.row0 + e % kTN;  // the row within its problem
           const int64_t m = m0 + e / kTN;
-          if (n >= p.N) continue;
+          if (n >= prob_n(p, out.pi)) continue;
           if (step == 2) {
             float up = own[o + 1];
 #pragma unroll
             for (int pc = 1; pc < kMaxPieces; ++pc)
               if (pc < npieces) up += __ldcg(piece_of<BN, C::kTP>(p, cta + pc, 0) + o + 1);
-            p.y[m * p.epi.ld + n / 2] = out_bits<DT>(silu_mul(acc, up));
+            prob_y(p, out.pi)[m * epi.ld + n / 2] = out_bits<DT>(silu_mul(acc, up));
           } else {
             int ld;
-            uint16_t *dst = epi_row(p.epi, p.y, n, &ld);
+            uint16_t *dst = epi_row(epi, prob_y(p, out.pi), n, &ld);
             dst[m * ld] = out_bits<DT>(acc);
           }
         }
@@ -986,18 +990,13 @@ DecParams dec_params(int64_t M, int32_t g, void *workspace, const GemmOptions &o
 
 }  // namespace
 
-cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y,
-                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, const EpiSpec &epi,
-                        cudaStream_t stream, bool *encode_failed) {
-  *encode_failed = false;
+// The tensor-memory launch of a validated plan over x [M, K]: builds the tensor maps and the schedule
+// fields of p; the caller has filled the problem fields (codes, meta, y, N, epi and nprob, or the
+// problem table). `packed` is the single problem's weights (two-tile units read them by tensor maps).
+cudaError_t launch_tmem(const void *x, const void *packed, int64_t M, int64_t K, int32_t g, void *workspace,
+                        const GemmPlan &plan, const GemmOptions &opt, Params &p, cudaStream_t stream,
+                        bool *encode_failed) {
   CUtensorMap map;
-  if (plan.kernel == kKernelDecode) {
-    DecParams p = dec_params(M, g, workspace, opt);
-    p.prob[0] = dec_problem(x, packed, y, N, K, g, epi, 0);
-    p.nprob = 1;
-    p.tiles = p.prob[0].NT;
-    return launch_gemm_dec(p, plan.block_n / 8, opt.dtype, plan.ctas, plan.cluster, stream);
-  }
   const int sbk = kSB / plan.tiles_per_unit;
   bool x3d = K % kTK == 0 && make_x_map(&map, x, M, K, plan.block_n, sbk, true, opt.dtype);
   if (!x3d && !make_x_map(&map, x, M, K, plan.block_n, sbk, false, opt.dtype)) {
@@ -1015,15 +1014,10 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
     }
   }
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  Params p;
-  p.codes = static_cast<const uint8_t *>(packed);
-  p.meta = p.codes + static_cast<int64_t>(plan.n_tiles) * plan.k_blocks * kTileBytes;
-  p.y = static_cast<uint16_t *>(y);
   p.pieces = reinterpret_cast<float *>(ws + plan.pieces_offset);
   p.counters = reinterpret_cast<uint32_t *>(ws + plan.counters_offset);
   p.err = reinterpret_cast<uint32_t *>(ws);
   p.M = static_cast<int>(M);
-  p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.g = g;
   p.gdiv = make_fastdiv(static_cast<uint32_t>(g));
@@ -1039,12 +1033,33 @@ cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N,
   p.grains = plan.grains;
   p.wait_limit = opt.wait_limit ? opt.wait_limit : kWaitLimitCycles;
   p.test_extra_piece = opt.test_timeout ? 1 : 0;
-  p.epi = make_epi(epi, N);
   if (opt.dtype == kDtypeBf16)
     return launch_variant<kDtypeBf16>(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p,
                                       plan.ctas, stream);
   return launch_variant<kDtypeF16>(plan.block_n, gemm_mode(g), plan.tiles_per_unit, map, code_map, rec_map, p,
                                    plan.ctas, stream);
+}
+
+cudaError_t launch_gemm(const void *x, const void *packed, int64_t M, int64_t N, int64_t K, int32_t g, void *y,
+                        void *workspace, const GemmPlan &plan, const GemmOptions &opt, const EpiSpec &epi,
+                        cudaStream_t stream, bool *encode_failed) {
+  *encode_failed = false;
+  if (plan.kernel == kKernelDecode) {
+    DecParams p = dec_params(M, g, workspace, opt);
+    p.prob[0] = dec_problem(x, packed, y, N, K, g, epi, 0);
+    p.nprob = 1;
+    p.tiles = p.prob[0].NT;
+    return launch_gemm_dec(p, plan.block_n / 8, opt.dtype, plan.ctas, plan.cluster, stream);
+  }
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.codes = static_cast<const uint8_t *>(packed);
+  p.meta = p.codes + static_cast<int64_t>(plan.n_tiles) * plan.k_blocks * kTileBytes;
+  p.y = static_cast<uint16_t *>(y);
+  p.N = static_cast<int>(N);
+  p.epi = make_epi(epi, N);
+  p.nprob = 1;
+  return launch_tmem(x, packed, M, K, g, workspace, plan, opt, p, stream, encode_failed);
 }
 
 
@@ -1075,6 +1090,21 @@ bool make_group_plan(const GemmProblem *probs, int count, int64_t M, int32_t g, 
     common = common || ok;
   }
   plan->decode = all_dec && common;
+  if (plan->decode || count > kTmemGroupMaxHost) return true;
+  // the tensor-memory kernel runs problems of one x and K together when the plan for their weight
+  // tiles laid one after another takes it with one-tile units
+  int64_t tiles = 0;
+  for (int i = 0; i < count; ++i) {
+    if (probs[i].x != probs[0].x || probs[i].K != probs[0].K) return true;
+    tiles += cdiv(probs[i].N, kTN);
+  }
+  GemmPlan pl;
+  if (count > 1 && tiles * kTN <= 0x7FFFFFFF && make_gemm_plan(M, tiles * kTN, probs[0].K, g, opt, num_sms, &pl) &&
+      pl.kernel == kKernelTmem && pl.tiles_per_unit == 1) {
+    plan->tmem = true;
+    plan->tmem_plan = pl;
+    plan->workspace_bytes = pl.workspace_bytes;
+  }
   return true;
 }
 
@@ -1098,6 +1128,28 @@ cudaError_t launch_gemm_grouped(const GemmProblem *probs, int count, int64_t M, 
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+  }
+  if (plan.tmem) {
+    static_assert(kTmemGroupMaxHost == kTmemGroupMax, "group table size");
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.nprob = count;
+    int tiles = 0;
+    for (int i = 0; i < count; ++i) {
+      const GemmProblem &pr = probs[i];
+      const int nt = static_cast<int>(cdiv(pr.N, kTN));
+      p.tile0[i] = tiles;
+      p.gN[i] = static_cast<int>(pr.N);
+      p.gcodes[i] = static_cast<const uint8_t *>(pr.packed);
+      p.gmeta[i] = p.gcodes[i] + static_cast<int64_t>(nt) * plan.tmem_plan.k_blocks * kTileBytes;
+      p.gy[i] = static_cast<uint16_t *>(pr.y);
+      p.gepi[i] = make_epi(pr.epi, pr.N);
+      tiles += nt;
+    }
+    p.tile0[count] = tiles;
+    p.N = tiles * kTN;
+    return launch_tmem(probs[0].x, probs[0].packed, M, probs[0].K, g, workspace, plan.tmem_plan, opt, p, stream,
+                       encode_failed);
   }
   for (int i = 0; i < count; ++i) {
     const GemmProblem &pr = probs[i];

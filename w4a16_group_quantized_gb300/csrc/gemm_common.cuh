@@ -86,8 +86,12 @@ __device__ __forceinline__ float silu_mul(float gate, float up) {
 // (gran = 1: stream-K, any cut; gran = KS: whole tiles only); or, for whole tiles of several token
 // tiles (tstride = P), the tiles c, c + P, c + 2P, ...: the CTAs running at one time then share
 // weight tiles (tile t * MT + mt for consecutive mt), whose re-reads hit L2.
+// Problems of one tensor-memory launch that share x and K (one-tile units only): their weight tiles
+// follow one another in the launch's tile numbering, problem i holding tiles [tile0[i], tile0[i + 1]).
+constexpr int kTmemGroupMax = 8;
+
 struct Params {
-  const uint8_t *codes;  // tile region of the packed weights
+  const uint8_t *codes;  // tile region of the packed weights (nprob == 1)
   const uint8_t *meta;   // group-record region of the packed weights
   uint16_t *y;           // fp16 or bf16 bits
   float *pieces;         // [P][2][BN][128] fp32 partial tiles (first and last segment of each CTA)
@@ -103,7 +107,54 @@ struct Params {
   uint64_t wait_limit;   // cycles a wait may take before the kernel gives up
   int test_extra_piece;  // test only: owners wait for this many pieces more than will come
   Epi epi;               // where the sums go (y: q for kEpiQkv, h for kEpiSiluMul)
+  // nprob > 1: the problems of a grouped launch (codes, meta, y, N and epi above are unused)
+  int nprob;
+  int tile0[kTmemGroupMax + 1];
+  int gN[kTmemGroupMax];
+  const uint8_t *gcodes[kTmemGroupMax];
+  const uint8_t *gmeta[kTmemGroupMax];
+  uint16_t *gy[kTmemGroupMax];
+  Epi gepi[kTmemGroupMax];
 };
+
+// The problem holding weight tile t (0 for a single problem).
+__device__ __forceinline__ int tile_problem(const Params &p, int t) {
+  int i = 0;
+  for (int j = 1; j < p.nprob; ++j) i += t >= p.tile0[j] ? 1 : 0;
+  return i;
+}
+
+// Weight tile t's problem: its packed weights and the tile's index within them.
+__device__ __forceinline__ void tile_weights(const Params &p, int t, const uint8_t **codes, const uint8_t **meta,
+                                             int *local_t) {
+  if (p.nprob <= 1) {
+    *codes = p.codes;
+    *meta = p.meta;
+    *local_t = t;
+    return;
+  }
+  const int i = tile_problem(p, t);
+  *codes = p.gcodes[i];
+  *meta = p.gmeta[i];
+  *local_t = t - p.tile0[i];
+}
+
+// Where the rows of weight tile t go: its problem (read its output, N and epilogue with the accessors
+// below, from the kernel parameters where they are used) and the tile's first row within it.
+struct TileOut {
+  int pi;
+  int row0;
+};
+
+__device__ __forceinline__ TileOut tile_out(const Params &p, int t) {
+  if (p.nprob <= 1) return TileOut{0, t * kTN};
+  const int i = tile_problem(p, t);
+  return TileOut{i, (t - p.tile0[i]) * kTN};
+}
+
+__device__ __forceinline__ uint16_t *prob_y(const Params &p, int pi) { return p.nprob <= 1 ? p.y : p.gy[pi]; }
+__device__ __forceinline__ int prob_n(const Params &p, int pi) { return p.nprob <= 1 ? p.N : p.gN[pi]; }
+__device__ __forceinline__ const Epi &prob_epi(const Params &p, int pi) { return p.nprob <= 1 ? p.epi : p.gepi[pi]; }
 
 __device__ __forceinline__ int64_t range_begin(const Params &p, int c) {
   return static_cast<int64_t>(c) * p.grains / p.P * p.gran;
@@ -332,10 +383,13 @@ __device__ __forceinline__ void produce_stages(const CUtensorMap *x_map, const P
     const int n0 = min(nst, min(S, p.KS - f.ks));  // first stages, contiguous within the first tile
     const int kend = min((f.ks + n0) * kStageK, p.K);
     const int blocks = min((f.ks + n0) * kSB, p.KB) - f.ks * kSB;
-    bulk_prefetch_l2(p.codes + (static_cast<int64_t>(f.t) * p.KB + f.ks * kSB) * kTileBytes, blocks * kTileBytes);
+    const uint8_t *codes, *meta;
+    int lt;
+    tile_weights(p, f.t, &codes, &meta, &lt);
+    bulk_prefetch_l2(codes + (static_cast<int64_t>(lt) * p.KB + f.ks * kSB) * kTileBytes, blocks * kTileBytes);
     const int jlo = p.gdiv.div(f.ks * kStageK);
     const int jhi = p.gdiv.div(kend - 1);
-    bulk_prefetch_l2(p.meta + (static_cast<int64_t>(f.t) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
+    bulk_prefetch_l2(meta + (static_cast<int64_t>(lt) * p.G + jlo) * kRecBytes, (jhi - jlo + 1) * kRecBytes);
   }
   griddep_wait();
   StageIter it;
@@ -367,9 +421,12 @@ __device__ __forceinline__ void produce_stages(const CUtensorMap *x_map, const P
       } else {
         for (int b = 0; b < nb; ++b) tma_load_2d(stage + b * kXSub, x_map, k0 + b * kTK, it.mt * BN, bar);
       }
-      bulk_g2s(stage + kXBytes, p.codes + (static_cast<int64_t>(it.t) * p.KB + it.ks * kSB) * kTileBytes,
+      const uint8_t *codes, *meta;
+      int lt;
+      tile_weights(p, it.t, &codes, &meta, &lt);
+      bulk_g2s(stage + kXBytes, codes + (static_cast<int64_t>(lt) * p.KB + it.ks * kSB) * kTileBytes,
                nb * kTileBytes, bar, pol_stream);
-      bulk_g2s(stage + kXBytes + kCodeBytes, p.meta + (static_cast<int64_t>(it.t) * p.G + jlo) * kRecBytes,
+      bulk_g2s(stage + kXBytes + kCodeBytes, meta + (static_cast<int64_t>(lt) * p.G + jlo) * kRecBytes,
                nrec * kRecBytes, bar, pol_stream);
     }
     __syncwarp();

@@ -111,11 +111,16 @@ struct GemmProblem {
 };
 
 // How a group runs: with the decode kernel, all problems in launches of up to kGroupMax problems
-// that walk their weight tiles in one persistent grid; otherwise one launch per problem.
+// that walk their weight tiles in one persistent grid; with the tensor-memory kernel, problems that
+// share x and K (up to kTmemGroupMax, one-tile units) in one launch over all their weight tiles
+// (`tmem_plan`, made for the tiles laid one after another); otherwise one launch per problem.
 constexpr int kGroupMax = 16;
+constexpr int kTmemGroupMaxHost = 8;
 struct GroupPlan {
   bool decode;
+  bool tmem;
   int block_n;            // decode kernel: 8 or 16
+  GemmPlan tmem_plan;
   size_t workspace_bytes;
 };
 
