@@ -76,6 +76,40 @@ def test_workspace_sizes(lib):
     assert w4.w4a16_workspace_bytes_ex(1, 1, 8, 8, 16, 0, 3) == 0  # no schedule 3
 
 
+def _grouped_bytes(lib, M, specs, g=128):
+    """w4a16_grouped_workspace_bytes for problems (x address, N, K); the host only compares and checks
+    the addresses, it never reads through them."""
+    arr = (w4.Problem * len(specs))()
+    for i, (x, N, K) in enumerate(specs):
+        arr[i].x_dev = x
+        arr[i].packed_dev = 0x1000000 * (i + 1)
+        arr[i].y_dev = 0x40000000 + 0x1000000 * i
+        arr[i].N = N
+        arr[i].K = K
+    return int(lib.w4a16_grouped_workspace_bytes(arr, len(specs), M, g, ctypes.byref(w4.Options())))
+
+
+def test_grouped_workspace_follows_the_group_plan(lib):
+    X, X2 = 0x100000, 0x200000
+    ws = w4.w4a16_workspace_bytes
+    # q, k, v of one x above the decode kernel's range: one tensor-memory launch, planned as one GEMM
+    # of their weight tiles laid end to end
+    assert _grouped_bytes(lib, 64, [(X, 4096, 4096)] * 3) == ws(64, 3 * 4096, 4096, 128)
+    # ragged problems count whole weight tiles (8 + 3 here)
+    assert _grouped_bytes(lib, 40, [(X, 1000, 1024), (X, 300, 1024)]) == ws(40, 128 * 11, 1024, 128)
+    # different x, or different K: one launch each, so the largest single workspace
+    assert _grouped_bytes(lib, 64, [(X, 4096, 4096), (X2, 11008, 4096)]) == max(ws(64, 4096, 4096, 128),
+                                                                               ws(64, 11008, 4096, 128))
+    assert _grouped_bytes(lib, 64, [(X, 4096, 4096), (X, 4096, 11008)]) == max(ws(64, 4096, 4096, 128),
+                                                                              ws(64, 4096, 11008, 128))
+    # two-tile units (M >= 256) are not grouped
+    assert _grouped_bytes(lib, 512, [(X, 8192, 8192)] * 2) == ws(512, 8192, 8192, 128)
+    # more than eight problems: one launch each
+    assert _grouped_bytes(lib, 64, [(X, 256, 1024)] * 9) == ws(64, 256, 1024, 128)
+    # the decode range: the decode kernel's 256-byte error block, grouped or not
+    assert _grouped_bytes(lib, 4, [(X, 4096, 4096)] * 3) == 256
+
+
 def test_automatic_block_n(lib):
     # 65..128 tokens: block_n 64 (two token tiles) on layers with fewer 128-row weight tiles than
     # SMs, else 128; the workspace size shows the choice (stream-K, 100 CTAs: two fp32 partial
