@@ -232,6 +232,13 @@ def test_tensor_memory_group_ragged(opts, K, g):
               g=g, **opts)
 
 
+@pytest.mark.parametrize("count", [8, 9])
+def test_tensor_memory_group_size_limit(count):
+    # eight problems of one x fill the launch's problem table; a ninth sends the group back to one
+    # launch per problem
+    run_group(48, [(128 * (1 + i % 3) + 8 * i, 512, 30 + i, 0, "y") for i in range(count)])
+
+
 def test_tensor_memory_group_bf16():
     run_group(64, LAYER_7B[:3] + [(11008, 4096, 5, 0, "y")], dtype="bf16")
 
