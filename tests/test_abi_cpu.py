@@ -102,6 +102,13 @@ def test_grouped_workspace_follows_the_group_plan(lib):
                                                                                ws(64, 11008, 4096, 128))
     assert _grouped_bytes(lib, 64, [(X, 4096, 4096), (X, 4096, 11008)]) == max(ws(64, 4096, 4096, 128),
                                                                               ws(64, 4096, 11008, 128))
+    # the 7B gate/up pair at M = 128: alone, 172 weight tiles would take two-tile units (86 pairs); the
+    # group keeps one launch of one-tile units (stream-K over every SM, one counter per tile, two
+    # partial tiles of 128 x 128 per CTA)
+    sms = 148  # no GPU here: the planner's default SM count
+    one_tile = 256 + 768 + sms * 2 * 128 * 128 * 4
+    assert _grouped_bytes(lib, 128, [(X, 11008, 4096)] * 2) == one_tile
+    assert ws(128, 22016, 4096, 128) != one_tile
     # two-tile units (M >= 256) are not grouped
     assert _grouped_bytes(lib, 512, [(X, 8192, 8192)] * 2) == ws(512, 8192, 8192, 128)
     # more than eight problems: one launch each
@@ -119,10 +126,15 @@ def test_automatic_block_n(lib):
     assert b == 256 + 256 + P * 2 * 128 * 64 * 4
     b = w4.w4a16_workspace_bytes_ex(96, 12288, 4096, 128, 0, P, 1)  # 96 weight tiles
     assert b == 256 + 768 + P * 2 * 128 * 64 * 4  # 2 x 96 counters
-    b = w4.w4a16_workspace_bytes_ex(128, 22016, 4096, 128, 0, P, 1)  # 172 weight tiles
-    assert b == 256 + 768 + P * 2 * 128 * 128 * 4
-    b = w4.w4a16_workspace_bytes_ex(200, 4096, 4096, 128, 0, P, 1)  # more than 128 tokens
+    # 172 weight tiles: block_n 128, in units of two weight tiles (86 pairs, at least 0.4 per SM):
+    # 86 counters, partial tiles of 2 x 128 x 128
+    b = w4.w4a16_workspace_bytes_ex(128, 22016, 4096, 128, 0, P, 1)
+    assert b == 256 + 512 + P * 2 * 2 * 128 * 128 * 4
+    b = w4.w4a16_workspace_bytes_ex(200, 4096, 4096, 128, 0, P, 1)  # more than 128 tokens, 32 tile pairs
     assert b == 256 + 256 + P * 2 * 128 * 128 * 4
+    # 200 tokens on 80 weight tiles: 2 token tiles x 40 pairs = 80 pairs, two-tile units
+    b = w4.w4a16_workspace_bytes_ex(200, 10240, 4096, 128, 0, P, 1)
+    assert b == 256 + 512 + P * 2 * 2 * 128 * 128 * 4
     # the decode kernel (8-token tiles) reduces its split along K in distributed shared memory: its
     # workspace is the error word alone
     assert w4.w4a16_workspace_bytes_ex(8, 4096, 4096, 128, 0, P, 1) == 256

@@ -332,6 +332,14 @@ def test_prefill_layers_sampled(L):
         check(M, L.n, L.k, L.g, rows=_sample_rows(M, 8), outliers=True)
 
 
+@pytest.mark.parametrize("M,N,K", [(80, 22016, 4096), (128, 22016, 4096), (200, 10240, 8192), (255, 8192, 2048)])
+def test_two_tile_units_below_256_tokens(M, N, K):
+    # block_n 128 below 256 tokens takes units of two weight tiles where the tile pairs are many (at
+    # least 0.4 per SM): one token tile (80 rows ragged, 128 full) or two with a ragged second (72 and
+    # 127 rows), stream-K with cut pairs
+    check(M, N, K, 128, rows=_sample_rows(M, 8), outliers=True)
+
+
 @pytest.mark.parametrize("L", [workloads.STACK_LAYER[4], workloads.STACK_HEAD], ids=lambda L: L.name)
 def test_stack_only_layers(L):
     # the decode stack's shapes that the decode sweep does not have: the unfused 11008 x 4096 gate/up

@@ -858,10 +858,16 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOption
   if (bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
   // Units of two weight tiles and 128-wide K stages for block_n 128 from M = 256 up (two or more
-  // token tiles, so each CTA holds long runs of units and a tile pair is cut at most a few times);
-  // below that the pieces of a cut pair (two 64 KB tiles) make the fixup costlier than the x traffic
-  // it saves. Otherwise one tile and 256-wide stages.
-  const int tp = bn == 128 && M >= 256 ? 2 : 1;
+  // token tiles, so each CTA holds long runs of units and a tile pair is cut at most a few times), and
+  // below that where the tile pairs are many (at least 0.4 per SM): a one-tile stage with 128 tokens of
+  // x (82 KB) leaves room for a ring of two, too short to hide the weight stream's latency, a pair
+  // stage (50 KB) for four. Measured at M = 80..224: 22016x4096 4-15% faster, 57344x8192 26-33%,
+  // 28672x8192 22%, 8192x28672 33%, 10240x8192 7%; with 32 pairs (4096-row layers) 40-110% slower, the
+  // fixup of the cut pairs (two 64 KB tiles a piece) costing more than the deeper ring saves.
+  // Otherwise one tile and 256-wide stages.
+  const int64_t pairs = cdiv(M, 128) * cdiv(cdiv(N, kTN), 2);
+  const int sms_tp = num_sms > 0 ? num_sms : 148;
+  const int tp = bn == 128 && (M >= 256 || (!opt.one_tile_mid && 5 * pairs >= 2 * sms_tp)) ? 2 : 1;
   const int64_t mt = cdiv(M, bn), nt = cdiv(N, kTN), kb = cdiv(K, kTK), ks = cdiv(kb, kSB / tp);
   const int64_t tiles = mt * cdiv(nt, tp);  // output tiles of the schedule (units along K: ks each)
   const int64_t units = tiles * ks;
@@ -1092,14 +1098,17 @@ bool make_group_plan(const GemmProblem *probs, int count, int64_t M, int32_t g, 
   plan->decode = all_dec && common;
   if (plan->decode || count > kTmemGroupMaxHost) return true;
   // the tensor-memory kernel runs problems of one x and K together when the plan for their weight
-  // tiles laid one after another takes it with one-tile units
+  // tiles laid one after another takes it with one-tile units (below M = 256 asked for: on the 7B
+  // gate/up pair at M = 65..128 one launch of one-tile units beats a launch per problem)
   int64_t tiles = 0;
   for (int i = 0; i < count; ++i) {
     if (probs[i].x != probs[0].x || probs[i].K != probs[0].K) return true;
     tiles += cdiv(probs[i].N, kTN);
   }
   GemmPlan pl;
-  if (count > 1 && tiles * kTN <= 0x7FFFFFFF && make_gemm_plan(M, tiles * kTN, probs[0].K, g, opt, num_sms, &pl) &&
+  GemmOptions one = opt;
+  one.one_tile_mid = true;
+  if (count > 1 && tiles * kTN <= 0x7FFFFFFF && make_gemm_plan(M, tiles * kTN, probs[0].K, g, one, num_sms, &pl) &&
       pl.kernel == kKernelTmem && pl.tiles_per_unit == 1) {
     plan->tmem = true;
     plan->tmem_plan = pl;

@@ -58,6 +58,7 @@ struct GemmOptions {
   bool test_timeout = false;  // test only: one wait expects more than will come (runs out after wait_limit)
   uint64_t wait_limit = 0;
   int dtype = kDtypeF16;      // x, scales and y
+  bool one_tile_mid = false;  // below M = 256, one-tile units only (the grouped tensor-memory launch takes no others)
 };
 
 struct GemmPlan {
