@@ -130,8 +130,14 @@ def test_automatic_block_n(lib):
     # 86 counters, partial tiles of 2 x 128 x 128
     b = w4.w4a16_workspace_bytes_ex(128, 22016, 4096, 128, 0, P, 1)
     assert b == 256 + 512 + P * 2 * 2 * 128 * 128 * 4
-    b = w4.w4a16_workspace_bytes_ex(200, 4096, 4096, 128, 0, P, 1)  # more than 128 tokens, 32 tile pairs
-    assert b == 256 + 256 + P * 2 * 128 * 128 * 4
+    # 129..192 tokens, and up to 255 on layers of at most 32 weight tiles (K <= 16384): block_n 64 too
+    b = w4.w4a16_workspace_bytes_ex(200, 4096, 4096, 128, 0, P, 1)  # 4 token tiles x 32 weight tiles
+    assert b == 256 + 512 + P * 2 * 128 * 64 * 4
+    b = w4.w4a16_workspace_bytes_ex(160, 8192, 8192, 128, 0, P, 1)  # 3 x 64 output tiles
+    assert b == 256 + 768 + P * 2 * 128 * 64 * 4
+    # ... but K = 28672 keeps block_n 128, in two-tile units (2 token tiles x 32 pairs)
+    b = w4.w4a16_workspace_bytes_ex(160, 8192, 28672, 128, 0, P, 1)
+    assert b == 256 + 256 + P * 2 * 2 * 128 * 128 * 4
     # 200 tokens on 80 weight tiles: 2 token tiles x 40 pairs = 80 pairs, two-tile units
     b = w4.w4a16_workspace_bytes_ex(200, 10240, 4096, 128, 0, P, 1)
     assert b == 256 + 512 + P * 2 * 2 * 128 * 128 * 4

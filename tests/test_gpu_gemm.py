@@ -340,6 +340,12 @@ def test_two_tile_units_below_256_tokens(M, N, K):
     check(M, N, K, 128, rows=_sample_rows(M, 8), outliers=True)
 
 
+@pytest.mark.parametrize("M,N,K", [(160, 8192, 8192), (255, 4096, 4096), (129, 11008, 4096)])
+def test_block_n_64_above_128_tokens(M, N, K):
+    # three or four token tiles of 64 on layers with fewer weight tiles than SMs, the last one ragged
+    check(M, N, K, 128, rows=_sample_rows(M, 8), outliers=True)
+
+
 @pytest.mark.parametrize("L", [workloads.STACK_LAYER[4], workloads.STACK_HEAD], ids=lambda L: L.name)
 def test_stack_only_layers(L):
     # the decode stack's shapes that the decode sweep does not have: the unfused 11008 x 4096 gate/up

@@ -851,9 +851,14 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t g, const GemmOption
     bn = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
     // 65..128 tokens on a layer with fewer 128-row weight tiles than SMs: two token tiles of 64
     // give twice the output tiles (cut less often) at one extra, mostly L2-served, pass over the
-    // weights; measured faster on the 4096- to 12288-row 7B layers, slower on the 22016-row one
+    // weights; measured faster on the 4096- to 12288-row 7B layers, slower on the 22016-row one.
+    // The same holds with three token tiles (129..192 tokens), and with four on layers of at most 32
+    // weight tiles, for K up to 16384 (at M = 129..255: 4096x4096 22% faster, 11008x4096 12-15%,
+    // 8192x8192 8-10%, 10240x8192 0-3%; four token tiles on the 64- to 96-tile layers 9-14% slower,
+    // and 8192x28672 12% slower than two-tile units)
     const int sms = num_sms > 0 ? num_sms : 148;
-    if (bn == 128 && M <= 128 && cdiv(N, kTN) < sms) bn = 64;
+    const int64_t nt_b = cdiv(N, kTN);
+    if (bn == 128 && nt_b < sms && (M <= 128 || (K <= 16384 && (M <= 192 || nt_b <= 32)))) bn = 64;
   }
   if (bn != 16 && bn != 32 && bn != 64 && bn != 128) return false;
   if (ctas < 0 || ctas > 65535 || schedule < 0 || schedule > 2) return false;
