@@ -777,8 +777,6 @@ def run_stack(args):
     for m in workloads.STACK_MS:
         xs = {k: (torch.randn(m, k, device=dev, generator=gen)).to(torch.float16) for k in {L.k for L in layers}}
         ys = [torch.empty((m, L.n), dtype=torch.float16, device=dev) for L in layers]
-        ws = torch.zeros(max(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g) for L in layers), dtype=torch.uint8,
-                         device=dev)
 
         def ours():
             for L, pk, y in zip(layers, packed, ys):
@@ -794,6 +792,12 @@ def run_stack(args):
         groups.append([len(layers) - 1])
         gprobs = [[dict(x=xs[layers[i].k], packed=packed[i], N=layers[i].n, K=layers[i].k, y=ys[i]) for i in grp]
                   for grp in groups]
+
+        # one workspace for every call: the largest single GEMM's, or a grouped launch's (a group of one x
+        # is planned as one GEMM of its weight tiles laid end to end, which may need more)
+        ws_need = max(max(w4.w4a16_workspace_bytes(m, L.n, L.k, L.g) for L in layers),
+                      max(w4.w4a16_grouped_workspace_bytes(pr, 128) for pr in gprobs))
+        ws = torch.zeros(ws_need, dtype=torch.uint8, device=dev)
 
         def ours_grouped():
             for pr in gprobs:
