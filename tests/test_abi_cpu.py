@@ -65,7 +65,7 @@ def test_workspace_sizes(lib):
     M, N, K, P = 16, 300, 1024, 4
     b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 16, P, 1)
     assert b == 256 + 256 + P * 2 * 128 * 16 * 4
-    b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 128, P, 1)  # M < 256: units of one weight tile
+    b = w4.w4a16_workspace_bytes_ex(M, N, K, 128, 128, P, 1)  # M < 256, two tile pairs: units of one weight tile
     assert b == 256 + 256 + P * 2 * 128 * 128 * 4
     b = w4.w4a16_workspace_bytes_ex(256, N, K, 128, 128, P, 1)  # M >= 256: units of two weight tiles
     assert b == 256 + 256 + P * 2 * 2 * 128 * 128 * 4

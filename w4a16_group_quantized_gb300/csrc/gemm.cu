@@ -9,7 +9,8 @@
 // dealt out round-robin (gemm_common.cuh).
 //
 // A stage is four 64-wide K blocks of one tile, or (TP = 2: BN = 128 from
-// M = 256) two K blocks of two weight tiles sharing one x tile: 16 KB of 4-bit
+// M = 256, and below where the tile pairs are many) two K blocks of two weight
+// tiles sharing one x tile: 16 KB of 4-bit
 // codes, the group records they need and the x sub-tiles, moved by three
 // copies (one thread can issue a bulk copy only every ~350 cycles, so copies
 // are made large). Warp roles (one CTA per SM):
