@@ -332,12 +332,14 @@ def test_prefill_layers_sampled(L):
         check(M, L.n, L.k, L.g, rows=_sample_rows(M, 8), outliers=True)
 
 
-@pytest.mark.parametrize("M,N,K", [(80, 22016, 4096), (128, 22016, 4096), (200, 10240, 8192), (255, 8192, 2048)])
-def test_two_tile_units_below_256_tokens(M, N, K):
+@pytest.mark.parametrize("M,N,K,g", [(80, 22016, 4096, 128), (128, 22016, 4096, 128), (200, 10240, 8192, 128),
+                                     (255, 8192, 2048, 128), (100, 19584, 1000, 40), (200, 10240, 1000, 40)])
+def test_two_tile_units_below_256_tokens(M, N, K, g):
     # block_n 128 below 256 tokens takes units of two weight tiles where the tile pairs are many (at
-    # least 0.4 per SM): one token tile (80 rows ragged, 128 full) or two with a ragged second (72 and
-    # 127 rows), stream-K with cut pairs
-    check(M, N, K, 128, rows=_sample_rows(M, 8), outliers=True)
+    # least 0.4 per SM): one token tile (80 and 100 rows ragged, 128 full) or two with a ragged second
+    # (72 and 127 rows), stream-K with cut pairs; g = 40 looks its groups up per 8 codes, and 153
+    # weight tiles (19584 rows) leave the last pair's second tile past N
+    check(M, N, K, g, rows=_sample_rows(M, 8), outliers=True)
 
 
 @pytest.mark.parametrize("M,N,K", [(160, 8192, 8192), (255, 4096, 4096), (129, 11008, 4096)])
